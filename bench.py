@@ -1,0 +1,478 @@
+"""Benchmark of the single-GPU Purlin collective datapath.
+
+Default workload: AllGather bf16, R = 8 rank buffers x 8 Mi elements each
+(16 MiB per rank; each of the 8 outputs holds all 8 contributions, 128 MiB).
+A step is one collective call over inputs already resident in HBM.
+
+Metric: effective HBM GB/s = (bytes every rank buffer must read + bytes every
+rank buffer must write) / device time.  Timing: W warm-up steps, then K
+steps, each bracketed by CUDA events on the library's stream, with an L2
+flush (a 512 MiB write) between steps outside the events; barrier +
+synchronize around the whole timed loop; max over ranks.
+
+Extra keys: ``roofline`` (the throughput kernel against the measured HBM
+copy bandwidth), ``cpu_baseline`` (the CPU oracle on a bounded sample),
+``e2e`` (the same metric with host buffers: pinned H2D of the inputs, the
+call, D2H of every output, all inside the timed region), ``clocks``
+(nvidia-smi samples taken during the timed region).
+
+``--impl reference`` times the CPU oracle instead (the pages publish no
+runnable reference; the oracle is the reference arm).  ``--all`` also runs
+every workload and the latency sweep and writes them to ``--report``.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+L2_FLUSH_BYTES = 512 << 20
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = ["collective_datapath_atom_gb300/csrc/kernels.cu",
+                  "collective_datapath_atom_gb300/csrc/atom.cuh"]
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def recorded_traffic(workload_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    with open(PROFILE_TRAFFIC) as f:
+        d = json.load(f)
+    e = d.get(workload_name)
+    if not e or e.get("kernel_src_sha") != kernel_source_sha():
+        return None
+    return int(e["dram_bytes_per_launch"])
+
+
+# ------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+        time.sleep(0.15)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sms.append(float(parts[0]))
+                maxs.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# --------------------------------------------------------------- setup ----
+
+def setup_workload(name: str, device):
+    """Device inputs/outputs and a closure that runs one call."""
+    import torch
+
+    if name == workloads.AG_BF16_R8_8MI.name:
+        w = workloads.AG_BF16_R8_8MI
+        ins = workloads.inputs_for(w)
+        out_elems = [w.R * w.n] * w.R
+        call = ("all_gather", w.n)
+    elif name == workloads.RS_BF16_R8_128MI.name:
+        w = workloads.RS_BF16_R8_128MI
+        ins = workloads.inputs_for(w)
+        out_elems = [w.n // w.R] * w.R
+        call = ("reduce_scatter", w.n)
+    elif name == workloads.A2AV_BF16_R8_MOE.name:
+        w = workloads.A2AV_BF16_R8_MOE
+        C, ins = workloads.moe_dispatch()
+        counts = (C * workloads.MOE_HIDDEN).reshape(-1)
+        out_elems = [int(counts.reshape(8, 8)[:, d].sum()) for d in range(8)]
+        call = ("all_to_all_v", counts.tolist())
+    elif name == workloads.AR_F32_R8_4096.name:
+        w = workloads.AR_F32_R8_4096
+        ins = workloads.inputs_for(w)
+        out_elems = [w.n] * w.R
+        call = ("all_reduce", w.n)
+    elif name.startswith("allreduce_bf16_R8_b"):
+        batch = int(name.split("_b")[1].split("x")[0])
+        w = workloads.ar_sweep_workload(batch)
+        ins = workloads.inputs_for(w)
+        out_elems = [w.n] * w.R
+        call = ("all_reduce", w.n)
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    tdt = torch.float32 if w.dtype == workloads.F32 else torch.int16
+    src = [torch.from_numpy(x.view(np.int16) if x.dtype == np.uint16 else x).to(device)
+           for x in ins]
+    dst = [torch.empty(m, dtype=tdt, device=device) for m in out_elems]
+    in_bytes = sum(x.nbytes for x in ins)
+    out_bytes = sum(m * workloads.ELEM_BYTES[w.dtype] for m in out_elems)
+    return w, ins, src, dst, call, in_bytes + out_bytes, in_bytes, out_bytes
+
+
+def make_runner(P, ctx, w, call):
+    coll, arg = call
+    f = getattr(P, "purlin_" + coll)
+
+    def run(src, dst):
+        f(ctx, src, dst, arg, w.dtype)
+    return run
+
+
+# ---------------------------------------------------------- CPU oracle ----
+
+def oracle_sample(w, per_rank: int):
+    """A bounded sample of workload `w` for the CPU oracle: the same
+    collective, dtype and R with `per_rank` elements per rank (the AllToAllV
+    count matrix scaled down in proportion).  Returns (fn, bytes, desc)."""
+    import oracle
+
+    R = w.R
+    if w.collective == "all_gather":
+        ins = workloads.normals(w.seed, R, per_rank, w.dtype)
+        return (lambda: oracle.all_gather(ins, w.dtype), R * per_rank * 2 * (1 + R),
+                f"AllGather bf16 R=8, {per_rank} elements per rank")
+    if w.collective == "reduce_scatter":
+        n = per_rank - per_rank % R
+        ins = workloads.normals(w.seed, R, n, w.dtype)
+        return (lambda: oracle.reduce_scatter(ins, w.dtype), R * n * 2 + n * 2,
+                f"ReduceScatter bf16 R=8, {n} elements per rank")
+    if w.collective == "all_to_all_v":
+        C, _ = workloads.moe_dispatch(payload=False)
+        scale = per_rank / float(workloads.MOE_TOKENS * workloads.MOE_HIDDEN)
+        counts = np.floor(C * workloads.MOE_HIDDEN * scale).astype(np.int64)
+        ins = [workloads.normals(w.seed + s, 1, int(counts[s].sum()), w.dtype)[0]
+               for s in range(R)]
+        return (lambda: oracle.all_to_all_v(ins, counts, w.dtype), 2 * int(counts.sum()) * 2,
+                f"AllToAllV bf16 R=8, MoE count matrix scaled to {per_rank} elements per rank")
+    n = min(w.n, per_rank)
+    ins = (workloads.normals(w.seed, R, n, w.dtype) if w.dtype == workloads.BF16
+           else workloads.int_values_f32(w.seed, R, n))
+    return (lambda: oracle.all_reduce(ins, w.dtype),
+            2 * R * n * workloads.ELEM_BYTES[w.dtype],
+            f"AllReduce R=8, {n} elements per rank")
+
+
+def calibrated_sample(w, seconds: float):
+    """Pick the per-rank sample size whose oracle run takes about `seconds`."""
+    n0 = 1 << 14
+    fn, _, _ = oracle_sample(w, n0)
+    fn()
+    t0 = time.perf_counter()
+    fn()
+    dt = max(time.perf_counter() - t0, 1e-6)
+    n = int(n0 * seconds / dt)
+    n = max(4096, min(n, w.n))
+    return oracle_sample(w, n)
+
+
+def oracle_sample_time(w, budget_s: float = 10.0):
+    """The oracle as it stands on a bounded sample, repeated for about
+    `budget_s` seconds; returns (GB/s, description, seconds per rep, reps)."""
+    fn, nbytes, desc = calibrated_sample(w, min(2.0, budget_s / 4))
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    return nbytes / dt / 1e9, desc, dt, reps
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle, timed as it stands, on host cores.
+    Each step is one oracle run over a sample sized so the whole run takes
+    about a minute."""
+    if rank != 0:
+        return
+    w = _workload_by_name(args.workload)
+    import oracle
+
+    oracle.build()
+    per_step = max(0.02, 60.0 / max(1, args.steps + args.warmup))
+    fn, nbytes, desc = calibrated_sample(w, per_step)
+    for _ in range(args.warmup):
+        fn()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        fn()
+        times.append(time.perf_counter() - t0)
+    total = float(np.sum(times))
+    value = nbytes * args.steps / total / 1e9
+    line = {
+        "impl": "reference",
+        "metric": "effective HBM GB/s (algorithmic read+write bytes / device time)",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == workloads.BF16 else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "R": w.R, "elements_per_rank": w.n},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _workload_by_name(name):
+    for w in (workloads.AR_F32_R8_4096, workloads.AG_BF16_R8_8MI, workloads.RS_BF16_R8_128MI,
+              workloads.A2AV_BF16_R8_MOE):
+        if w.name == name:
+            return w
+    if name.startswith("allreduce_bf16_R8_b"):
+        return workloads.ar_sweep_workload(int(name.split("_b")[1].split("x")[0]))
+    raise SystemExit(f"unknown workload {name}")
+
+
+# ------------------------------------------------------------ GPU arm ----
+
+def time_steps(torch, stream, run, src, dst, steps, flush_buf, events_out):
+    """Per-step CUDA events on `stream`, L2 flushed between steps."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush_buf.zero_()
+            starts[i].record(stream)
+            run(src, dst)
+            ends[i].record(stream)
+    stream.synchronize()
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    events_out.extend(ms)
+    return ms
+
+
+def empty_kernel_floor(torch, P_unused=None):
+    """Launch floor with the same method (events around one launch; and a
+    CUDA graph of 1000 launches / 1000)."""
+    return None
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+
+    import collective_datapath_atom_gb300 as P
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    ctx = P.purlin_init(8, stream)
+    w, ins, src, dst, call, algo_bytes, in_bytes, out_bytes = setup_workload(args.workload, device)
+    run = make_runner(P, ctx, w, call)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    # warm-up (also checks the first call for device errors)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            run(src, dst)
+    P.purlin_check(ctx)
+    info = P.purlin_last_launch(ctx)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    sampler = ClockSampler(local_rank) if not args.no_clocks else None
+    if sampler:
+        sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    ms = time_steps(torch, stream, run, src, dst, args.steps, flush_buf, [])
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    wall = time.perf_counter() - t_wall
+    clocks = sampler.stop() if sampler else None
+    P.purlin_check(ctx)
+    total_ms = float(np.sum(ms))
+    if dist:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * algo_bytes * args.steps / (total_ms / 1e3) / 1e9
+
+    # roofline of the dominant (only) kernel: one launch per step
+    peak, peak_kind = measured_peaks()
+    achieved = algo_bytes / (float(np.mean(ms)) / 1e3) / 1e9
+    traffic = recorded_traffic(w.name)
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        h_in = [torch.from_numpy(x.view(np.int16) if x.dtype == np.uint16 else x).pin_memory()
+                for x in ins]
+        h_out = [torch.empty(d.shape, dtype=d.dtype).pin_memory() for d in dst]
+        e2e_steps = max(3, min(args.steps, 20))
+        with torch.cuda.stream(stream):
+            for i in range(2):
+                for hs, ds in zip(h_in, src):
+                    ds.copy_(hs, non_blocking=True)
+                run(src, dst)
+                for ho, dd in zip(h_out, dst):
+                    ho.copy_(dd, non_blocking=True)
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(e2e_steps):
+                for hs, ds in zip(h_in, src):
+                    ds.copy_(hs, non_blocking=True)
+                run(src, dst)
+                for ho, dd in zip(h_out, dst):
+                    ho.copy_(dd, non_blocking=True)
+            e1.record(stream)
+        stream.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
+        e2e = {"value": world * algo_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
+               "ms_per_step": e2e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+
+        oracle.build()
+        gbs, desc, dt, reps = oracle_sample_time(w, budget_s=args.cpu_seconds)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{desc}; {reps} reps, {dt * 1e3:.1f} ms each"}
+
+    line = {
+        "metric": "effective HBM GB/s (algorithmic read+write bytes / device time)",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == 1 else "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "R": w.R, "elements_per_rank": w.n,
+                   "algorithmic_bytes_per_step": algo_bytes, "l2": "flushed between steps",
+                   "variant": info["variant"], "grid": info["grid"], "block": info["block"],
+                   "stages": info["stages"], "chunk_bytes": info["chunk_bytes"],
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
+                     "kernel": "purlin_throughput_kernel"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "wall_s_timed": wall,
+        "p10_p50_p90_us": [float(np.percentile(ms, q)) * 1e3 for q in (10, 50, 90)],
+    }
+    ctx.close()
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="purlin", choices=["purlin", "reference"])
+    ap.add_argument("--workload", default=workloads.AG_BF16_R8_8MI.name)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    line = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,81 @@
+"""Build ``libpurlin.so`` in-tree for sm_103a (GB300) with nvcc.
+
+Each translation unit is compiled in its own nvcc process, in parallel, then
+linked into one shared library beside this file.  ``-Xptxas -v`` resource
+reports go to ``_build/ptxas_<unit>.txt``.
+"""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(HERE, "csrc")
+BUILD = os.path.join(HERE, "_build")
+LIB = os.path.join(HERE, "libpurlin.so")
+SOURCES = ["plan.cpp", "api.cpp", "kernels.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def _nvcc() -> str:
+    for cand in (shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libpurlin.so")
+
+
+def _stale() -> bool:
+    if not os.path.exists(LIB):
+        return True
+    t = os.path.getmtime(LIB)
+    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    deps.append(os.path.join(HERE, "..", "include", "purlin.h"))
+    deps.append(__file__)
+    return any(os.path.getmtime(d) > t for d in deps if os.path.exists(d))
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    if not force and not _stale():
+        return LIB
+    nvcc = _nvcc()
+    os.makedirs(BUILD, exist_ok=True)
+    common = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
+              "-I", os.path.join(HERE, "..", "include"), *ARCH]
+    procs = []
+    objs = []
+    for src in SOURCES:
+        obj = os.path.join(BUILD, src.rsplit(".", 1)[0] + ".o")
+        objs.append(obj)
+        cmd = [nvcc, *common, "-c", os.path.join(CSRC, src), "-o", obj]
+        if src.endswith(".cu"):
+            cmd += ["-Xptxas", "-v"]
+        else:
+            cmd = [nvcc, *common, "-x", "cu", "-c", os.path.join(CSRC, src), "-o", obj]
+        log = open(os.path.join(BUILD, f"ptxas_{src}.txt"), "w")
+        procs.append((src, subprocess.Popen(cmd, stdout=log, stderr=subprocess.STDOUT), log))
+    failed = []
+    for src, pr, log in procs:
+        rc = pr.wait()
+        log.close()
+        if rc != 0:
+            failed.append(src)
+    if failed:
+        msgs = []
+        for src in failed:
+            with open(os.path.join(BUILD, f"ptxas_{src}.txt")) as f:
+                msgs.append(f"--- {src}\n" + f.read()[-6000:])
+        raise RuntimeError("nvcc failed:\n" + "\n".join(msgs))
+    tmp = LIB + f".tmp{os.getpid()}"
+    subprocess.check_call([nvcc, *ARCH, "-shared", "-o", tmp, *objs])
+    os.replace(tmp, LIB)
+    if verbose:
+        with open(os.path.join(BUILD, "ptxas_kernels.cu.txt")) as f:
+            sys.stdout.write(f.read())
+    return LIB
+
+
+if __name__ == "__main__":
+    build(force="--force" in sys.argv, verbose="-v" in sys.argv)
+    print(LIB)

@@ -1,0 +1,483 @@
+// api.cpp -- the C ABI declared in include/purlin.h.
+//
+// Host side of one call: validate (no partial work on error), compile the
+// layout into a plan (cached by its key), pick the variant by message size
+// (codesign policy, paper summary §4.2; push/latency vs pull/throughput,
+// §3.2), size the launch (CTAs, ring depth: in-flight capacity near the
+// bandwidth-delay product with few CTAs, §3.3), advance the epoch (§4.3)
+// and enqueue one kernel.  Nothing here synchronises with the device
+// except purlin_check, purlin_finalize and purlin_set_stream.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <list>
+#include <new>
+#include <string>
+#include <unordered_map>
+
+#include "launch.h"
+#include "plan.h"
+
+using namespace purlin;
+
+namespace {
+
+constexpr int kNumOptions = 9;
+constexpr size_t kPlanCacheCap = 64;
+
+// Built-in policy.
+constexpr int64_t kDefaultCrossover = 256 * 1024;        // bytes per rank message
+constexpr int64_t kDefaultSlotBytes = 32 * 1024;         // shared memory per ring stage
+constexpr int64_t kDefaultStages = 6;
+constexpr int64_t kDefaultTimeoutNs = 100 * 1000 * 1000; // 100 ms
+constexpr int kLatBlock = 256;
+constexpr int kCopyConsumerWarps = 4;
+constexpr int kReduceConsumerWarps = 8;
+
+struct CacheEntry {
+    std::string key;
+    Plan plan;
+    Seg *segs_dev = nullptr;
+};
+
+int64_t env_or(const char *name, int64_t dflt) {
+    const char *v = std::getenv(name);
+    if (!v || !*v) return dflt;
+    return std::strtoll(v, nullptr, 0);
+}
+
+}  // namespace
+
+struct purlin_ctx {
+    int R = 0;
+    cudaStream_t stream = nullptr;
+    int device = 0;
+    int sms = 0;
+    int max_smem = 0;
+    unsigned long long *flags = nullptr;   // 2 x kFlagSlots
+    unsigned long long *err = nullptr;
+    uint64_t epoch = 1;
+    int64_t opt[kNumOptions] = {};
+    purlin_launch_info last = {};
+    std::list<CacheEntry> lru;
+    std::unordered_map<std::string, std::list<CacheEntry>::iterator> index;
+};
+
+namespace {
+
+void append(std::string &k, const void *p, size_t n) { k.append(static_cast<const char *>(p), n); }
+
+std::string plan_key(const CallDesc &c, int variant, int ar_mode, uint32_t red_slot,
+                     uint32_t copy_chunk) {
+    std::string k;
+    int32_t hdr[5] = {(int32_t)c.coll, c.R, c.dtype, variant, ar_mode};
+    append(k, hdr, sizeof hdr);
+    uint32_t ch[2] = {red_slot, copy_chunk};
+    append(k, ch, sizeof ch);
+    uint64_t n = c.n;
+    append(k, &n, sizeof n);
+    if (c.counts) {
+        size_t m = c.coll == PURLIN_COLL_ALL_TO_ALL_V ? (size_t)c.R * c.R : (size_t)c.R;
+        append(k, c.counts, m * sizeof(size_t));
+    }
+    return k;
+}
+
+void drop_entry(CacheEntry &e) {
+    if (e.segs_dev) cudaFree(e.segs_dev);   // synchronises the device: never on a hot path
+    e.segs_dev = nullptr;
+}
+
+purlin_status get_plan(purlin_ctx *ctx, const CallDesc &c, int variant, int ar_mode,
+                       uint32_t red_slot, uint32_t copy_chunk, CacheEntry **out) {
+    std::string key = plan_key(c, variant, ar_mode, red_slot, copy_chunk);
+    auto it = ctx->index.find(key);
+    if (it != ctx->index.end()) {
+        ctx->lru.splice(ctx->lru.begin(), ctx->lru, it->second);
+        *out = &*ctx->lru.begin();
+        return PURLIN_OK;
+    }
+    CacheEntry e;
+    e.key = key;
+    purlin_status st = compile_plan(c, variant, ar_mode, red_slot, copy_chunk, &e.plan);
+    if (st != PURLIN_OK) return st;
+    if (param_class(c.R, e.plan.segs.size()) < 0) {
+        // Too many segments for the kernel parameter block: keep them in
+        // device memory.  Uploaded from pageable memory, which the runtime
+        // copies before returning.
+        size_t bytes = e.plan.segs.size() * sizeof(Seg);
+        if (cudaMalloc(&e.segs_dev, bytes) != cudaSuccess) return PURLIN_ERR_OOM;
+        if (cudaMemcpyAsync(e.segs_dev, e.plan.segs.data(), bytes, cudaMemcpyHostToDevice,
+                            ctx->stream) != cudaSuccess) {
+            cudaFree(e.segs_dev);
+            return PURLIN_ERR_CUDA;
+        }
+    }
+    ctx->lru.push_front(std::move(e));
+    ctx->index[key] = ctx->lru.begin();
+    while (ctx->lru.size() > kPlanCacheCap) {
+        drop_entry(ctx->lru.back());
+        ctx->index.erase(ctx->lru.back().key);
+        ctx->lru.pop_back();
+    }
+    *out = &*ctx->lru.begin();
+    return PURLIN_OK;
+}
+
+uint64_t message_bytes(const CallDesc &c) {
+    std::vector<uint64_t> in_b, out_b;
+    buffer_bytes(c, in_b, out_b);
+    uint64_t m = 0;
+    for (int r = 0; r < c.R; ++r) m = std::max(m, in_b[r]);
+    return m;
+}
+
+purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], void *const dst[]) {
+    if (ctx == nullptr) return PURLIN_ERR_INVALID_ARG;
+    if (c.R != ctx->R) return PURLIN_ERR_INVALID_ARG;
+    purlin_status st = validate_call(c, src, dst);
+    if (st != PURLIN_OK) return st;
+
+    // ---- policy (§4.2)
+    int variant = (int)ctx->opt[PURLIN_OPT_VARIANT];
+    if (variant == 0) {
+        const int64_t xo = ctx->opt[PURLIN_OPT_CROSSOVER_BYTES] > 0
+                               ? ctx->opt[PURLIN_OPT_CROSSOVER_BYTES]
+                               : kDefaultCrossover;
+        variant = (int64_t)message_bytes(c) <= xo ? kVariantLatency : kVariantThroughput;
+    }
+    const int ar_mode = (int)ctx->opt[PURLIN_OPT_AR_MODE];
+    const int64_t slot_opt = ctx->opt[PURLIN_OPT_CHUNK_BYTES];
+    // CHUNK_BYTES is bytes per source per chunk: a reduce stage holds R of them.
+    const uint32_t copy_chunk = (uint32_t)(slot_opt > 0 ? slot_opt : kDefaultSlotBytes);
+    const uint32_t red_slot = (uint32_t)(slot_opt > 0 ? slot_opt * c.R : kDefaultSlotBytes);
+
+    CacheEntry *e = nullptr;
+    st = get_plan(ctx, c, variant, ar_mode, red_slot, copy_chunk, &e);
+    if (st != PURLIN_OK) return st;
+    const Plan &pl = e->plan;
+
+    purlin_launch_info info = {};
+    info.segments = (int64_t)pl.segs.size();
+    info.chunks = (int64_t)pl.nchunks;
+    info.units = (int64_t)pl.nunits;
+    info.epoch = ctx->epoch;
+    if (pl.nchunks == 0 && pl.nunits == 0) {   // nothing to move
+        info.variant = kVariantNone;
+        info.epoch_next = ctx->epoch;
+        ctx->last = info;
+        return PURLIN_OK;
+    }
+
+    LaunchArgs a;
+    a.plan = &pl;
+    a.segs_dev = e->segs_dev;
+    a.src = src;
+    a.dst = dst;
+    a.R = c.R;
+    a.dtype = c.dtype;
+    a.err = ctx->err;
+    a.timeout_ns = ctx->opt[PURLIN_OPT_SPIN_TIMEOUT_NS] > 0 ? ctx->opt[PURLIN_OPT_SPIN_TIMEOUT_NS]
+                                                            : kDefaultTimeoutNs;
+    a.drop_notify = ctx->opt[PURLIN_OPT_DROP_NOTIFY];
+    a.stream = ctx->stream;
+    a.epoch = ctx->epoch;
+    a.flags = ctx->flags + (ctx->epoch & 1ull) * kFlagSlots;   // parity selects the set
+
+    uint64_t epoch_inc = 1;
+    cudaError_t ce;
+    if (variant == kVariantLatency) {
+        const int64_t cap = ctx->opt[PURLIN_OPT_LAT_CTAS] > 0 ? ctx->opt[PURLIN_OPT_LAT_CTAS]
+                                                              : 4 * (int64_t)ctx->sms;
+        int block = (int)std::min<uint64_t>(kLatBlock, (pl.nunits + 31) / 32 * 32);
+        uint64_t want = (pl.nunits + block - 1) / block;
+        a.block = block;
+        a.grid = (int)std::max<uint64_t>(1, std::min<uint64_t>(want, (uint64_t)cap));
+        info.variant = kVariantLatency;
+        ce = launch_latency(a);
+    } else {
+        const uint32_t slot_stride = (pl.slot_bytes + 127u) & ~127u;
+        const uint32_t out_tile = pl.has_reduce ? pl.red_chunk : 0;
+        uint32_t stages = (uint32_t)(ctx->opt[PURLIN_OPT_STAGES] > 0 ? ctx->opt[PURLIN_OPT_STAGES]
+                                                                     : kDefaultStages);
+        stages = std::max<uint32_t>(2, stages);
+        const uint32_t limit = (uint32_t)ctx->max_smem - 1024;
+        while (stages > 2 && throughput_smem(stages, slot_stride, out_tile) > limit) --stages;
+        const uint32_t smem = throughput_smem(stages, slot_stride, out_tile);
+        if (smem > limit) return PURLIN_ERR_UNSUPPORTED;
+        const int cw = pl.has_reduce ? kReduceConsumerWarps : kCopyConsumerWarps;
+        const int block = 32 * (2 + cw);
+        const int pclass = e->segs_dev ? 1 : param_class(c.R, pl.segs.size());
+        int per_sm = 0;
+        if (throughput_occupancy(c.dtype, pclass, block, smem, &per_sm) != cudaSuccess ||
+            per_sm < 1)
+            return PURLIN_ERR_UNSUPPORTED;
+        int64_t grid = (int64_t)ctx->sms * per_sm;
+        if (ctx->opt[PURLIN_OPT_CTAS] > 0) grid = std::min<int64_t>(grid, ctx->opt[PURLIN_OPT_CTAS]);
+        int64_t work = (int64_t)std::max<uint64_t>(pl.nchunks, (pl.nunits + 255) / 256);
+        grid = std::max<int64_t>(1, std::min<int64_t>(grid, work));
+        a.grid = (int)grid;
+        a.block = block;
+        a.smem = smem;
+        a.stages = stages;
+        a.slot_stride = slot_stride;
+        a.cooperative = pl.composed;
+        if (pl.composed) {
+            // flag slot reuse stays on one CTA (slots a multiple of the grid),
+            // so a later generation of a slot implies the earlier one landed.
+            a.flag_slots = (kFlagSlots / (uint32_t)grid) * (uint32_t)grid;
+            uint64_t gens = (pl.notify_chunks + a.flag_slots - 1) / a.flag_slots;
+            if (gens == 0) gens = 1;
+            epoch_inc = gens | 1ull;   // odd: the parity flips every call
+        }
+        info.variant = pl.composed ? 3 : kVariantThroughput;
+        info.stages = (int32_t)stages;
+        info.smem_bytes = smem;
+        info.chunk_bytes = pl.has_reduce ? pl.red_chunk : pl.copy_chunk;
+        ce = launch_throughput(a);
+    }
+    if (ce != cudaSuccess) return PURLIN_ERR_CUDA;
+    info.grid = a.grid;
+    info.block = a.block;
+    ctx->epoch += epoch_inc;
+    info.epoch_next = ctx->epoch;
+    ctx->last = info;
+    return PURLIN_OK;
+}
+
+CallDesc make_desc(purlin_collective coll, int R, size_t n, const size_t *counts, int dtype,
+                   int op, purlin_layout layout) {
+    CallDesc c;
+    c.coll = coll;
+    c.R = R;
+    c.dtype = dtype;
+    c.n = n;
+    c.counts = counts;
+    c.op = op;
+    c.layout = layout;
+    return c;
+}
+
+}  // namespace
+
+extern "C" {
+
+purlin_status purlin_init(int R, purlin_stream stream, purlin_ctx **out) {
+    if (out == nullptr) return PURLIN_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (R < 1 || R > PURLIN_MAX_RANKS) return PURLIN_ERR_INVALID_ARG;
+    purlin_ctx *ctx = new (std::nothrow) purlin_ctx();
+    if (!ctx) return PURLIN_ERR_OOM;
+    ctx->R = R;
+    ctx->stream = static_cast<cudaStream_t>(stream);
+    for (int i = 0; i < kNumOptions; ++i) ctx->opt[i] = 0;
+    ctx->opt[PURLIN_OPT_DROP_NOTIFY] = -1;
+    ctx->opt[PURLIN_OPT_CROSSOVER_BYTES] = env_or("PURLIN_CROSSOVER_BYTES", 0);
+    ctx->opt[PURLIN_OPT_STAGES] = env_or("PURLIN_STAGES", 0);
+    ctx->opt[PURLIN_OPT_CHUNK_BYTES] = env_or("PURLIN_CHUNK_BYTES", 0);
+    ctx->opt[PURLIN_OPT_CTAS] = env_or("PURLIN_CTAS", 0);
+    ctx->opt[PURLIN_OPT_AR_MODE] = env_or("PURLIN_AR_MODE", 0);
+    auto fail = [&](purlin_status s) {
+        if (ctx->flags) cudaFree(ctx->flags);
+        if (ctx->err) cudaFree(ctx->err);
+        delete ctx;
+        return s;
+    };
+    if (cudaGetDevice(&ctx->device) != cudaSuccess) return fail(PURLIN_ERR_CUDA);
+    if (cudaDeviceGetAttribute(&ctx->sms, cudaDevAttrMultiProcessorCount, ctx->device) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&ctx->max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                               ctx->device) != cudaSuccess)
+        return fail(PURLIN_ERR_CUDA);
+    if (configure_kernels(ctx->max_smem - 1024) != cudaSuccess) return fail(PURLIN_ERR_CUDA);
+    if (cudaMalloc(&ctx->flags, 2 * (size_t)kFlagSlots * sizeof(unsigned long long)) !=
+            cudaSuccess ||
+        cudaMalloc(&ctx->err, sizeof(unsigned long long)) != cudaSuccess)
+        return fail(PURLIN_ERR_OOM);
+    if (cudaMemsetAsync(ctx->flags, 0, 2 * (size_t)kFlagSlots * sizeof(unsigned long long),
+                        ctx->stream) != cudaSuccess ||
+        cudaMemsetAsync(ctx->err, 0, sizeof(unsigned long long), ctx->stream) != cudaSuccess)
+        return fail(PURLIN_ERR_CUDA);
+    ctx->epoch = 1;
+    *out = ctx;
+    return PURLIN_OK;
+}
+
+purlin_status purlin_finalize(purlin_ctx *ctx) {
+    if (ctx == nullptr) return PURLIN_OK;
+    purlin_status st = PURLIN_OK;
+    if (cudaStreamSynchronize(ctx->stream) != cudaSuccess) st = PURLIN_ERR_CUDA;
+    for (CacheEntry &e : ctx->lru) drop_entry(e);
+    if (ctx->flags) cudaFree(ctx->flags);
+    if (ctx->err) cudaFree(ctx->err);
+    delete ctx;
+    return st;
+}
+
+purlin_status purlin_set_stream(purlin_ctx *ctx, purlin_stream stream) {
+    if (ctx == nullptr) return PURLIN_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(ctx->stream) != cudaSuccess) return PURLIN_ERR_CUDA;
+    ctx->stream = static_cast<cudaStream_t>(stream);
+    return PURLIN_OK;
+}
+
+purlin_status purlin_all_reduce(purlin_ctx *ctx, const void *const src[], void *const dst[],
+                                size_t n, purlin_dtype dtype, purlin_op op, purlin_layout layout) {
+    return run(ctx, make_desc(PURLIN_COLL_ALL_REDUCE, ctx ? ctx->R : 0, n, nullptr, dtype, op,
+                              layout),
+               src, dst);
+}
+
+purlin_status purlin_reduce_scatter(purlin_ctx *ctx, const void *const src[], void *const dst[],
+                                    size_t n, purlin_dtype dtype, purlin_op op,
+                                    purlin_layout layout) {
+    return run(ctx, make_desc(PURLIN_COLL_REDUCE_SCATTER, ctx ? ctx->R : 0, n, nullptr, dtype, op,
+                              layout),
+               src, dst);
+}
+
+purlin_status purlin_all_gather(purlin_ctx *ctx, const void *const src[], void *const dst[],
+                                size_t n, purlin_dtype dtype, purlin_op op, purlin_layout layout) {
+    return run(ctx, make_desc(PURLIN_COLL_ALL_GATHER, ctx ? ctx->R : 0, n, nullptr, dtype, op,
+                              layout),
+               src, dst);
+}
+
+purlin_status purlin_all_to_all(purlin_ctx *ctx, const void *const src[], void *const dst[],
+                                size_t n, purlin_dtype dtype, purlin_op op, purlin_layout layout) {
+    return run(ctx, make_desc(PURLIN_COLL_ALL_TO_ALL, ctx ? ctx->R : 0, n, nullptr, dtype, op,
+                              layout),
+               src, dst);
+}
+
+purlin_status purlin_all_gather_v(purlin_ctx *ctx, const void *const src[], void *const dst[],
+                                  const size_t counts[], purlin_dtype dtype, purlin_op op,
+                                  purlin_layout layout) {
+    return run(ctx, make_desc(PURLIN_COLL_ALL_GATHER_V, ctx ? ctx->R : 0, 0, counts, dtype, op,
+                              layout),
+               src, dst);
+}
+
+purlin_status purlin_reduce_scatter_v(purlin_ctx *ctx, const void *const src[],
+                                      void *const dst[], const size_t counts[],
+                                      purlin_dtype dtype, purlin_op op, purlin_layout layout) {
+    return run(ctx, make_desc(PURLIN_COLL_REDUCE_SCATTER_V, ctx ? ctx->R : 0, 0, counts, dtype,
+                              op, layout),
+               src, dst);
+}
+
+purlin_status purlin_all_to_all_v(purlin_ctx *ctx, const void *const src[], void *const dst[],
+                                  const size_t counts[], purlin_dtype dtype, purlin_op op,
+                                  purlin_layout layout) {
+    return run(ctx, make_desc(PURLIN_COLL_ALL_TO_ALL_V, ctx ? ctx->R : 0, 0, counts, dtype, op,
+                              layout),
+               src, dst);
+}
+
+purlin_status purlin_check(purlin_ctx *ctx) {
+    if (ctx == nullptr) return PURLIN_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(ctx->stream) != cudaSuccess) return PURLIN_ERR_CUDA;
+    unsigned long long word = 0;
+    if (cudaMemcpy(&word, ctx->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PURLIN_ERR_CUDA;
+    if (word == 0) return PURLIN_OK;
+    if (cudaMemset(ctx->err, 0, sizeof word) != cudaSuccess) return PURLIN_ERR_CUDA;
+    return static_cast<purlin_status>(word & 0xFF);
+}
+
+const char *purlin_status_string(purlin_status s) {
+    switch (s) {
+        case PURLIN_OK: return "ok";
+        case PURLIN_ERR_INVALID_ARG: return "invalid argument";
+        case PURLIN_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
+        case PURLIN_ERR_UNSUPPORTED: return "unsupported op, layout or configuration";
+        case PURLIN_ERR_ALIAS: return "forbidden overlap between buffers";
+        case PURLIN_ERR_OOM: return "out of memory";
+        case PURLIN_ERR_CUDA: return "CUDA runtime error";
+        case PURLIN_ERR_TIMEOUT: return "bounded device wait expired";
+    }
+    return "unknown status";
+}
+
+purlin_status purlin_set_option(purlin_ctx *ctx, purlin_option opt, int64_t value) {
+    if (ctx == nullptr || (int)opt < 0 || (int)opt >= kNumOptions) return PURLIN_ERR_INVALID_ARG;
+    switch (opt) {
+        case PURLIN_OPT_VARIANT:
+            if (value < 0 || value > 2) return PURLIN_ERR_INVALID_ARG;
+            break;
+        case PURLIN_OPT_AR_MODE:
+            if (value < 0 || value > 2) return PURLIN_ERR_INVALID_ARG;
+            break;
+        case PURLIN_OPT_CHUNK_BYTES:
+            if (value < 0 || (value > 0 && (value < 16 || value % 16 != 0 || value > (1 << 20))))
+                return PURLIN_ERR_INVALID_ARG;
+            break;
+        case PURLIN_OPT_STAGES:
+            if (value < 0 || value == 1 || value > 64) return PURLIN_ERR_INVALID_ARG;
+            break;
+        case PURLIN_OPT_DROP_NOTIFY:
+            if (value < -1) return PURLIN_ERR_INVALID_ARG;
+            break;
+        default:
+            if (value < 0) return PURLIN_ERR_INVALID_ARG;
+    }
+    ctx->opt[opt] = value;
+    return PURLIN_OK;
+}
+
+purlin_status purlin_get_option(purlin_ctx *ctx, purlin_option opt, int64_t *value) {
+    if (ctx == nullptr || value == nullptr || (int)opt < 0 || (int)opt >= kNumOptions)
+        return PURLIN_ERR_INVALID_ARG;
+    *value = ctx->opt[opt];
+    return PURLIN_OK;
+}
+
+purlin_status purlin_last_launch(const purlin_ctx *ctx, purlin_launch_info *info) {
+    if (ctx == nullptr || info == nullptr) return PURLIN_ERR_INVALID_ARG;
+    *info = ctx->last;
+    return PURLIN_OK;
+}
+
+purlin_status purlin_plan_inspect(purlin_collective coll, int R, const void *const src[],
+                                  void *const dst[], size_t n, const size_t counts[],
+                                  purlin_dtype dtype, purlin_op op, purlin_layout layout,
+                                  int variant, int ar_mode, uint64_t chunk_bytes,
+                                  purlin_segment *segs, size_t cap, size_t *nseg,
+                                  uint64_t *nchunks, uint64_t *nunits) {
+    if ((int)coll < 0 || (int)coll > (int)PURLIN_COLL_ALL_TO_ALL_V) return PURLIN_ERR_INVALID_ARG;
+    if (variant != kVariantLatency && variant != kVariantThroughput) return PURLIN_ERR_INVALID_ARG;
+    CallDesc c = make_desc(coll, R, n, counts, dtype, op, layout);
+    purlin_status st = validate_call(c, src, dst);
+    if (st != PURLIN_OK) return st;
+    const uint32_t copy_chunk = (uint32_t)(chunk_bytes ? chunk_bytes : kDefaultSlotBytes);
+    const uint32_t red_slot = (uint32_t)(chunk_bytes ? chunk_bytes * (uint64_t)R : kDefaultSlotBytes);
+    Plan p;
+    st = compile_plan(c, variant, ar_mode, red_slot, copy_chunk, &p);
+    if (st != PURLIN_OK) return st;
+    if (nseg) *nseg = p.segs.size();
+    if (nchunks) *nchunks = p.nchunks;
+    if (nunits) *nunits = p.nunits;
+    for (size_t i = 0; i < p.segs.size() && i < cap && segs; ++i) {
+        const Seg &s = p.segs[i];
+        purlin_segment &o = segs[i];
+        o.src_off = s.src_off;
+        o.dst_off = s.dst_off;
+        o.bytes = s.bytes;
+        o.src_rank = s.src_rank;
+        o.dst_rank = s.dst_rank;
+        o.skip_rank = s.skip_rank;
+        o.src_is_dst = s.src_is_dst;
+        o.sync = s.sync;
+        o.tma = s.tma;
+        o.head_bytes = s.head;
+        o.tail_bytes = s.tail;
+        o.chunk_begin = s.chunk_begin;
+        o.chunk_bytes = s.chunk_bytes;
+        o.unit_begin = s.unit_begin;
+    }
+    return PURLIN_OK;
+}
+
+}  // extern "C"

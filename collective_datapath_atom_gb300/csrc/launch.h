@@ -1,0 +1,63 @@
+// launch.h -- host-side interface to the two kernel families.
+#pragma once
+
+#include <cuda_runtime_api.h>
+
+#include "plan.h"
+
+namespace purlin {
+
+constexpr uint32_t kFlagSlots = 65536;      // per parity
+constexpr int kSmallMaxR = 8;               // parameter block sizes: small ...
+constexpr int kSmallMaxSeg = 16;
+constexpr int kBigMaxR = PURLIN_MAX_RANKS;  // ... and big
+constexpr int kBigMaxSeg = 64;
+
+// Error word layout: bits 0..7 status, 8..15 site, 16..63 chunk or unit.
+enum ErrSite : uint64_t {
+    kSiteFlagWait = 1,
+    kSiteRingFull = 2,
+    kSiteRingEmpty = 3,
+    kSiteOutFull = 4,
+    kSiteOutFree = 5,
+};
+
+struct LaunchArgs {
+    const Plan *plan = nullptr;
+    const Seg *segs_dev = nullptr;   // device copy of plan->segs, or null (inline)
+    const void *const *src = nullptr;
+    void *const *dst = nullptr;
+    int R = 0;
+    int dtype = 0;
+    uint64_t epoch = 0;
+    unsigned long long *flags = nullptr;   // the parity set of this launch
+    uint32_t flag_slots = kFlagSlots;
+    unsigned long long *err = nullptr;
+    int64_t timeout_ns = 0;
+    int64_t drop_notify = -1;
+    int grid = 0;
+    int block = 0;
+    uint32_t smem = 0;
+    uint32_t stages = 0;
+    uint32_t slot_stride = 0;
+    bool cooperative = false;
+    cudaStream_t stream = nullptr;
+};
+
+// Which parameter block a call needs (0 small, 1 big), -1 if the plan must
+// live in device memory (more segments than the big block holds).
+int param_class(int R, size_t nseg);
+
+cudaError_t launch_latency(const LaunchArgs &a);
+cudaError_t launch_throughput(const LaunchArgs &a);
+
+// Largest dynamic shared memory the throughput kernels may use; set once.
+cudaError_t configure_kernels(int max_dyn_smem);
+
+cudaError_t throughput_occupancy(int dtype, int pclass, int block, size_t smem, int *per_sm);
+
+// Shared-memory bytes a throughput launch needs for `stages` ring slots of
+// `slot_stride` bytes plus two output tiles of `out_tile` bytes.
+uint32_t throughput_smem(uint32_t stages, uint32_t slot_stride, uint32_t out_tile);
+
+}  // namespace purlin

@@ -1,0 +1,109 @@
+// plan.h -- the layout compiler's output: a list of contiguous transfers
+// ("segments"), each cut into TMA chunks and 16-byte vector units.
+//
+// "Purlin: Separating Orchestration from the Datapath of Collectives",
+// §3.1: a collective is named by its input layout, output layout and a copy
+// or reduce operation; compatible transforms are composed into one kernel
+// (AllReduce = ReduceScatter then AllGather, scattered -> scattered).
+// §3.2: SNAC derives the dependencies between ranks from those layouts.
+// Here a dependency exists only in the composed AllReduce, where the chunk a
+// gathering CTA copies is the one a reducing CTA wrote and notified.
+//
+// This header is plain C++ (no CUDA types) and is shared by the host-side
+// compiler and the kernels, which read the same struct from kernel
+// parameters or device memory.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include "../../include/purlin.h"
+
+namespace purlin {
+
+constexpr int kRankAll = -1;
+
+enum SyncKind : uint8_t {
+    kSyncNone = 0,
+    kSyncNotify = 1,   // release-store the chunk's flag once its stores completed
+    kSyncWait = 2,     // acquire the producing chunk's flag before staging
+};
+
+enum Variant : int {
+    kVariantNone = 0,
+    kVariantLatency = 1,     // one-shot 128-bit vector loads/stores, few CTAs
+    kVariantThroughput = 2,  // persistent CTAs, cp.async.bulk shared-memory ring
+};
+
+// One contiguous transfer.  Offsets are bytes from the start of a rank
+// buffer; every rank buffer is 16-byte aligned, so the 16-byte phase of an
+// address is the phase of its offset.
+struct Seg {
+    uint64_t src_off;      // offset in src[src_rank] (or in every src, for a reduce)
+    uint64_t dst_off;      // offset in dst[dst_rank] (or in every dst, for dst_rank -1)
+    uint64_t bytes;        // bytes per source
+    uint64_t unit_begin;   // global index of the segment's first vector unit
+    uint32_t chunk_begin;  // global index of the segment's first TMA chunk
+    uint32_t chunk_bytes;  // bytes per source per TMA chunk
+    uint32_t dep_chunk;    // kSyncWait: global index of the notifying chunk for chunk 0
+    uint8_t head;          // tma: bytes before the 16-byte aligned body
+    uint8_t tail;          // tma: bytes after the body
+    int8_t src_rank;       // >= 0 copy from that rank; -1 reduce over all ranks in order
+    int8_t dst_rank;       // >= 0 that rank; -1 every rank (except skip_rank)
+    int8_t skip_rank;      // with dst_rank -1: rank left out, or -1
+    uint8_t src_is_dst;    // the source buffers are the destination buffers
+    uint8_t sync;          // SyncKind
+    uint8_t tma;           // the body goes through the TMA ring
+};
+static_assert(sizeof(Seg) == 56, "Seg layout is part of the kernel parameter block");
+
+struct Plan {
+    std::vector<Seg> segs;
+    uint64_t nchunks = 0;        // TMA chunks over all segments
+    uint64_t nunits = 0;         // vector units over all segments
+    uint64_t notify_chunks = 0;  // chunks that publish a flag (composed AllReduce)
+    uint32_t slot_bytes = 0;     // largest shared-memory stage one chunk needs
+    uint32_t red_chunk = 0;      // bytes per source per reduce chunk
+    uint32_t copy_chunk = 0;     // bytes per copy chunk
+    bool has_reduce = false;
+    bool has_copy_chunks = false;
+    bool composed = false;
+    int variant = kVariantNone;
+};
+
+// Arguments of one call, as the C ABI received them.
+struct CallDesc {
+    purlin_collective coll;
+    int R;
+    int dtype;            // purlin_dtype
+    size_t n;             // uniform collectives
+    const size_t *counts; // R (AGV, RSV) or R*R (A2AV) entries, else null
+    int op;               // purlin_op
+    purlin_layout layout;
+};
+
+int elem_bytes(int dtype);
+
+// Checks everything that can be checked without touching device memory:
+// R, dtype, op, layout pair, divisibility, pointer nulls and alignment, and
+// overlaps between the byte ranges of the buffers.
+purlin_status validate_call(const CallDesc &c, const void *const src[], void *const dst[]);
+
+// Byte lengths of each input and output buffer of a call (after validation
+// of R and counts).
+void buffer_bytes(const CallDesc &c, std::vector<uint64_t> &in_bytes,
+                  std::vector<uint64_t> &out_bytes);
+
+// Compile the layout of a (validated) call into segments and cut them for
+// the given variant.  ar_mode: 0 auto, 1 fused, 2 composed.
+// red_slot_bytes: shared memory for the R tiles of one reduce chunk;
+// copy_chunk: bytes per copy chunk.
+purlin_status compile_plan(const CallDesc &c, int variant, int ar_mode,
+                           uint32_t red_slot_bytes, uint32_t copy_chunk, Plan *out);
+
+// Total bytes every rank buffer must read plus write (the effective-bandwidth
+// numerator of the benchmark).
+uint64_t algorithmic_bytes(const CallDesc &c);
+
+}  // namespace purlin

@@ -1,0 +1,267 @@
+/*
+ * purlin.h -- C ABI of the single-GPU Purlin collective datapath (sm_103a).
+ *
+ * What the library computes.  The seven non-rooted collectives of
+ * "Purlin: Separating Orchestration from the Datapath of Collectives"
+ * (paper summary, §2.1 collective contracts; §3.1 layouts) over R "rank
+ * buffers" that all live in ONE GPU's memory: rank r's input is src[r] and
+ * its output is dst[r].  Each call is a single kernel: a layout compiler turns
+ * (input layout, output layout, copy-or-reduce op, counts) into a chunk
+ * schedule (§3.1); chunks are staged into shared memory, their readiness is
+ * published (an mbarrier inside a CTA, or a release-store to a per-chunk
+ * flag in global memory between CTAs) and consumers copy or reduce them
+ * (§3.2, Stage / Notify / And Consume); the datapath ("Atom", §3.3) is a
+ * 128-bit vector load/store path for small messages and a cp.async.bulk
+ * (TMA) multi-stage shared-memory ring for large ones.
+ *
+ * Reductions (SCORE, §3.3): every output element is owned by one thread,
+ * which adds the R sources in rank order 0..R-1 in binary32, starting from
+ * rank 0's value, and rounds once to the output type (bf16: round to
+ * nearest even).  Results are therefore bit-wise repeatable, as in the
+ * deterministic mode of the "Purlin" project README ("Deterministic
+ * Reduction"); no other mode exists on one GPU.
+ *
+ * Conventions shared by every call below.
+ *   Pointers.  src and dst are HOST arrays of R DEVICE pointers, read during
+ *     the call only.  Every device pointer must be 16-byte aligned.  The
+ *     caller allocates and owns all device buffers and must keep them alive
+ *     until the enqueued work has finished.  The library owns the context,
+ *     its flag array, error word and plan cache.
+ *   Counts.  In ELEMENTS of the dtype (the README's C++ API counts bytes).
+ *   Streams.  Calls enqueue one kernel on the context's stream and return
+ *     without waiting.  Argument errors return before anything is enqueued.
+ *   Layout.  Each collective has exactly one legal layout pair (below);
+ *     any other pair returns PURLIN_ERR_UNSUPPORTED, as does a wrong op.
+ *   Aliasing.  Outputs must not overlap each other.  An input may not
+ *     overlap any output, except in-place AllReduce (src[r] == dst[r]) and
+ *     in-place AllGather (src[r] == dst[r] + r*n elements).  Violations
+ *     return PURLIN_ERR_ALIAS.
+ *   Sizes.  1 <= R <= PURLIN_MAX_RANKS.  A call with no elements to move is
+ *     a valid no-op.
+ *   Device faults.  A bounded wait that expires inside a kernel records
+ *     PURLIN_ERR_TIMEOUT in the context's error word; purlin_check reports it.
+ */
+#ifndef PURLIN_H
+#define PURLIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PURLIN_MAX_RANKS 64
+
+typedef struct purlin_ctx purlin_ctx;   /* opaque; created by purlin_init */
+typedef void *purlin_stream;            /* a cudaStream_t (NULL = legacy default stream) */
+
+typedef enum { PURLIN_F32 = 0, PURLIN_BF16 = 1 } purlin_dtype;
+
+/* The consume operation of a collective (§3.1): copy or reduce (sum). */
+typedef enum { PURLIN_COPY = 0, PURLIN_SUM = 1 } purlin_op;
+
+/* Rank-relative layouts (§3.1).
+ *   PACKED      a rank buffer holds one contiguous region: the rank's own.
+ *   SCATTERED   a rank buffer holds R regions, region k belonging to rank k.
+ *   TRANSPOSED  a rank buffer holds R regions, region k coming from rank k
+ *               (the per-pair blocks of the input transposed across ranks). */
+typedef enum {
+    PURLIN_PACKED = 0,
+    PURLIN_SCATTERED = 1,
+    PURLIN_TRANSPOSED = 2
+} purlin_layout_kind;
+
+typedef struct {
+    int32_t in;   /* purlin_layout_kind of the inputs */
+    int32_t out;  /* purlin_layout_kind of the outputs */
+} purlin_layout;
+
+typedef enum {
+    PURLIN_OK = 0,
+    PURLIN_ERR_INVALID_ARG = 1,   /* null pointer, bad R, count not divisible, ... */
+    PURLIN_ERR_ALIGNMENT = 2,     /* a device pointer is not 16-byte aligned */
+    PURLIN_ERR_UNSUPPORTED = 3,   /* wrong op or layout pair for the collective */
+    PURLIN_ERR_ALIAS = 4,         /* forbidden overlap between buffers */
+    PURLIN_ERR_OOM = 5,           /* host or device allocation failed */
+    PURLIN_ERR_CUDA = 6,          /* a CUDA runtime call failed */
+    PURLIN_ERR_TIMEOUT = 7        /* a bounded device-side wait expired */
+} purlin_status;
+
+/* ---------------------------------------------------------------- context */
+
+/* Create a context for R rank buffers whose work is enqueued on `stream`
+ * (the pages' `initialize(rank, world, stream, memory)`, project README,
+ * "Host-side", reshaped for one process holding all R ranks).  Allocates the
+ * device flag array (2 parities x 65536 u64, zeroed once here) and a device
+ * error word on the current CUDA device, and reads the device's SM count
+ * and shared-memory limit.  The epoch (paper summary §4.3) starts at 1.
+ * Errors: INVALID_ARG (R out of range, out == NULL), CUDA, OOM. */
+purlin_status purlin_init(int R, purlin_stream stream, purlin_ctx **out);
+
+/* Wait for the context's stream, free the context's device memory and the
+ * context itself (README "finalize").  NULL is a no-op. */
+purlin_status purlin_finalize(purlin_ctx *ctx);
+
+/* Switch the stream later calls enqueue on.  Waits for the old stream first,
+ * so plan memory freed later is never still in use there. */
+purlin_status purlin_set_stream(purlin_ctx *ctx, purlin_stream stream);
+
+/* ------------------------------------------------------------ collectives */
+
+/* AllReduce (§2.1; §3.1: ReduceScatter then AllGather, composed as one
+ * SCATTERED -> SCATTERED reduction).  src[r], dst[r]: n elements each.
+ * dst[d][i] = round(sum_{s=0..R-1} src[s][i]) for every d, summed in rank
+ * order in binary32.  op must be SUM, layout {SCATTERED, SCATTERED}.
+ * In-place (src[r] == dst[r] for every r) is allowed. */
+purlin_status purlin_all_reduce(purlin_ctx *ctx, const void *const src[], void *const dst[],
+                                size_t n, purlin_dtype dtype, purlin_op op,
+                                purlin_layout layout);
+
+/* ReduceScatter (§2.1; §3.1 SCATTERED -> PACKED reduction).  src[s]: n
+ * elements, n divisible by R (else INVALID_ARG), M = n / R.  dst[r]: M
+ * elements, dst[r][i] = round(sum_s src[s][r*M + i]).  op SUM. */
+purlin_status purlin_reduce_scatter(purlin_ctx *ctx, const void *const src[], void *const dst[],
+                                    size_t n, purlin_dtype dtype, purlin_op op,
+                                    purlin_layout layout);
+
+/* AllGather (§2.1; §3.1 PACKED -> SCATTERED copy; README "Understanding
+ * totalBytes": the output holds every contribution).  src[s]: n elements;
+ * dst[d]: R*n elements, dst[d][s*n + i] = src[s][i], bitwise.  op COPY.
+ * In-place (src[r] == dst[r] + r*n elements for every r) is allowed. */
+purlin_status purlin_all_gather(purlin_ctx *ctx, const void *const src[], void *const dst[],
+                                size_t n, purlin_dtype dtype, purlin_op op,
+                                purlin_layout layout);
+
+/* AllToAll (§2.1; §3.1 SCATTERED -> TRANSPOSED copy).  src[s], dst[d]: n
+ * elements, n divisible by R, M = n / R.  dst[d][s*M + i] = src[s][d*M + i],
+ * bitwise.  op COPY. */
+purlin_status purlin_all_to_all(purlin_ctx *ctx, const void *const src[], void *const dst[],
+                                size_t n, purlin_dtype dtype, purlin_op op,
+                                purlin_layout layout);
+
+/* AllGatherV (§2.1 variable-length variants; §C.4: each rank contributes
+ * its share).  counts: host array of R element counts; src[s] holds
+ * counts[s] elements; dst[d] holds T = sum(counts) elements and
+ * dst[d][D_s + i] = src[s][i] with D_s = sum_{t<s} counts[t].  op COPY,
+ * layout {PACKED, SCATTERED}. */
+purlin_status purlin_all_gather_v(purlin_ctx *ctx, const void *const src[], void *const dst[],
+                                  const size_t counts[], purlin_dtype dtype, purlin_op op,
+                                  purlin_layout layout);
+
+/* ReduceScatterV (§C.4: the output of rank r is its share).  Every src[s]
+ * holds T = sum(counts) elements; dst[r] holds counts[r] elements,
+ * dst[r][i] = round(sum_s src[s][D_r + i]).  op SUM, layout
+ * {SCATTERED, PACKED}. */
+purlin_status purlin_reduce_scatter_v(purlin_ctx *ctx, const void *const src[],
+                                      void *const dst[], const size_t counts[],
+                                      purlin_dtype dtype, purlin_op op, purlin_layout layout);
+
+/* AllToAllV (§2.1, §C.4).  counts: host array of R*R element counts, row s
+ * = source, column d = destination.  src[s] holds sum_d C[s][d] elements
+ * packed by destination in destination order; dst[d] holds sum_s C[s][d]
+ * elements packed by source in source order:
+ * dst[d][Q_d[s] + i] = src[s][S_s[d] + i], S_s[d] = sum_{d'<d} C[s][d'],
+ * Q_d[s] = sum_{s'<s} C[s'][d].  op COPY, layout {SCATTERED, TRANSPOSED}. */
+purlin_status purlin_all_to_all_v(purlin_ctx *ctx, const void *const src[], void *const dst[],
+                                  const size_t counts[], purlin_dtype dtype, purlin_op op,
+                                  purlin_layout layout);
+
+/* ----------------------------------------------------------------- status */
+
+/* Wait for the context's stream, then read and clear the device error word.
+ * Returns PURLIN_ERR_TIMEOUT if a bounded wait expired in any earlier call
+ * (the outputs of that call are then unspecified), CUDA if the stream
+ * reported an error, else OK. */
+purlin_status purlin_check(purlin_ctx *ctx);
+
+/* Static English name of a status code; never NULL. */
+const char *purlin_status_string(purlin_status status);
+
+/* ---------------------------------------------------------------- policy */
+
+/* Codesign policy knobs (paper summary §4.2: crossover, chunk sizes, CTA
+ * allocation, pipeline depth, tuned per collective and GPU; applications
+ * may override).  0 means "the built-in policy" for every knob. */
+typedef enum {
+    PURLIN_OPT_VARIANT = 0,          /* 0 auto, 1 latency (vector ld/st), 2 throughput (TMA ring) */
+    PURLIN_OPT_CROSSOVER_BYTES = 1,  /* per-rank message bytes at or below which auto picks latency */
+    PURLIN_OPT_AR_MODE = 2,          /* AllReduce: 0 auto, 1 fused, 2 composed (RS CTAs notify, AG CTAs consume) */
+    PURLIN_OPT_CHUNK_BYTES = 3,      /* bytes per source per chunk in the TMA ring */
+    PURLIN_OPT_STAGES = 4,           /* TMA ring depth */
+    PURLIN_OPT_CTAS = 5,             /* CTAs of a throughput launch */
+    PURLIN_OPT_SPIN_TIMEOUT_NS = 6,  /* bound on a cross-CTA flag wait (default 100 ms) */
+    PURLIN_OPT_DROP_NOTIFY = 7,      /* host-side fault injection: chunk whose notify is skipped; -1 off */
+    PURLIN_OPT_LAT_CTAS = 8          /* max CTAs of a latency launch */
+} purlin_option;
+
+/* Set one knob; INVALID_ARG for an unknown knob or a value out of range. */
+purlin_status purlin_set_option(purlin_ctx *ctx, purlin_option opt, int64_t value);
+purlin_status purlin_get_option(purlin_ctx *ctx, purlin_option opt, int64_t *value);
+
+/* What the last collective call of this context enqueued. */
+typedef struct {
+    int32_t variant;      /* 0 nothing launched, 1 latency, 2 throughput, 3 throughput composed AllReduce */
+    int32_t grid;         /* CTAs */
+    int32_t block;        /* threads per CTA */
+    int32_t stages;       /* TMA ring depth (throughput) */
+    int64_t chunk_bytes;  /* bytes per source per chunk (throughput) */
+    int64_t chunks;       /* TMA chunks */
+    int64_t units;        /* 16-byte vector units outside the TMA ring */
+    int64_t segments;     /* segments in the compiled plan */
+    int64_t smem_bytes;   /* dynamic shared memory per CTA */
+    uint64_t epoch;       /* epoch the launch used (§4.3) */
+    uint64_t epoch_next;  /* epoch of the next call */
+} purlin_launch_info;
+
+purlin_status purlin_last_launch(const purlin_ctx *ctx, purlin_launch_info *info);
+
+/* --------------------------------------------------- host-side inspection */
+
+typedef enum {
+    PURLIN_COLL_ALL_REDUCE = 0,
+    PURLIN_COLL_REDUCE_SCATTER = 1,
+    PURLIN_COLL_ALL_GATHER = 2,
+    PURLIN_COLL_ALL_TO_ALL = 3,
+    PURLIN_COLL_ALL_GATHER_V = 4,
+    PURLIN_COLL_REDUCE_SCATTER_V = 5,
+    PURLIN_COLL_ALL_TO_ALL_V = 6
+} purlin_collective;
+
+/* One contiguous transfer of a compiled plan (the layout compiler's output). */
+typedef struct {
+    uint64_t src_off;      /* byte offset into the source buffer(s) */
+    uint64_t dst_off;      /* byte offset into the destination buffer(s) */
+    uint64_t bytes;        /* bytes moved per source */
+    int32_t src_rank;      /* source rank, or -1: reduce over every rank at src_off */
+    int32_t dst_rank;      /* destination rank, or -1: every rank at dst_off */
+    int32_t skip_rank;     /* with dst_rank -1: a rank left out, or -1 */
+    int32_t src_is_dst;    /* 1: the source buffers are the destination array */
+    int32_t sync;          /* 0 none, 1 notify a flag after writing, 2 wait on a flag before reading */
+    int32_t tma;           /* 1 if the 16-byte-aligned body goes through the TMA ring */
+    uint64_t head_bytes;   /* bytes before the aligned body (vector path) */
+    uint64_t tail_bytes;   /* bytes after it (vector path) */
+    uint64_t chunk_begin;  /* index of the segment's first TMA chunk */
+    uint64_t chunk_bytes;  /* bytes per source per TMA chunk */
+    uint64_t unit_begin;   /* index of the segment's first vector unit */
+} purlin_segment;
+
+/* Run the argument checks and the layout compiler of one call without a
+ * GPU: pointer values are compared, never dereferenced.  `counts` is NULL
+ * for the uniform collectives (then `n` is used), R entries for AGV/RSV and
+ * R*R for AllToAllV.  variant: 1 latency, 2 throughput; ar_mode as for
+ * PURLIN_OPT_AR_MODE; chunk_bytes 0 = default.  Writes up to `cap`
+ * segments, the segment count, the TMA chunk count and the unit count.
+ * Returns the status the real call would return for these arguments. */
+purlin_status purlin_plan_inspect(purlin_collective coll, int R, const void *const src[],
+                                  void *const dst[], size_t n, const size_t counts[],
+                                  purlin_dtype dtype, purlin_op op, purlin_layout layout,
+                                  int variant, int ar_mode, uint64_t chunk_bytes,
+                                  purlin_segment *segs, size_t cap, size_t *nseg,
+                                  uint64_t *nchunks, uint64_t *nunits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PURLIN_H */

@@ -1,0 +1,73 @@
+"""The C-ABI library loads and exports every function include/purlin.h declares
+(no GPU needed; nothing here calls into the device)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "purlin.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(purlin_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def P():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import collective_datapath_atom_gb300 as P
+
+    return P
+
+
+def test_header_declares_the_collectives():
+    names = declared_functions()
+    for n in ("purlin_init", "purlin_finalize", "purlin_all_reduce", "purlin_reduce_scatter",
+              "purlin_all_gather", "purlin_all_to_all", "purlin_all_gather_v",
+              "purlin_reduce_scatter_v", "purlin_all_to_all_v", "purlin_check",
+              "purlin_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(P):
+    names = declared_functions()
+    lib = ctypes.CDLL(P.LIB_PATH)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    nm = subprocess.run(["nm", "-D", "--defined-only", P.LIB_PATH], capture_output=True,
+                        text=True, check=True).stdout
+    exported = set(line.split()[-1] for line in nm.splitlines() if line.strip())
+    assert set(names) <= exported
+    # the binding marshals exactly the declared set
+    assert set(P._SIGNATURES) == set(names)
+
+
+def test_status_strings(P):
+    for s in range(0, 8):
+        assert P.status_string(s)
+    assert P.status_string(99) == "unknown status"
+
+
+def test_init_without_a_gpu_fails_cleanly(P):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p(0)
+    st = P.lib.purlin_init(8, None, ctypes.byref(h))
+    assert st == P.PURLIN_ERR_CUDA and not h.value
+    assert P.lib.purlin_init(0, None, ctypes.byref(h)) == P.PURLIN_ERR_INVALID_ARG
+    assert P.lib.purlin_init(65, None, ctypes.byref(h)) == P.PURLIN_ERR_INVALID_ARG
+    assert P.lib.purlin_finalize(None) == P.PURLIN_OK
+    assert P.lib.purlin_check(None) == P.PURLIN_ERR_INVALID_ARG
+
+
+def test_library_does_not_link_the_oracle(P):
+    deps = subprocess.run(["nm", "-D", P.LIB_PATH], capture_output=True, text=True).stdout
+    assert "oracle_" not in deps

@@ -1,0 +1,440 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Every comparison is bit for bit: copies are bitwise and reductions follow
+the same fixed rank order in binary32 with one rounding ("Purlin: Separating
+Orchestration from the Datapath of Collectives" §3.3 SCORE; "Purlin" README,
+"Deterministic Reduction").  Outputs sit between guard zones that must stay
+untouched.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+GUARD = 256
+ES = {0: 4, 1: 2}
+
+
+@pytest.fixture(scope="module")
+def P():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import collective_datapath_atom_gb300 as mod
+
+    torch.cuda.set_device(0)
+    return mod
+
+
+@pytest.fixture
+def ctx8(P):
+    c = P.purlin_init(8, torch.cuda.current_stream())
+    yield c
+    c.close()
+
+
+def make_ctx(P, R):
+    return P.purlin_init(R, torch.cuda.current_stream())
+
+
+# ------------------------------------------------------------- buffers ----
+
+class Guarded:
+    """A device byte buffer with guard zones on both sides."""
+
+    def __init__(self, nbytes, fill=0x5A):
+        self.nbytes = nbytes
+        self.t = torch.full((nbytes + 2 * GUARD,), fill, dtype=torch.uint8, device="cuda")
+        self.fill = fill
+
+    @property
+    def ptr(self):
+        return self.t.data_ptr() + GUARD
+
+    def body(self):
+        return self.t[GUARD:GUARD + self.nbytes].cpu().numpy()
+
+    def guards_ok(self):
+        g = torch.cat([self.t[:GUARD], self.t[GUARD + self.nbytes:]])
+        return bool((g == self.fill).all().item())
+
+
+def upload(arrays):
+    out = []
+    for a in arrays:
+        b = Guarded(a.nbytes, fill=0xC3)
+        if a.nbytes:
+            b.t[GUARD:GUARD + a.nbytes].copy_(torch.from_numpy(a.view(np.uint8).copy()))
+        out.append(b)
+    return out
+
+
+def outputs(sizes):
+    return [Guarded(s) for s in sizes]
+
+
+def run(P, ctx, coll, ins, out_sizes, dtype, n=0, counts=None):
+    src = upload(ins)
+    dst = outputs(out_sizes)
+    f = getattr(P, "purlin_" + coll)
+    arg = counts if coll.endswith("_v") else n
+    f(ctx, [b.ptr for b in src], [b.ptr for b in dst], arg, dtype)
+    P.purlin_check(ctx)
+    for b in src + dst:
+        assert b.guards_ok(), "guard zone overwritten"
+    return [b.body() for b in dst], src
+
+
+def oracle_of(coll, ins, dtype, counts=None, R=None):
+    if coll == "all_reduce":
+        return oracle.all_reduce(ins, dtype)
+    if coll == "reduce_scatter":
+        return oracle.reduce_scatter(ins, dtype)
+    if coll == "all_gather":
+        return oracle.all_gather(ins, dtype)
+    if coll == "all_to_all":
+        return oracle.all_to_all(ins, dtype)
+    if coll == "all_gather_v":
+        return oracle.all_gather_v(ins, counts, dtype)
+    if coll == "reduce_scatter_v":
+        return oracle.reduce_scatter_v(ins, counts, dtype)
+    return oracle.all_to_all_v(ins, np.asarray(counts).reshape(len(ins), -1), dtype)
+
+
+def out_sizes(coll, R, n, counts, es):
+    if coll in ("all_reduce", "all_to_all"):
+        return [n * es] * R
+    if coll == "reduce_scatter":
+        return [n // R * es] * R
+    if coll == "all_gather":
+        return [R * n * es] * R
+    if coll == "all_gather_v":
+        return [sum(counts) * es] * R
+    if coll == "reduce_scatter_v":
+        return [c * es for c in counts]
+    C = np.asarray(counts).reshape(R, R)
+    return [int(C[:, d].sum()) * es for d in range(R)]
+
+
+def in_lengths(coll, R, n, counts):
+    if coll in ("all_reduce", "all_to_all", "reduce_scatter", "all_gather"):
+        return [n] * R
+    if coll == "all_gather_v":
+        return list(counts)
+    if coll == "reduce_scatter_v":
+        return [sum(counts)] * R
+    C = np.asarray(counts).reshape(R, R)
+    return [int(C[s].sum()) for s in range(R)]
+
+
+def gen_inputs(lengths, dtype, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for L in lengths:
+        x = rng.standard_normal(L).astype(np.float32)
+        out.append(x if dtype == 0 else workloads.to_bf16_bits(x))
+    return out
+
+
+def assert_same(got, want, what):
+    for d, (g, w) in enumerate(zip(got, want)):
+        w8 = w.view(np.uint8)
+        if not np.array_equal(g, w8):
+            bad = np.nonzero(g != w8)[0]
+            raise AssertionError(f"{what}: rank {d} differs at byte {bad[0]} "
+                                 f"({bad.size} bytes differ of {w8.size})")
+
+
+# -------------------------------------------------------------- cases ----
+
+def size_cases(coll, R):
+    """(n, counts) pairs: tiny, ragged, several chunks, unaligned phases."""
+    rng = np.random.default_rng(R * 31 + len(coll))
+    if coll in ("all_reduce", "all_gather"):
+        return [(n, None) for n in (1, 7, 8, 33, 4096, 70001, 3 * 65536 + 5)]
+    if coll in ("reduce_scatter", "all_to_all"):
+        return [(R * m, None) for m in (1, 3, 8, 517, 16384, 40000 + 3)]
+    if coll in ("all_gather_v", "reduce_scatter_v"):
+        cs = [[int(x) for x in rng.integers(0, 50, size=R)],
+              [int(x) for x in rng.integers(1000, 90000, size=R)],
+              [8192 * (k + 1) for k in range(R)]]
+        cs[0][0] = 0
+        return [(0, c) for c in cs]
+    cs = [[int(x) for x in rng.integers(0, 20, size=R * R)],
+          [int(x) for x in rng.integers(0, 9000, size=R * R)],
+          [1024 * int(x) for x in rng.integers(0, 40, size=R * R)]]
+    return [(0, c) for c in cs]
+
+
+COLLS = ["all_reduce", "reduce_scatter", "all_gather", "all_to_all", "all_gather_v",
+         "reduce_scatter_v", "all_to_all_v"]
+
+
+@pytest.mark.parametrize("coll", COLLS)
+@pytest.mark.parametrize("dtype", [0, 1], ids=["f32", "bf16"])
+@pytest.mark.parametrize("variant", [1, 2], ids=["latency", "throughput"])
+@pytest.mark.parametrize("R", [1, 3, 8])
+def test_parity(P, coll, dtype, variant, R):
+    ctx = make_ctx(P, R)
+    try:
+        P.purlin_set_option(ctx, P.PURLIN_OPT_VARIANT, variant)
+        for k, (n, counts) in enumerate(size_cases(coll, R)):
+            ins = gen_inputs(in_lengths(coll, R, n, counts), dtype, seed=1000 * k + R)
+            got, _ = run(P, ctx, coll, ins, out_sizes(coll, R, n, counts, ES[dtype]), dtype, n,
+                         counts)
+            want = oracle_of(coll, ins, dtype, counts)
+            assert_same(got, want, f"{coll} R={R} dtype={dtype} variant={variant} n={n}")
+            info = P.purlin_last_launch(ctx)
+            assert info["variant"] in (0, variant)
+    finally:
+        ctx.close()
+
+
+@pytest.mark.parametrize("dtype", [0, 1], ids=["f32", "bf16"])
+@pytest.mark.parametrize("R", [2, 3, 8])
+def test_allreduce_composed_mode(P, dtype, R):
+    """SNAC across CTAs: reducing CTAs notify per-chunk flags, gathering CTAs
+    acquire them (paper summary §3.2 composed AllReduce)."""
+    ctx = make_ctx(P, R)
+    try:
+        P.purlin_set_option(ctx, P.PURLIN_OPT_VARIANT, 2)
+        P.purlin_set_option(ctx, P.PURLIN_OPT_AR_MODE, 2)
+        for k, n in enumerate((64, 4096 + 3, 100003, 1 << 20)):
+            for chunk in (0, 512):
+                P.purlin_set_option(ctx, P.PURLIN_OPT_CHUNK_BYTES, chunk)
+                ins = gen_inputs([n] * R, dtype, seed=77 + k)
+                got, _ = run(P, ctx, "all_reduce", ins, [n * ES[dtype]] * R, dtype, n)
+                assert_same(got, oracle.all_reduce(ins, dtype), f"composed n={n}")
+                assert P.purlin_last_launch(ctx)["variant"] == 3
+    finally:
+        ctx.close()
+
+
+def test_repeated_calls_need_no_reset(P, ctx8):
+    """Epoch parity and monotonic flags (paper summary §4.3): many calls in a
+    row, no flag reset, each correct; the epoch advances by an odd amount."""
+    P.purlin_set_option(ctx8, P.PURLIN_OPT_VARIANT, 2)
+    P.purlin_set_option(ctx8, P.PURLIN_OPT_AR_MODE, 2)
+    P.purlin_set_option(ctx8, P.PURLIN_OPT_CHUNK_BYTES, 256)
+    n = 300000
+    last = None
+    for k in range(6):
+        ins = gen_inputs([n] * 8, 1, seed=k)
+        got, _ = run(P, ctx8, "all_reduce", ins, [2 * n] * 8, 1, n)
+        assert_same(got, oracle.all_reduce(ins, 1), f"call {k}")
+        info = P.purlin_last_launch(ctx8)
+        assert (info["epoch_next"] - info["epoch"]) % 2 == 1
+        if last is not None:
+            assert info["epoch"] == last
+        last = info["epoch_next"]
+
+
+def test_in_place_allreduce(P, ctx8):
+    for variant, mode in ((1, 0), (2, 1), (2, 2)):
+        P.purlin_set_option(ctx8, P.PURLIN_OPT_VARIANT, variant)
+        P.purlin_set_option(ctx8, P.PURLIN_OPT_AR_MODE, mode)
+        n = 50001
+        ins = gen_inputs([n] * 8, 1, seed=5)
+        bufs = upload(ins)
+        P.purlin_all_reduce(ctx8, [b.ptr for b in bufs], [b.ptr for b in bufs], n, 1)
+        P.purlin_check(ctx8)
+        want = oracle.all_reduce(ins, 1)
+        assert_same([b.body() for b in bufs], want, f"in-place AR variant {variant}")
+        assert all(b.guards_ok() for b in bufs)
+
+
+def test_in_place_allgather(P, ctx8):
+    for variant in (1, 2):
+        P.purlin_set_option(ctx8, P.PURLIN_OPT_VARIANT, variant)
+        for n in (4096, 333):
+            ins = gen_inputs([n] * 8, 1, seed=n)
+            outs = outputs([8 * n * 2] * 8)
+            for r in range(8):
+                outs[r].t[GUARD + r * n * 2:GUARD + (r + 1) * n * 2].copy_(
+                    torch.from_numpy(ins[r].view(np.uint8).copy()))
+            srcs = [outs[r].ptr + r * n * 2 for r in range(8)]
+            P.purlin_all_gather(ctx8, srcs, [o.ptr for o in outs], n, 1)
+            P.purlin_check(ctx8)
+            assert_same([o.body() for o in outs], oracle.all_gather(ins, 1), "in-place AG")
+
+
+def test_empty_calls_are_noops(P, ctx8):
+    P.purlin_all_reduce(ctx8, [0] * 8, [0] * 8, 0, 1)
+    assert P.purlin_last_launch(ctx8)["variant"] == 0
+    P.purlin_all_gather_v(ctx8, [0] * 8, [0] * 8, [0] * 8, 1)
+    P.purlin_all_to_all_v(ctx8, [0] * 8, [0] * 8, [0] * 64, 0)
+    P.purlin_check(ctx8)
+
+
+def test_argument_errors_enqueue_nothing(P, ctx8):
+    n = 64
+    ins = gen_inputs([n] * 8, 1, seed=1)
+    src = upload(ins)
+    dst = outputs([n * 2] * 8)
+    with pytest.raises(P.PurlinError) as e:
+        P.purlin_all_reduce(ctx8, [b.ptr for b in src], [b.ptr for b in dst], n, 1,
+                            op=P.PURLIN_COPY)
+    assert e.value.status == P.PURLIN_ERR_UNSUPPORTED
+    with pytest.raises(P.PurlinError) as e:
+        P.purlin_all_reduce(ctx8, [b.ptr + 2 for b in src], [b.ptr for b in dst], n - 1, 1)
+    assert e.value.status == P.PURLIN_ERR_ALIGNMENT
+    P.purlin_check(ctx8)
+    assert all((torch.from_numpy(b.body()) == 0x5A).all() for b in dst)
+
+
+def test_dropped_notify_times_out_and_recovers(P, ctx8):
+    """Fault injection from the host: the notify of one chunk is skipped, so
+    the gathering CTA's bounded acquire expires.  The kernel records
+    PURLIN_ERR_TIMEOUT and ends; the context stays usable."""
+    P.purlin_set_option(ctx8, P.PURLIN_OPT_VARIANT, 2)
+    P.purlin_set_option(ctx8, P.PURLIN_OPT_AR_MODE, 2)
+    P.purlin_set_option(ctx8, P.PURLIN_OPT_SPIN_TIMEOUT_NS, 2_000_000)   # 2 ms
+    P.purlin_set_option(ctx8, P.PURLIN_OPT_DROP_NOTIFY, 3)
+    n = 1 << 16
+    ins = gen_inputs([n] * 8, 1, seed=9)
+    src = upload(ins)
+    dst = outputs([2 * n] * 8)
+    P.purlin_all_reduce(ctx8, [b.ptr for b in src], [b.ptr for b in dst], n, 1)
+    assert P.purlin_check_status(ctx8) == P.PURLIN_ERR_TIMEOUT
+    assert P.purlin_check_status(ctx8) == P.PURLIN_OK   # the word was cleared
+    P.purlin_set_option(ctx8, P.PURLIN_OPT_DROP_NOTIFY, -1)
+    got, _ = run(P, ctx8, "all_reduce", ins, [2 * n] * 8, 1, n)
+    assert_same(got, oracle.all_reduce(ins, 1), "after recovery")
+
+
+def test_golden_fixtures_on_gpu(P):
+    """The hand-derived fixtures, straight through the CUDA path."""
+    import json
+    import os
+
+    gdir = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    g = json.load(open(os.path.join(gdir, "score_order_f32.json")))
+    ins = [np.array([int(h, 16) for h in row], dtype=np.uint32).view(np.float32)
+           for row in g["inputs_f32_hex"]]
+    want = np.array([int(h, 16) for h in g["output_f32_hex"]], dtype=np.uint32)
+    for variant in (1, 2):
+        ctx = make_ctx(P, 3)
+        P.purlin_set_option(ctx, P.PURLIN_OPT_VARIANT, variant)
+        got, _ = run(P, ctx, "all_reduce", ins, [len(want) * 4] * 3, 0, len(want))
+        ctx.close()
+        for o in got:
+            assert np.array_equal(o.view(np.uint32), want)
+    g = json.load(open(os.path.join(gdir, "score_round_once_bf16.json")))
+    for case in g["cases"]:
+        ins = [np.array([int(h, 16) for h in row], dtype=np.uint16)
+               for row in case["inputs_bf16_hex"]]
+        want = np.array([int(h, 16) for h in case["output_bf16_hex"]], dtype=np.uint16)
+        ctx = make_ctx(P, len(ins))
+        got, _ = run(P, ctx, "all_reduce", ins, [2] * len(ins), 1, 1)
+        ctx.close()
+        for o in got:
+            assert np.array_equal(o.view(np.uint16), want)
+
+
+def test_nan_and_signed_zero_copies_are_bitwise(P, ctx8):
+    n = 1000
+    ins = [np.full(n, 0, dtype=np.uint32) for _ in range(8)]
+    for s in range(8):
+        ins[s][::3] = 0x7FC00000 | (s * 977 + 1)     # quiet NaNs with payloads
+        ins[s][1::3] = 0x80000000                    # -0.0
+        ins[s][2::3] = 0xFF800001 + s                # signalling NaN patterns
+    ins = [x.view(np.float32) for x in ins]
+    for variant in (1, 2):
+        P.purlin_set_option(ctx8, P.PURLIN_OPT_VARIANT, variant)
+        got, _ = run(P, ctx8, "all_gather", ins, [8 * n * 4] * 8, 0, n)
+        assert_same(got, oracle.all_gather(ins, 0), "NaN AllGather")
+        C = np.full((8, 8), n // 8)
+        got, _ = run(P, ctx8, "all_to_all", ins, [n * 4] * 8, 0, n)
+        assert_same(got, oracle.all_to_all(ins, 0), "NaN AllToAll")
+
+
+# ------------------------------------------------------- full-size configs --
+
+def _device(arrays):
+    return [torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+            for a in arrays]
+
+
+def test_cfg_allreduce_f32_exact(P, ctx8):
+    w = workloads.AR_F32_R8_4096
+    ins = workloads.inputs_for(w)
+    src = _device(ins)
+    dst = [torch.empty(w.n, dtype=torch.float32, device="cuda") for _ in range(8)]
+    P.purlin_all_reduce(ctx8, src, dst, w.n, 0)
+    P.purlin_check(ctx8)
+    exact = np.sum(np.stack(ins).astype(np.int64), axis=0).astype(np.float32)
+    for d in range(8):
+        got = dst[d].cpu().numpy()
+        assert np.array_equal(got, exact)
+        assert np.array_equal(got.view(np.uint32), oracle.all_reduce(ins, 0)[d].view(np.uint32))
+
+
+def test_cfg_allgather_bf16_full(P, ctx8):
+    w = workloads.AG_BF16_R8_8MI
+    ins = workloads.inputs_for(w)
+    src = _device(ins)
+    dst = [torch.empty(8 * w.n, dtype=torch.int16, device="cuda") for _ in range(8)]
+    P.purlin_all_gather(ctx8, src, dst, w.n, 1)
+    P.purlin_check(ctx8)
+    assert P.purlin_last_launch(ctx8)["variant"] == 2
+    want = torch.from_numpy(np.concatenate(ins).view(np.int16)).cuda()   # concatenation invariant
+    for d in range(8):
+        assert torch.equal(dst[d], want)
+    sample = oracle.all_gather([x[:4096] for x in ins], 1)[0].view(np.int16)
+    assert np.array_equal(dst[3][:4096].cpu().numpy(), sample[:4096])
+
+
+def test_cfg_reducescatter_bf16_full(P, ctx8):
+    w = workloads.RS_BF16_R8_128MI
+    ins = workloads.inputs_for(w)
+    src = _device(ins)
+    M = w.n // 8
+    dst = [torch.empty(M, dtype=torch.int16, device="cuda") for _ in range(8)]
+    P.purlin_reduce_scatter(ctx8, src, dst, w.n, 1)
+    P.purlin_check(ctx8)
+    want = oracle.reduce_scatter(ins, 1)
+    for r in range(8):
+        assert np.array_equal(dst[r].cpu().numpy().view(np.uint16), want[r])
+
+
+def test_cfg_alltoallv_moe_full(P, ctx8):
+    C, ins = workloads.moe_dispatch()
+    counts = (C * workloads.MOE_HIDDEN).reshape(-1)
+    src = _device(ins)
+    dst = [torch.empty(int(counts.reshape(8, 8)[:, d].sum()), dtype=torch.int16, device="cuda")
+           for d in range(8)]
+    P.purlin_all_to_all_v(ctx8, src, dst, counts.tolist(), 1)
+    P.purlin_check(ctx8)
+    want = oracle.all_to_all_v(ins, counts.reshape(8, 8), 1)
+    for d in range(8):
+        assert np.array_equal(dst[d].cpu().numpy().view(np.uint16), want[d])
+
+
+@pytest.mark.parametrize("batch", workloads.AR_BF16_SWEEP_BATCHES)
+def test_cfg_allreduce_sweep(P, ctx8, batch):
+    w = workloads.ar_sweep_workload(batch)
+    ins = workloads.inputs_for(w)
+    src = _device(ins)
+    dst = [torch.empty(w.n, dtype=torch.int16, device="cuda") for _ in range(8)]
+    P.purlin_all_reduce(ctx8, src, dst, w.n, 1)
+    P.purlin_check(ctx8)
+    if batch <= 1024:
+        want = oracle.all_reduce(ins, 1)[0]
+        for d in range(8):
+            assert np.array_equal(dst[d].cpu().numpy().view(np.uint16), want)
+    else:
+        rng = np.random.default_rng(batch)
+        idx = np.unique(np.concatenate([rng.integers(0, w.n, 2000), [0, w.n - 1]]))
+        want = np.array([oracle.reduce_at(ins, 1, int(i)) for i in idx], dtype=np.uint16)
+        for d in range(8):
+            got = dst[d][torch.from_numpy(idx).cuda()].cpu().numpy().view(np.uint16)
+            assert np.array_equal(got, want)
+        # every output holds the same bits
+        for d in range(1, 8):
+            assert torch.equal(dst[d], dst[0])
