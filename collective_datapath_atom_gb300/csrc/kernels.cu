@@ -462,11 +462,12 @@ __global__ void __launch_bounds__(kTputMaxThreads, 1) purlin_throughput_kernel(
             const Seg &sg = *g.sg;
             if (sg.src_rank >= 0) continue;
             const uint32_t slot = k % S;
-            if (!ring_wait(&full[slot], (k / S) & 1u, &ctl, p.err, kSiteRingFull, true)) break;
             const uint32_t b = kr & 1u;
-            if (kr >= 2 &&
-                !ring_wait(&ofree[b], ((kr >> 1) & 1u) ^ 1u, &ctl, p.err, kSiteOutFree, true))
-                break;
+            // Every lane waits (bounded) and the warp leaves together.
+            bool ok = ring_wait(&full[slot], (k / S) & 1u, &ctl, p.err, kSiteRingFull, true);
+            if (ok && kr >= 2)
+                ok = ring_wait(&ofree[b], ((kr >> 1) & 1u) ^ 1u, &ctl, p.err, kSiteOutFree, true);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
             const unsigned char *sp = ring + (size_t)slot * p.slot_stride;
             unsigned char *op = outt + (size_t)b * p.out_tile;
             const uint32_t cb = sg.chunk_bytes;

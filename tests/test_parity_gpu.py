@@ -252,7 +252,7 @@ def test_in_place_allreduce(P, ctx8):
 def test_in_place_allgather(P, ctx8):
     for variant in (1, 2):
         P.purlin_set_option(ctx8, P.PURLIN_OPT_VARIANT, variant)
-        for n in (4096, 333):
+        for n in (4096, 336, 100008):
             ins = gen_inputs([n] * 8, 1, seed=n)
             outs = outputs([8 * n * 2] * 8)
             for r in range(8):
@@ -262,6 +262,13 @@ def test_in_place_allgather(P, ctx8):
             P.purlin_all_gather(ctx8, srcs, [o.ptr for o in outs], n, 1)
             P.purlin_check(ctx8)
             assert_same([o.body() for o in outs], oracle.all_gather(ins, 1), "in-place AG")
+    # r*n elements off a 16-byte boundary: the in-place input is misaligned
+    n = 333
+    outs = outputs([8 * n * 2] * 8)
+    with pytest.raises(P.PurlinError) as e:
+        P.purlin_all_gather(ctx8, [outs[r].ptr + r * n * 2 for r in range(8)],
+                            [o.ptr for o in outs], n, 1)
+    assert e.value.status == P.PURLIN_ERR_ALIGNMENT
 
 
 def test_empty_calls_are_noops(P, ctx8):
