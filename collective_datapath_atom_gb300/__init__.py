@@ -107,6 +107,9 @@ _SIGNATURES = {
                                                ctypes.c_int, purlin_layout]),
     "purlin_all_to_all_v": (ctypes.c_int, [_CTX, _VPP, _VPP, _SZP, ctypes.c_int, ctypes.c_int,
                                            purlin_layout]),
+    "purlin_all_reduce_noalloc": (ctypes.c_int, [ctypes.c_int, _VPP, _VPP, ctypes.c_size_t,
+                                                 ctypes.c_int, ctypes.c_int, purlin_layout,
+                                                 ctypes.c_void_p]),
     "purlin_check": (ctypes.c_int, [_CTX]),
     "purlin_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "purlin_set_option": (ctypes.c_int, [_CTX, ctypes.c_int, ctypes.c_int64]),
@@ -263,6 +266,19 @@ def purlin_reduce_scatter_v(ctx, src, dst, counts, dtype, op=None, layout=None):
 def purlin_all_to_all_v(ctx, src, dst, counts, dtype, op=None, layout=None):
     """``counts``: R*R element counts, row s = source, column d = destination."""
     _varlen(lib.purlin_all_to_all_v, "all_to_all_v", ctx, src, dst, counts, dtype, op, layout)
+
+
+def purlin_all_reduce_noalloc(R, src, dst, n, dtype, op=None, layout=None, stream=None):
+    """AllReduce with no device allocation (static scratch inside the
+    library); see include/purlin.h for its limits."""
+    dflt_op, dflt_layout = LAYOUTS["all_reduce"]
+    op = dflt_op if op is None else op
+    layout = dflt_layout if layout is None else layout
+    ps, _keep1 = _ptr_array(src)
+    pd, _keep2 = _ptr_array(dst)
+    _ok(lib.purlin_all_reduce_noalloc(int(R), ps, pd, int(n), int(dtype), int(op),
+                                      _layout(layout), ctypes.c_void_p(_stream_handle(stream))),
+        "purlin_all_reduce_noalloc")
 
 
 def purlin_check(ctx) -> int:

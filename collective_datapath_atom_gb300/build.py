@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpurlin.so")
-SOURCES = ["plan.cpp", "api.cpp", "kernels.cu"]
+SOURCES = ["plan.cpp", "api.cpp", "kernels.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -167,6 +167,29 @@ purlin_status purlin_all_to_all_v(purlin_ctx *ctx, const void *const src[], void
                                   const size_t counts[], purlin_dtype dtype, purlin_op op,
                                   purlin_layout layout);
 
+/* AllReduce without any device allocation.  The pages have no counterpart
+ * to this entry point; it is an addition of this library for callers that
+ * cannot call cudaMalloc at the time they reduce: code running while a CUDA
+ * graph is being captured, and engines that give all free device memory to
+ * their own pool and let no library take more.  Same contract and result
+ * (bit for bit) as purlin_all_reduce with PURLIN_OPT_AR_MODE = composed,
+ * without a context: R (1..31) rank buffers, n elements each, enqueued on
+ * `stream`.  Its scratch (per-chunk flags and an error word, 128 KiB + 8
+ * bytes) is a fixed device array inside the library, held by every GPU that
+ * loads it until the process exits.  Limit: at most 8192 reduce chunks of
+ * 32 KiB / R bytes per source, i.e. n * element size <= 8192 * (32768 / R)
+ * bytes per rank (32 MiB at R = 8); larger calls and R > 31 return
+ * INVALID_ARG.  The first call on a device looks up the array's address,
+ * sets kernel attributes and zeroes the array with a blocking cudaMemset:
+ * make it before any stream capture.  Every call shares the array (it keeps
+ * the previous call's contents; the error word is cleared per call), so
+ * calls that overlap on the GPU race: order them on one stream.  Device-side
+ * timeouts are not reported here.  Errors as for purlin_all_reduce, plus
+ * CUDA if the set-up or the launch fails. */
+purlin_status purlin_all_reduce_noalloc(int R, const void *const src[], void *const dst[],
+                                        size_t n, purlin_dtype dtype, purlin_op op,
+                                        purlin_layout layout, purlin_stream stream);
+
 /* ----------------------------------------------------------------- status */
 
 /* Wait for the context's stream, then read and clear the device error word.
