@@ -140,17 +140,26 @@ class ClockSampler:
 
 # --------------------------------------------------------------- setup ----
 
-def setup_workload(name: str, device):
-    """Device inputs/outputs and a closure that runs one call."""
+def setup_workload(name: str, device, elements: int = 0):
+    """Device inputs/outputs and a closure that runs one call.  `elements`
+    (if set) replaces the elements per rank of the AllGather, ReduceScatter
+    or AllReduce workload: a smaller case of the same kernel for profiling."""
+    import dataclasses
+
     import torch
 
     if name == workloads.AG_BF16_R8_8MI.name:
         w = workloads.AG_BF16_R8_8MI
+        if elements:
+            w = dataclasses.replace(w, n=elements, name=f"allgather_bf16_R8_n{elements}")
         ins = workloads.inputs_for(w)
         out_elems = [w.R * w.n] * w.R
         call = ("all_gather", w.n)
     elif name == workloads.RS_BF16_R8_128MI.name:
         w = workloads.RS_BF16_R8_128MI
+        if elements:
+            w = dataclasses.replace(w, n=elements - elements % 8,
+                                    name=f"reducescatter_bf16_R8_n{elements}")
         ins = workloads.inputs_for(w)
         out_elems = [w.n // w.R] * w.R
         call = ("reduce_scatter", w.n)
@@ -166,7 +175,7 @@ def setup_workload(name: str, device):
         out_elems = [w.n] * w.R
         call = ("all_reduce", w.n)
     elif name.startswith("allreduce_bf16_R8_b"):
-        batch = int(name.split("_b")[1].split("x")[0])
+        batch = int(name.rsplit("_b", 1)[1].split("x")[0])
         w = workloads.ar_sweep_workload(batch)
         ins = workloads.inputs_for(w)
         out_elems = [w.n] * w.R
@@ -295,7 +304,7 @@ def _workload_by_name(name):
         if w.name == name:
             return w
     if name.startswith("allreduce_bf16_R8_b"):
-        return workloads.ar_sweep_workload(int(name.split("_b")[1].split("x")[0]))
+        return workloads.ar_sweep_workload(int(name.rsplit("_b", 1)[1].split("x")[0]))
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -332,7 +341,8 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(device)
     stream = torch.cuda.Stream(device)
     ctx = P.purlin_init(8, stream)
-    w, ins, src, dst, call, algo_bytes, in_bytes, out_bytes = setup_workload(args.workload, device)
+    w, ins, src, dst, call, algo_bytes, in_bytes, out_bytes = setup_workload(
+        args.workload, device, args.elements)
     run = make_runner(P, ctx, w, call)
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
 
@@ -440,6 +450,137 @@ def run_gpu(args, rank, world, local_rank):
     return line
 
 
+# --------------------------------------------------------------- sweep ----
+
+def _events_us(torch, stream, fn, reps, flush=None):
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for i in range(reps):
+            if flush is not None:
+                flush.zero_()
+            starts[i].record(stream)
+            fn()
+            ends[i].record(stream)
+    stream.synchronize()
+    us = np.array([a.elapsed_time(b) * 1e3 for a, b in zip(starts, ends)])
+    return float(np.median(us)), float(np.percentile(us, 10)), float(np.percentile(us, 90))
+
+
+def _graph_us(torch, stream, fn, k):
+    """Device time per launch from a CUDA graph of k launches."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(k):
+            fn()
+    g.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(5):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (5 * k)
+
+
+def sweep(args):
+    """Every workload, both variants across the AllReduce sweep, composed vs
+    fused AllReduce, and small-message latency against the empty-kernel
+    floor.  Timing inputs are seeded N(0,1) values drawn on the device (the
+    values do not change the work); the parity tests use the CPU-generated
+    workloads."""
+    import torch
+
+    import collective_datapath_atom_gb300 as P
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    ctx = P.purlin_init(8, stream)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    peak, peak_kind = measured_peaks()
+    gen = torch.Generator(device=device)
+    gen.manual_seed(4)
+    rows = []
+
+    def emit(row):
+        rows.append(row)
+        print(json.dumps(row), flush=True)
+
+    def bufs(n_in, n_out, dtype=1):
+        tdt = torch.float32 if dtype == 0 else torch.bfloat16
+        src = [torch.randn(n_in, generator=gen, device=device, dtype=torch.float32).to(tdt)
+               for _ in range(8)]
+        dst = [torch.empty(n_out, device=device, dtype=tdt) for _ in range(8)]
+        return src, dst
+
+    def setopt(variant, mode=0):
+        P.purlin_set_option(ctx, P.PURLIN_OPT_VARIANT, variant)
+        P.purlin_set_option(ctx, P.PURLIN_OPT_AR_MODE, mode)
+
+    # ---- small messages (<= 2 KiB per rank) against the empty-kernel floor,
+    # timed from C through the public ABI (no Python in the timed path)
+    exe = os.path.join(ROOT, "collective_datapath_atom_gb300", "purlin_bench")
+    for coll in ("AR", "RS", "AG", "A2A", "AGV", "RSV", "A2AV"):
+        res = subprocess.run([exe, coll, "256", "2048", "200", "200", "10", "42"],
+                             capture_output=True, text=True, check=True)
+        for line in res.stdout.splitlines():
+            r = json.loads(line)
+            r["row"] = "small"
+            emit(r)
+
+    # ---- AllReduce bf16 sweep, batch x 4096, both variants, L2 flushed
+    for b in workloads.AR_BF16_SWEEP_BATCHES:
+        n = b * workloads.HIDDEN
+        src, dst = bufs(n, n)
+        algo = 2 * 8 * n * 2
+        reps = 200 if n <= (1 << 20) else 30
+        for variant, mode in ((1, 0), (2, 1), (2, 2), (0, 0)):
+            if variant == 1 and n > (16 << 20):
+                continue
+            setopt(variant, mode)
+            call = lambda: P.purlin_all_reduce(ctx, src, dst, n, 1)   # noqa: E731
+            call()
+            P.purlin_check(ctx)
+            info = P.purlin_last_launch(ctx)
+            med, p10, p90 = _events_us(torch, stream, call, reps, flush)
+            warm = _events_us(torch, stream, call, reps)[0] if n <= (8 << 20) else None
+            emit({"row": "ar_sweep", "batch": b, "bytes_per_rank": 2 * n,
+                  "mode": {(1, 0): "latency", (2, 1): "throughput fused",
+                           (2, 2): "throughput composed", (0, 0): "auto"}[(variant, mode)],
+                  "chosen_variant": info["variant"], "us_cold": med, "p10": p10, "p90": p90,
+                  "us_warm": warm, "gbs_cold": algo / (med * 1e-6) / 1e9,
+                  "frac_cold": algo / (med * 1e-6) / 1e9 / peak})
+        del src, dst
+        torch.cuda.empty_cache()
+    setopt(0)
+
+    # ---- the large workloads, L2 flushed
+    for name in (workloads.AG_BF16_R8_8MI.name, workloads.RS_BF16_R8_128MI.name,
+                 workloads.A2AV_BF16_R8_MOE.name, workloads.AR_F32_R8_4096.name):
+        w, ins, src, dst, call, algo, _, _ = setup_workload(name, device)
+        run = make_runner(P, ctx, w, call)
+        for variant in (0, 1, 2):
+            setopt(variant)
+            run(src, dst)
+            P.purlin_check(ctx)
+            info = P.purlin_last_launch(ctx)
+            med, p10, p90 = _events_us(torch, stream, lambda: run(src, dst), 20, flush)
+            emit({"row": "workload", "workload": w.name, "variant_opt": variant,
+                  "variant": info["variant"], "us": med, "p10": p10, "p90": p90,
+                  "gbs": algo / (med * 1e-6) / 1e9, "frac": algo / (med * 1e-6) / 1e9 / peak,
+                  "grid": info["grid"], "block": info["block"], "stages": info["stages"]})
+        del ins, src, dst
+        torch.cuda.empty_cache()
+    ctx.close()
+    if args.report:
+        with open(args.report, "w") as f:
+            for r in rows:
+                f.write(json.dumps(r) + "\n")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -451,7 +592,15 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--elements", type=int, default=0,
+                    help="elements per rank (a smaller case of the same kernel)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="measure every workload, both variants and the launch floor")
+    ap.add_argument("--report", default="", help="with --sweep: also write the rows here")
     args = ap.parse_args()
+    if args.sweep:
+        sweep(args)
+        return
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -33,7 +33,7 @@ PURLIN_ERR_TIMEOUT = 7
 
 (PURLIN_OPT_VARIANT, PURLIN_OPT_CROSSOVER_BYTES, PURLIN_OPT_AR_MODE, PURLIN_OPT_CHUNK_BYTES,
  PURLIN_OPT_STAGES, PURLIN_OPT_CTAS, PURLIN_OPT_SPIN_TIMEOUT_NS, PURLIN_OPT_DROP_NOTIFY,
- PURLIN_OPT_LAT_CTAS) = range(9)
+ PURLIN_OPT_LAT_CTAS, PURLIN_OPT_LAT_BLOCK) = range(10)
 
 (PURLIN_COLL_ALL_REDUCE, PURLIN_COLL_REDUCE_SCATTER, PURLIN_COLL_ALL_GATHER,
  PURLIN_COLL_ALL_TO_ALL, PURLIN_COLL_ALL_GATHER_V, PURLIN_COLL_REDUCE_SCATTER_V,
@@ -71,7 +71,7 @@ class purlin_segment(ctypes.Structure):
                 ("bytes", ctypes.c_uint64), ("src_rank", ctypes.c_int32),
                 ("dst_rank", ctypes.c_int32), ("skip_rank", ctypes.c_int32),
                 ("src_is_dst", ctypes.c_int32), ("sync", ctypes.c_int32), ("tma", ctypes.c_int32),
-                ("head_bytes", ctypes.c_uint64), ("tail_bytes", ctypes.c_uint64),
+                ("shift", ctypes.c_int32), ("head_bytes", ctypes.c_uint64), ("tail_bytes", ctypes.c_uint64),
                 ("chunk_begin", ctypes.c_uint64), ("chunk_bytes", ctypes.c_uint64),
                 ("unit_begin", ctypes.c_uint64)]
 
@@ -110,6 +110,7 @@ _SIGNATURES = {
     "purlin_all_reduce_noalloc": (ctypes.c_int, [ctypes.c_int, _VPP, _VPP, ctypes.c_size_t,
                                                  ctypes.c_int, ctypes.c_int, purlin_layout,
                                                  ctypes.c_void_p]),
+    "purlin_empty_launch": (ctypes.c_int, [ctypes.c_void_p]),
     "purlin_check": (ctypes.c_int, [_CTX]),
     "purlin_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "purlin_set_option": (ctypes.c_int, [_CTX, ctypes.c_int, ctypes.c_int64]),
@@ -279,6 +280,10 @@ def purlin_all_reduce_noalloc(R, src, dst, n, dtype, op=None, layout=None, strea
     _ok(lib.purlin_all_reduce_noalloc(int(R), ps, pd, int(n), int(dtype), int(op),
                                       _layout(layout), ctypes.c_void_p(_stream_handle(stream))),
         "purlin_all_reduce_noalloc")
+
+
+def purlin_empty_launch(stream=None):
+    _ok(lib.purlin_empty_launch(ctypes.c_void_p(_stream_handle(stream))), "purlin_empty_launch")
 
 
 def purlin_check(ctx) -> int:

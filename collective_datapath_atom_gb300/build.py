@@ -15,6 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpurlin.so")
+BENCH = os.path.join(HERE, "purlin_bench")
 SOURCES = ["plan.cpp", "api.cpp", "kernels.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -27,9 +28,9 @@ def _nvcc() -> str:
 
 
 def _stale() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(BENCH):
         return True
-    t = os.path.getmtime(LIB)
+    t = min(os.path.getmtime(LIB), os.path.getmtime(BENCH))
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
     deps.append(os.path.join(HERE, "..", "include", "purlin.h"))
     deps.append(__file__)
@@ -70,6 +71,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
     tmp = LIB + f".tmp{os.getpid()}"
     subprocess.check_call([nvcc, *ARCH, "-shared", "-o", tmp, *objs])
     os.replace(tmp, LIB)
+    # the C benchmark program links the library through its public ABI
+    tmp = BENCH + f".tmp{os.getpid()}"
+    subprocess.check_call([nvcc, "-O2", "-I", os.path.join(HERE, "..", "include"),
+                           os.path.join(CSRC, "purlin_bench.c"), "-o", tmp, "-L", HERE,
+                           "-lpurlin", "-Xlinker", "-rpath,$ORIGIN", "-lm"])
+    os.replace(tmp, BENCH)
     if verbose:
         with open(os.path.join(BUILD, "ptxas_kernels.cu.txt")) as f:
             sys.stdout.write(f.read())

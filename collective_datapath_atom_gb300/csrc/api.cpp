@@ -24,17 +24,51 @@ using namespace purlin;
 
 namespace {
 
-constexpr int kNumOptions = 9;
+constexpr int kNumOptions = 10;
 constexpr size_t kPlanCacheCap = 64;
 
 // Built-in policy.
-constexpr int64_t kDefaultCrossover = 256 * 1024;        // bytes per rank message
-constexpr int64_t kDefaultSlotBytes = 32 * 1024;         // shared memory per ring stage
-constexpr int64_t kDefaultStages = 6;
+constexpr int64_t kInspectChunkBytes = 32 * 1024;        // plan_inspect default chunk
 constexpr int64_t kDefaultTimeoutNs = 100 * 1000 * 1000; // 100 ms
 constexpr int kLatBlock = 256;
 constexpr int kCopyConsumerWarps = 4;
 constexpr int kReduceConsumerWarps = 8;
+
+// Policy per collective (codesign policy, paper summary §4.2), measured on
+// GB300 over 256 B..64 MiB per rank and at the workloads' sizes.
+// Crossover: per-rank message bytes up to which the one-shot vector kernel
+// beats the staged ring (it keeps ~150k threads' loads in flight, so for
+// reductions it stays competitive up to several MiB).
+// Ring shape:
+//   ReduceScatter(V)  one destination per reduced chunk: large per-source
+//                     chunks (96 KiB per stage), 2 stages;
+//   AllReduce         R stores per reduced vector: 32 KiB per stage, 3 stages;
+//   AllGather(V)      one staged tile, R bulk stores: 8 KiB chunks, 2 stages
+//                     (shallow read-ahead leaves HBM to the writes);
+//   AllToAll(V)       one load, one store per chunk: 16 KiB chunks, 3 stages.
+struct Policy {
+    uint32_t chunk;       // bytes per source per chunk
+    uint32_t stages;
+    uint64_t crossover;   // latency kernel at or below this many bytes per rank
+};
+
+Policy policy_for(purlin_collective coll, int R) {
+    auto clamp16 = [](uint64_t v, uint64_t lo, uint64_t hi) {
+        return (uint32_t)(std::min(hi, std::max(lo, v)) & ~uint64_t(15));
+    };
+    switch (coll) {
+        case PURLIN_COLL_REDUCE_SCATTER:
+        case PURLIN_COLL_REDUCE_SCATTER_V:
+            return {clamp16(98304 / (uint64_t)R, 1024, 16384), 2, 4ull << 20};
+        case PURLIN_COLL_ALL_REDUCE:
+            return {clamp16(32768 / (uint64_t)R, 512, 8192), 3, 8ull << 20};
+        case PURLIN_COLL_ALL_GATHER:
+        case PURLIN_COLL_ALL_GATHER_V:
+            return {8192, 2, 128ull << 10};
+        default:
+            return {16384, 3, 128ull << 10};
+    }
+}
 
 struct CacheEntry {
     std::string key;
@@ -141,22 +175,32 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
     if (st != PURLIN_OK) return st;
 
     // ---- policy (§4.2)
+    const Policy shape = policy_for(c.coll, c.R);
     int variant = (int)ctx->opt[PURLIN_OPT_VARIANT];
     if (variant == 0) {
-        const int64_t xo = ctx->opt[PURLIN_OPT_CROSSOVER_BYTES] > 0
-                               ? ctx->opt[PURLIN_OPT_CROSSOVER_BYTES]
-                               : kDefaultCrossover;
-        variant = (int64_t)message_bytes(c) <= xo ? kVariantLatency : kVariantThroughput;
+        const uint64_t xo = ctx->opt[PURLIN_OPT_CROSSOVER_BYTES] > 0
+                                ? (uint64_t)ctx->opt[PURLIN_OPT_CROSSOVER_BYTES]
+                                : shape.crossover;
+        variant = message_bytes(c) <= xo ? kVariantLatency : kVariantThroughput;
     }
     const int ar_mode = (int)ctx->opt[PURLIN_OPT_AR_MODE];
-    const int64_t slot_opt = ctx->opt[PURLIN_OPT_CHUNK_BYTES];
+    const int64_t chunk_opt = ctx->opt[PURLIN_OPT_CHUNK_BYTES];
     // CHUNK_BYTES is bytes per source per chunk: a reduce stage holds R of them.
-    const uint32_t copy_chunk = (uint32_t)(slot_opt > 0 ? slot_opt : kDefaultSlotBytes);
-    const uint32_t red_slot = (uint32_t)(slot_opt > 0 ? slot_opt * c.R : kDefaultSlotBytes);
+    const uint32_t chunk = (uint32_t)(chunk_opt > 0 ? chunk_opt : shape.chunk);
+    const uint32_t copy_chunk = chunk;
+    const uint32_t red_slot = chunk * (uint32_t)c.R;
 
     CacheEntry *e = nullptr;
     st = get_plan(ctx, c, variant, ar_mode, red_slot, copy_chunk, &e);
     if (st != PURLIN_OK) return st;
+    if (ctx->opt[PURLIN_OPT_VARIANT] == 0 && variant == kVariantThroughput &&
+        2 * e->plan.loose_bytes > e->plan.total_bytes) {
+        // Most bytes sit at 16-byte phases the ring cannot move (ragged V
+        // counts): the vector kernel, with every thread shifting, is faster.
+        variant = kVariantLatency;
+        st = get_plan(ctx, c, variant, ar_mode, red_slot, copy_chunk, &e);
+        if (st != PURLIN_OK) return st;
+    }
     const Plan &pl = e->plan;
 
     purlin_launch_info info = {};
@@ -191,7 +235,9 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
     if (variant == kVariantLatency) {
         const int64_t cap = ctx->opt[PURLIN_OPT_LAT_CTAS] > 0 ? ctx->opt[PURLIN_OPT_LAT_CTAS]
                                                               : 4 * (int64_t)ctx->sms;
-        int block = (int)std::min<uint64_t>(kLatBlock, (pl.nunits + 31) / 32 * 32);
+        const int max_block = ctx->opt[PURLIN_OPT_LAT_BLOCK] > 0
+                                  ? (int)ctx->opt[PURLIN_OPT_LAT_BLOCK] : kLatBlock;
+        int block = (int)std::min<uint64_t>(max_block, (pl.nunits + 31) / 32 * 32);
         uint64_t want = (pl.nunits + block - 1) / block;
         a.block = block;
         a.grid = (int)std::max<uint64_t>(1, std::min<uint64_t>(want, (uint64_t)cap));
@@ -199,13 +245,12 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
         ce = launch_latency(a);
     } else {
         const uint32_t slot_stride = (pl.slot_bytes + 127u) & ~127u;
-        const uint32_t out_tile = pl.has_reduce ? pl.red_chunk : 0;
         uint32_t stages = (uint32_t)(ctx->opt[PURLIN_OPT_STAGES] > 0 ? ctx->opt[PURLIN_OPT_STAGES]
-                                                                     : kDefaultStages);
-        stages = std::max<uint32_t>(2, stages);
+                                                                     : shape.stages);
+        stages = std::min<uint32_t>(32, std::max<uint32_t>(2, stages));
         const uint32_t limit = (uint32_t)ctx->max_smem - 1024;
-        while (stages > 2 && throughput_smem(stages, slot_stride, out_tile) > limit) --stages;
-        const uint32_t smem = throughput_smem(stages, slot_stride, out_tile);
+        while (stages > 2 && throughput_smem(stages, slot_stride) > limit) --stages;
+        const uint32_t smem = throughput_smem(stages, slot_stride);
         if (smem > limit) return PURLIN_ERR_UNSUPPORTED;
         const int cw = pl.has_reduce ? kReduceConsumerWarps : kCopyConsumerWarps;
         const int block = 32 * (2 + cw);
@@ -274,6 +319,7 @@ purlin_status purlin_init(int R, purlin_stream stream, purlin_ctx **out) {
     ctx->stream = static_cast<cudaStream_t>(stream);
     for (int i = 0; i < kNumOptions; ++i) ctx->opt[i] = 0;
     ctx->opt[PURLIN_OPT_DROP_NOTIFY] = -1;
+    ctx->opt[PURLIN_OPT_VARIANT] = env_or("PURLIN_VARIANT", 0);
     ctx->opt[PURLIN_OPT_CROSSOVER_BYTES] = env_or("PURLIN_CROSSOVER_BYTES", 0);
     ctx->opt[PURLIN_OPT_STAGES] = env_or("PURLIN_STAGES", 0);
     ctx->opt[PURLIN_OPT_CHUNK_BYTES] = env_or("PURLIN_CHUNK_BYTES", 0);
@@ -376,6 +422,11 @@ purlin_status purlin_all_to_all_v(purlin_ctx *ctx, const void *const src[], void
                src, dst);
 }
 
+purlin_status purlin_empty_launch(purlin_stream stream) {
+    return launch_empty(static_cast<cudaStream_t>(stream)) == cudaSuccess ? PURLIN_OK
+                                                                          : PURLIN_ERR_CUDA;
+}
+
 purlin_status purlin_check(purlin_ctx *ctx) {
     if (ctx == nullptr) return PURLIN_ERR_INVALID_ARG;
     if (cudaStreamSynchronize(ctx->stream) != cudaSuccess) return PURLIN_ERR_CUDA;
@@ -415,10 +466,13 @@ purlin_status purlin_set_option(purlin_ctx *ctx, purlin_option opt, int64_t valu
                 return PURLIN_ERR_INVALID_ARG;
             break;
         case PURLIN_OPT_STAGES:
-            if (value < 0 || value == 1 || value > 64) return PURLIN_ERR_INVALID_ARG;
+            if (value < 0 || value == 1 || value > 32) return PURLIN_ERR_INVALID_ARG;
             break;
         case PURLIN_OPT_DROP_NOTIFY:
             if (value < -1) return PURLIN_ERR_INVALID_ARG;
+            break;
+        case PURLIN_OPT_LAT_BLOCK:
+            if (value < 0 || value > 256 || value % 32 != 0) return PURLIN_ERR_INVALID_ARG;
             break;
         default:
             if (value < 0) return PURLIN_ERR_INVALID_ARG;
@@ -451,8 +505,9 @@ purlin_status purlin_plan_inspect(purlin_collective coll, int R, const void *con
     CallDesc c = make_desc(coll, R, n, counts, dtype, op, layout);
     purlin_status st = validate_call(c, src, dst);
     if (st != PURLIN_OK) return st;
-    const uint32_t copy_chunk = (uint32_t)(chunk_bytes ? chunk_bytes : kDefaultSlotBytes);
-    const uint32_t red_slot = (uint32_t)(chunk_bytes ? chunk_bytes * (uint64_t)R : kDefaultSlotBytes);
+    const uint32_t copy_chunk = (uint32_t)(chunk_bytes ? chunk_bytes : kInspectChunkBytes);
+    const uint32_t red_slot =
+        (uint32_t)(chunk_bytes ? chunk_bytes * (uint64_t)R : kInspectChunkBytes);
     Plan p;
     st = compile_plan(c, variant, ar_mode, red_slot, copy_chunk, &p);
     if (st != PURLIN_OK) return st;
@@ -471,6 +526,7 @@ purlin_status purlin_plan_inspect(purlin_collective coll, int R, const void *con
         o.src_is_dst = s.src_is_dst;
         o.sync = s.sync;
         o.tma = s.tma;
+        o.shift = s.shift;
         o.head_bytes = s.head;
         o.tail_bytes = s.tail;
         o.chunk_begin = s.chunk_begin;

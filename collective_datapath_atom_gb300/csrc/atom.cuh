@@ -157,6 +157,28 @@ __device__ __forceinline__ uint4 ld_v4(const void *p) {
     return v;
 }
 
+// 128-bit load that may allocate in L1: the shifted path reads each source
+// vector from two neighbouring threads.
+__device__ __forceinline__ uint4 ld_v4_l1(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Bytes [sh, sh + 16) of the 32-byte pair (a, b), 0 <= sh < 16.
+__device__ __forceinline__ uint4 shift_pair(uint4 a, uint4 b, uint32_t sh) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const uint32_t k = sh >> 2, r = (sh & 3u) * 8u;
+    uint32_t o[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i)
+        o[i] = k == 0 ? w[i] : k == 1 ? w[i + 1] : k == 2 ? w[i + 2] : w[i + 3];
+    return make_uint4(__funnelshift_r(o[0], o[1], r), __funnelshift_r(o[1], o[2], r),
+                      __funnelshift_r(o[2], o[3], r), __funnelshift_r(o[3], o[4], r));
+}
+
 __device__ __forceinline__ void st_v4(void *p, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)

@@ -23,12 +23,16 @@
 //                      the stage's mbarrier.  For a chunk that depends on
 //                      another CTA's chunk it first acquires that chunk's
 //                      flag (bounded spin).
-//   warps 2..          Consume (reduce): SCORE over the R tiles into an
-//                      output tile; also the ragged head/tail units.
-//   warp 1 (one lane)  Consume (copy) / write-back: cp.async.bulk shared ->
-//                      global to one or all destinations; then Notify:
-//                      once a chunk's stores have completed, release-store
-//                      epoch + generation into its flag.
+//   warps 2..          Consume (reduce): SCORE over the R tiles, each thread
+//                      storing its 16-byte results straight to one or all
+//                      destinations.  Also copies whose source sits at
+//                      another 16-byte phase (staged as an aligned hull and
+//                      shifted into place), and the ragged head/tail units.
+//   warp 1 (one lane)  Consume (copy): cp.async.bulk shared -> global to one
+//                      or all destinations.  Notify: for a reduce chunk that
+//                      other CTAs wait on, once the consumer warps report it
+//                      stored (after a GPU-scope fence), release-store
+//                      epoch + generation into its flag, then free the stage.
 // Every wait is bounded; an expired wait records PURLIN_ERR_TIMEOUT in the
 // error word and the CTA winds down (its own bulk copies are waited for).
 #include <cuda_runtime.h>
@@ -40,8 +44,6 @@ namespace purlin {
 
 namespace {
 
-constexpr int kNotifyLag = 4;      // bulk groups kept in flight before notifying
-constexpr int kNotifyQueue = 16;
 constexpr int kTputMaxThreads = 512;
 constexpr uint64_t kRingWaitNs = 2000000000ull;   // 2 s bound on a ring wait
 
@@ -61,7 +63,6 @@ struct KParams {
     uint32_t flag_slots;
     uint32_t stages;
     uint32_t slot_stride;
-    uint32_t out_tile;
     int32_t nseg;
     int32_t R;
 };
@@ -69,6 +70,20 @@ struct KParams {
 template <class P>
 __device__ __forceinline__ const Seg *seg_table(const P &p) {
     return p.segs_dev != nullptr ? p.segs_dev : p.segs;
+}
+
+// Copy the segment table into shared memory with every thread of the CTA
+// (one round of parallel loads instead of a chain of dependent parameter
+// reads in each lookup).  Tables too large for the parameter block stay in
+// global memory and are read from there.
+template <class P>
+__device__ __forceinline__ const Seg *stage_segs(const P &p, Seg *sm) {
+    if (p.segs_dev != nullptr) return p.segs_dev;
+    const uint64_t *from = reinterpret_cast<const uint64_t *>(p.segs);
+    uint64_t *to = reinterpret_cast<uint64_t *>(sm);
+    const int words = p.nseg * (int)(sizeof(Seg) / sizeof(uint64_t));
+    for (int i = threadIdx.x; i < words; i += blockDim.x) to[i] = from[i];
+    return sm;
 }
 
 // Last segment whose first chunk (unit) index is <= x: the one holding x.
@@ -128,25 +143,50 @@ __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
         hi = (b < e ? b : e) - sg.dst_off;
     }
     const int R = p.R;
-    const bool vec = (hi - lo == 16) && (((sg.src_off + lo) & 15u) == 0);
+    // A full destination window is written with one 128-bit store.  Its 16
+    // source bytes are one aligned vector (same phase), or two aligned
+    // vectors shifted into place when both lie inside the segment's source
+    // range (so no byte outside the segment is read); else element by element.
+    const bool full = hi - lo == 16;
+    const uint64_t sx = sg.src_off + lo;
+    const uint32_t sh = (uint32_t)(sx & 15u);
+    const uint64_t sxa = sx - sh;
+    const bool vec = full && sh == 0;
+    const bool shifted = full && sh != 0 && sxa >= sg.src_off && sxa + 32 <= sg.src_off + sg.bytes;
     const uint64_t doff = sg.dst_off + lo;
 
     if (sg.src_rank >= 0) {   // copy, bitwise
         const char *s = static_cast<const char *>(sg.src_is_dst ? p.dst[sg.src_rank]
                                                                 : p.src[sg.src_rank]) +
                         sg.src_off + lo;
+        // Read the window once (16 bytes, as a vector or element by element),
+        // then write it to every destination.
+        constexpr int NE = 16 / ES;
+        const int ne = (int)((hi - lo) / ES);
+        uint4 v = make_uint4(0, 0, 0, 0);
+        uint32_t e[NE];
+        if (vec) {
+            v = atom::ld_v4(s);
+        } else if (shifted) {
+            const char *a = s - sh;
+            v = atom::shift_pair(atom::ld_v4_l1(a), atom::ld_v4_l1(a + 16), sh);
+        } else {
+#pragma unroll
+            for (int j = 0; j < NE; ++j)
+                e[j] = j < ne ? (ES == 4 ? *reinterpret_cast<const uint32_t *>(s + j * ES)
+                                         : *reinterpret_cast<const uint16_t *>(s + j * ES))
+                              : 0u;
+        }
         auto put = [&](char *d) {
             if (d == s) return;   // in-place AllGather: the block is already there
-            if (vec) {
-                atom::st_v4(d, atom::ld_v4(s));
+            if (vec || shifted) {
+                atom::st_v4(d, v);
             } else {
-                for (uint64_t j = 0; j < hi - lo; j += ES) {
-                    if (ES == 4)
-                        *reinterpret_cast<uint32_t *>(d + j) =
-                            *reinterpret_cast<const uint32_t *>(s + j);
-                    else
-                        *reinterpret_cast<uint16_t *>(d + j) =
-                            *reinterpret_cast<const uint16_t *>(s + j);
+#pragma unroll
+                for (int j = 0; j < NE; ++j) {
+                    if (j >= ne) break;
+                    if (ES == 4) *reinterpret_cast<uint32_t *>(d + j * ES) = e[j];
+                    else *reinterpret_cast<uint16_t *>(d + j * ES) = (uint16_t)e[j];
                 }
             }
         };
@@ -161,12 +201,18 @@ __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
 
     // reduce (SCORE): rank order 0..R-1, binary32, one rounding at the end
     const uint64_t soff = sg.src_off + lo;
-    if (vec) {
+    if (vec || shifted) {
+        // source j's 16 bytes: one aligned vector, or two shifted into place
+        auto load = [&](int j) -> uint4 {
+            const char *b = static_cast<const char *>(p.src[j]) + soff;
+            if (vec) return atom::ld_v4(b);
+            return atom::shift_pair(atom::ld_v4_l1(b - sh), atom::ld_v4_l1(b - sh + 16), sh);
+        };
         float acc[V::VE];
         uint4 v[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-            if (j < R) v[j] = atom::ld_v4(static_cast<const char *>(p.src[j]) + soff);
+            if (j < R) v[j] = load(j);
         V::init(acc, v[0]);
 #pragma unroll
         for (int j = 1; j < 8; ++j)
@@ -175,8 +221,7 @@ __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
             for (int s0 = 8; s0 < R; s0 += 8) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    if (s0 + j < R)
-                        v[j] = atom::ld_v4(static_cast<const char *>(p.src[s0 + j]) + soff);
+                    if (s0 + j < R) v[j] = load(s0 + j);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     if (s0 + j < R) V::add(acc, v[j]);
@@ -205,17 +250,30 @@ __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
     }
 }
 
+// Units u0, u0 + stride, ... of the plan: the first one's segment is found by
+// binary search, later ones by walking forward (units only increase), so
+// the search cost fades for threads that own many units.
+template <int DT, int MAXR, class P>
+__device__ __forceinline__ void units_loop(const P &p, const Seg *segs, uint64_t u0,
+                                           uint64_t stride) {
+    if (u0 >= p.nunits) return;
+    int si = seg_of_unit(segs, p.nseg, u0);
+    for (uint64_t u = u0; u < p.nunits; u += stride) {
+        while (si + 1 < p.nseg && segs[si + 1].unit_begin <= u) ++si;
+        do_unit<DT, MAXR>(p, segs[si], u - segs[si].unit_begin);
+    }
+}
+
 // ---------------------------------------------------------- latency kernel --
 
 template <int DT, int MAXR, int MAXSEG>
-__global__ void __launch_bounds__(256) purlin_latency_kernel(
+__global__ void __launch_bounds__(256, 2) purlin_latency_kernel(
     const __grid_constant__ KParams<MAXR, MAXSEG> p) {
-    const Seg *segs = seg_table(p);
+    __shared__ Seg s_segs[MAXSEG];
+    const Seg *segs = stage_segs(p, s_segs);
+    __syncthreads();
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-    for (uint64_t u = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; u < p.nunits; u += stride) {
-        const Seg &sg = segs[seg_of_unit(segs, p.nseg, u)];
-        do_unit<DT, MAXR>(p, sg, u - sg.unit_begin);
-    }
+    units_loop<DT, MAXR>(p, segs, (uint64_t)blockIdx.x * blockDim.x + threadIdx.x, stride);
 }
 
 // ------------------------------------------------------- throughput kernel --
@@ -301,28 +359,28 @@ __global__ void __launch_bounds__(kTputMaxThreads, 1) purlin_throughput_kernel(
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ Ctl ctl;
 
-    const Seg *segs = seg_table(p);
     const uint32_t S = p.stages;
     const int R = p.R;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ncw = (int)(blockDim.x >> 5) - 2;   // consumer warps
 
     unsigned char *ring = smem;
-    unsigned char *outt = smem + (size_t)S * p.slot_stride;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(outt + 2 * (size_t)p.out_tile);
-    uint64_t *full = bars;             // S: producer arrive + transaction bytes
-    uint64_t *empty = bars + S;        // S: ncw arrivals (consumer warps, or the writer)
-    uint64_t *ofull = bars + 2 * S;    // 2: ncw arrivals (consumer warps)
-    uint64_t *ofree = bars + 2 * S + 2;// 2: writer arrival
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)S * p.slot_stride);
+    uint64_t *full = bars;           // S: producer arrive + transaction bytes
+    uint64_t *empty = bars + S;      // S: ncw + 1 arrivals: every consumer warp and the writer
+    uint64_t *cdone = bars + 2 * S;  // S: ncw arrivals: a chunk to publish has been stored
+    // Every role waits on full[] for EVERY chunk, in order, and arrives once
+    // per chunk on empty[] (or, for a chunk to publish, the consumer warps on
+    // cdone[] and the writer on their behalf): a parity wait is only sound if
+    // the slot's previous phase is known complete, and a slot is refilled
+    // only after every role has passed it.
+    const Seg *segs = stage_segs(p, reinterpret_cast<Seg *>(bars + 3 * S));
 
     if (threadIdx.x == 0) {
         for (uint32_t i = 0; i < S; ++i) {
             atom::mbar_init(&full[i], 1);
-            atom::mbar_init(&empty[i], (uint32_t)ncw);
-        }
-        for (int i = 0; i < 2; ++i) {
-            atom::mbar_init(&ofull[i], (uint32_t)ncw);
-            atom::mbar_init(&ofree[i], 1);
+            atom::mbar_init(&empty[i], (uint32_t)ncw + 1u);
+            atom::mbar_init(&cdone[i], (uint32_t)ncw);
         }
         ctl.abort = 0;
         atom::mbar_init_fence();
@@ -331,168 +389,172 @@ __global__ void __launch_bounds__(kTputMaxThreads, 1) purlin_throughput_kernel(
 
     if (warp == 0) {
         // ---------------------------------------------------------- Stage --
-        if (lane == 0) {
-            const uint64_t pol = atom::policy_evict_first();
-            uint32_t k = 0;
-            for (uint64_t c = blockIdx.x; c < p.nchunks; c += gridDim.x, ++k) {
-                const uint32_t slot = k % S;
-                if (k >= S && !ring_wait(&empty[slot], ((k / S) & 1u) ^ 1u, &ctl, p.err,
-                                         kSiteRingEmpty, true))
-                    break;
-                const ChunkGeo g = chunk_geo(segs, p.nseg, c);
-                const Seg &sg = *g.sg;
-                if (sg.sync == kSyncWait) acquire_chunk(p, sg.dep_chunk + g.ci);
-                unsigned char *sp = ring + (size_t)slot * p.slot_stride;
-                if (sg.src_rank < 0) {
-                    atom::mbar_arrive_expect_tx(&full[slot], g.bytes * (uint32_t)R);
-                    for (int s = 0; s < R; ++s)
-                        atom::bulk_load(sp + (size_t)s * sg.chunk_bytes,
-                                        static_cast<const char *>(p.src[s]) + sg.src_off + g.off,
-                                        g.bytes, &full[slot], pol);
-                } else {
-                    const char *base = static_cast<const char *>(
-                        sg.src_is_dst ? p.dst[sg.src_rank] : p.src[sg.src_rank]);
-                    atom::mbar_arrive_expect_tx(&full[slot], g.bytes);
-                    atom::bulk_load(sp, base + sg.src_off + g.off, g.bytes, &full[slot], pol);
-                }
+        // The whole warp walks the chunk list; lane s issues the bulk load
+        // of source s, so the R loads of a chunk go out in parallel.
+        const uint64_t pol = atom::policy_evict_first();
+        uint32_t k = 0;
+        for (uint64_t c = blockIdx.x; c < p.nchunks; c += gridDim.x, ++k) {
+            const uint32_t slot = k % S;
+            bool ok = true;
+            if (k >= S)
+                ok = ring_wait(&empty[slot], ((k / S) & 1u) ^ 1u, &ctl, p.err, kSiteRingEmpty, true);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            const ChunkGeo g = chunk_geo(segs, p.nseg, c);
+            const Seg &sg = *g.sg;
+            if (sg.sync == kSyncWait && lane == 0) acquire_chunk(p, sg.dep_chunk + g.ci);
+            unsigned char *sp = ring + (size_t)slot * p.slot_stride;
+            const int nsrc = sg.src_rank < 0 ? R : 1;
+            // A shifted source is staged as its 16-byte aligned hull.
+            const uint32_t extra = sg.shift ? 16u : 0u;
+            const uint32_t tile = sg.chunk_bytes + extra;
+            const uint32_t ld_bytes = g.bytes + extra;
+            if (lane == 0) atom::mbar_arrive_expect_tx(&full[slot], ld_bytes * (uint32_t)nsrc);
+            __syncwarp();
+            for (int s = lane; s < nsrc; s += 32) {
+                const char *base =
+                    sg.src_rank < 0 ? static_cast<const char *>(p.src[s])
+                                    : static_cast<const char *>(sg.src_is_dst ? p.dst[sg.src_rank]
+                                                                              : p.src[sg.src_rank]);
+                atom::bulk_load(sp + (size_t)s * tile, base + sg.src_off + g.off - sg.shift,
+                                ld_bytes, &full[slot], pol);
             }
-            // Every load this thread issued must land before the CTA exits.
-            const uint32_t issued = k;
+        }
+        // Every load this warp issued must land before the CTA exits.
+        const uint32_t issued = k;
+        if (lane == 0)
             for (uint32_t j = issued > S ? issued - S : 0; j < issued; ++j)
                 ring_wait(&full[j % S], (j / S) & 1u, &ctl, p.err, kSiteRingFull, false);
-        }
     } else if (warp == 1) {
-        // ----------------------------------------- write-back and Notify --
-        if (lane == 0) {
-            const uint64_t pol = atom::policy_evict_first();
-            uint32_t k = 0, kr = 0;
-            int owed_kind = 0;          // staging owed back for the newest group: 1 out tile, 2 slot
-            uint32_t owed_idx = 0;
-            uint64_t q_chunk[kNotifyQueue] = {}, q_group[kNotifyQueue] = {};
-            uint32_t q_head = 0, q_tail = 0;
-            uint64_t group = 0;
-            auto settle = [&]() {
-                if (owed_kind == 1) atom::mbar_arrive(&ofree[owed_idx]);
-                else if (owed_kind == 2) atom::mbar_arrive_count(&empty[owed_idx], (uint32_t)ncw);
-                owed_kind = 0;
-            };
-            auto retire = [&](uint64_t upto) {
-                while (q_head != q_tail && q_group[q_head % kNotifyQueue] <= upto) {
-                    notify_chunk(p, q_chunk[q_head % kNotifyQueue]);
-                    ++q_head;
-                }
-            };
-            for (uint64_t c = blockIdx.x; c < p.nchunks; c += gridDim.x, ++k) {
-                const ChunkGeo g = chunk_geo(segs, p.nseg, c);
-                const Seg &sg = *g.sg;
-                const unsigned char *from;
-                const char *self = nullptr;
-                int kind;
-                uint32_t idx;
-                if (sg.src_rank < 0) {
-                    idx = kr & 1u;
-                    if (!ring_wait(&ofull[idx], (kr >> 1) & 1u, &ctl, p.err, kSiteOutFull, true))
-                        break;
-                    from = outt + (size_t)idx * p.out_tile;
-                    kind = 1;
-                    ++kr;
-                } else {
-                    if (sg.sync == kSyncWait && q_head != q_tail) {
-                        // Publish everything before possibly waiting on others.
-                        atom::bulk_wait_all<0>();
-                        settle();
-                        atom::fence_async_global();
-                        retire(group);
-                    }
-                    idx = k % S;
-                    if (!ring_wait(&full[idx], (k / S) & 1u, &ctl, p.err, kSiteRingFull, true))
-                        break;
-                    from = ring + (size_t)idx * p.slot_stride;
-                    kind = 2;
-                    self = static_cast<const char *>(sg.src_is_dst ? p.dst[sg.src_rank]
-                                                                   : p.src[sg.src_rank]) +
-                           sg.src_off + g.off;
-                }
-                const uint64_t doff = sg.dst_off + g.off;
-                if (sg.dst_rank >= 0) {
-                    char *d = static_cast<char *>(p.dst[sg.dst_rank]) + doff;
-                    if (d != self) atom::bulk_store(d, from, g.bytes, pol);
-                } else {
-                    for (int d = 0; d < R; ++d) {
-                        if (d == sg.skip_rank) continue;
-                        char *dp = static_cast<char *>(p.dst[d]) + doff;
-                        if (dp != self) atom::bulk_store(dp, from, g.bytes, pol);
+        // ------------------------- Consume (copy): write-back; Notify --
+        // Lane d issues the bulk store to destination d; each lane tracks its
+        // own bulk groups, and lane 0 hands a stage back once every lane's
+        // stores have read it.
+        const uint64_t pol = atom::policy_evict_first();
+        uint32_t k = 0;
+        int owed = -1;             // slot whose release waits on the newest bulk group
+        uint64_t cd_phase = 0;     // per-slot phase bit of cdone (lane 0)
+        for (uint64_t c = blockIdx.x; c < p.nchunks; c += gridDim.x, ++k) {
+            const ChunkGeo g = chunk_geo(segs, p.nseg, c);
+            const Seg &sg = *g.sg;
+            const uint32_t slot = k % S;
+            if (sg.src_rank < 0 || sg.shift) {
+                // A chunk the consumer warps store.  Settle the owed release
+                // first (never hold a stage while waiting on another), pass
+                // the chunk's full phase, then release it -- after publishing
+                // it if others wait on it.
+                atom::bulk_wait_read<0>();
+                __syncwarp();
+                bool ok = true;
+                if (lane == 0) {
+                    if (owed >= 0) atom::mbar_arrive(&empty[owed]);
+                    ok = ring_wait(&full[slot], (k / S) & 1u, &ctl, p.err, kSiteRingFull, true);
+                    if (ok && sg.sync == kSyncNotify) {
+                        ok = ring_wait(&cdone[slot], (uint32_t)(cd_phase >> slot) & 1u, &ctl,
+                                       p.err, kSiteChunkDone, true);
+                        if (ok) {
+                            cd_phase ^= 1ull << slot;
+                            notify_chunk(p, c);
+                            atom::mbar_arrive_count(&empty[slot], (uint32_t)ncw + 1u);
+                        }
+                    } else if (ok) {
+                        atom::mbar_arrive(&empty[slot]);
                     }
                 }
-                atom::bulk_commit();
-                ++group;
-                if (sg.sync == kSyncNotify) {
-                    q_chunk[q_tail % kNotifyQueue] = c;
-                    q_group[q_tail % kNotifyQueue] = group;
-                    ++q_tail;
-                }
-                // The previous group has finished reading its staging: hand it back.
-                atom::bulk_wait_read<1>();
-                settle();
-                owed_kind = kind;
-                owed_idx = idx;
-                if (q_head != q_tail && q_group[q_head % kNotifyQueue] + kNotifyLag <= group) {
-                    atom::bulk_wait_all<kNotifyLag>();
-                    atom::fence_async_global();
-                    retire(group - kNotifyLag);
+                owed = -1;
+                if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                continue;
+            }
+            const bool ok = ring_wait(&full[slot], (k / S) & 1u, &ctl, p.err, kSiteRingFull, true);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            const unsigned char *from = ring + (size_t)slot * p.slot_stride;
+            const char *self = static_cast<const char *>(sg.src_is_dst ? p.dst[sg.src_rank]
+                                                                       : p.src[sg.src_rank]) +
+                               sg.src_off + g.off;
+            const uint64_t doff = sg.dst_off + g.off;
+            if (sg.dst_rank >= 0) {
+                char *d = static_cast<char *>(p.dst[sg.dst_rank]) + doff;
+                if (lane == 0 && d != self) atom::bulk_store(d, from, g.bytes, pol);
+            } else {
+                for (int d = lane; d < R; d += 32) {
+                    char *dp = static_cast<char *>(p.dst[d]) + doff;
+                    if (d != sg.skip_rank && dp != self) atom::bulk_store(dp, from, g.bytes, pol);
                 }
             }
-            atom::bulk_wait_all<0>();
-            settle();
-            atom::fence_async_global();
-            retire(group);
+            atom::bulk_commit();
+            // The previous group has finished reading its stage: hand it back.
+            atom::bulk_wait_read<1>();
+            __syncwarp();
+            if (lane == 0 && owed >= 0) atom::mbar_arrive(&empty[owed]);
+            owed = (int)slot;
         }
+        atom::bulk_wait_all<0>();
+        __syncwarp();
+        if (lane == 0 && owed >= 0) atom::mbar_arrive(&empty[owed]);
     } else {
         // --------------------------------------------- Consume (reduce) --
         const int ctid = (int)threadIdx.x - 64;
         const int nct = (int)blockDim.x - 64;
-        const uint64_t ustride = (uint64_t)gridDim.x * nct;
-        for (uint64_t u = (uint64_t)blockIdx.x * nct + ctid; u < p.nunits; u += ustride) {
-            const Seg &sg = segs[seg_of_unit(segs, p.nseg, u)];
-            do_unit<DT, MAXR>(p, sg, u - sg.unit_begin);
-        }
-        uint32_t k = 0, kr = 0;
+        units_loop<DT, MAXR>(p, segs, (uint64_t)blockIdx.x * nct + ctid, (uint64_t)gridDim.x * nct);
+        uint32_t k = 0;
         for (uint64_t c = blockIdx.x; c < p.nchunks; c += gridDim.x, ++k) {
             const ChunkGeo g = chunk_geo(segs, p.nseg, c);
             const Seg &sg = *g.sg;
-            if (sg.src_rank >= 0) continue;
+            const bool reduce = sg.src_rank < 0;
             const uint32_t slot = k % S;
-            const uint32_t b = kr & 1u;
             // Every lane waits (bounded) and the warp leaves together.
-            bool ok = ring_wait(&full[slot], (k / S) & 1u, &ctl, p.err, kSiteRingFull, true);
-            if (ok && kr >= 2)
-                ok = ring_wait(&ofree[b], ((kr >> 1) & 1u) ^ 1u, &ctl, p.err, kSiteOutFree, true);
+            const bool ok = ring_wait(&full[slot], (k / S) & 1u, &ctl, p.err, kSiteRingFull, true);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            if (!reduce && !sg.shift) {   // an aligned copy: the writer lane stores it
+                __syncwarp();
+                if (lane == 0) atom::mbar_arrive(&empty[slot]);
+                continue;
+            }
             const unsigned char *sp = ring + (size_t)slot * p.slot_stride;
-            unsigned char *op = outt + (size_t)b * p.out_tile;
-            const uint32_t cb = sg.chunk_bytes;
+            const uint32_t sh = sg.shift;
+            const uint32_t tile = sg.chunk_bytes + (sh ? 16u : 0u);
             const int nvec = (int)(g.bytes >> 4);
+            const uint64_t doff = sg.dst_off + g.off;
+            // 16 destination bytes of source tile s at vector v
+            auto tile_v4 = [&](int s, int v) -> uint4 {
+                const unsigned char *t = sp + (size_t)s * tile + 16 * (size_t)v;
+                if (!sh) return atom::lds_v4(t);
+                return atom::shift_pair(atom::lds_v4(t), atom::lds_v4(t + 16), sh);
+            };
             for (int v = ctid; v < nvec; v += nct) {
-                float acc[V::VE];
-                const unsigned char *t = sp + 16 * (size_t)v;
-                V::init(acc, atom::lds_v4(t));
-                if (MAXR <= 8) {
+                uint4 out;
+                if (reduce) {
+                    float acc[V::VE];
+                    V::init(acc, tile_v4(0, v));
+                    if (MAXR <= 8) {
 #pragma unroll
-                    for (int s = 1; s < MAXR; ++s)
-                        if (s < R) V::add(acc, atom::lds_v4(t + (size_t)s * cb));
-                } else {
+                        for (int s = 1; s < MAXR; ++s)
+                            if (s < R) V::add(acc, tile_v4(s, v));
+                    } else {
 #pragma unroll 8
-                    for (int s = 1; s < R; ++s) V::add(acc, atom::lds_v4(t + (size_t)s * cb));
+                        for (int s = 1; s < R; ++s) V::add(acc, tile_v4(s, v));
+                    }
+                    out = V::pack(acc);
+                } else {
+                    out = tile_v4(0, v);
                 }
-                atom::sts_v4(op + 16 * (size_t)v, V::pack(acc));
+                const uint64_t o = doff + 16 * (uint64_t)v;
+                if (sg.dst_rank >= 0) {
+                    atom::st_v4(static_cast<char *>(p.dst[sg.dst_rank]) + o, out);
+                } else {
+                    for (int d = 0; d < R; ++d)
+                        if (d != sg.skip_rank) atom::st_v4(static_cast<char *>(p.dst[d]) + o, out);
+                }
             }
-            atom::fence_async_shared();
-            __syncwarp();
-            if (lane == 0) {
-                atom::mbar_arrive(&empty[slot]);
-                atom::mbar_arrive(&ofull[b]);
+            if (sg.sync == kSyncNotify) {
+                // Others will read this chunk: make the stores visible at GPU
+                // scope before the writer lane publishes it.
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atom::mbar_arrive(&cdone[slot]);
+            } else {
+                __syncwarp();
+                if (lane == 0) atom::mbar_arrive(&empty[slot]);
             }
-            ++kr;
         }
     }
 }
@@ -517,7 +579,6 @@ void fill_params(KParams<MAXR, MAXSEG> &p, const LaunchArgs &a) {
     p.flag_slots = a.flag_slots;
     p.stages = a.stages;
     p.slot_stride = a.slot_stride;
-    p.out_tile = pl.has_reduce ? pl.red_chunk : 0;
     p.nseg = (int32_t)nseg;
     p.R = a.R;
 }
@@ -554,10 +615,14 @@ cudaError_t launch_tput_t(const LaunchArgs &a) {
     return cudaLaunchKernelEx(&cfg, purlin_throughput_kernel<DT, MAXR, MAXSEG>, p);
 }
 
-template <template <int, int, int> class F>
-struct Dispatch;
+__global__ void purlin_empty_kernel() {}
 
 }  // namespace
+
+cudaError_t launch_empty(cudaStream_t stream) {
+    purlin_empty_kernel<<<1, 32, 0, stream>>>();
+    return cudaGetLastError();
+}
 
 int param_class(int R, size_t nseg) {
     if (R <= kSmallMaxR && nseg <= (size_t)kSmallMaxSeg) return 0;
@@ -565,8 +630,8 @@ int param_class(int R, size_t nseg) {
     return -1;
 }
 
-uint32_t throughput_smem(uint32_t stages, uint32_t slot_stride, uint32_t out_tile) {
-    return stages * slot_stride + 2 * out_tile + (2 * stages + 4) * 8;
+uint32_t throughput_smem(uint32_t stages, uint32_t slot_stride) {
+    return stages * slot_stride + 3 * stages * 8 + kBigMaxSeg * (uint32_t)sizeof(Seg);
 }
 
 cudaError_t launch_latency(const LaunchArgs &a) {

@@ -18,8 +18,7 @@ enum ErrSite : uint64_t {
     kSiteFlagWait = 1,
     kSiteRingFull = 2,
     kSiteRingEmpty = 3,
-    kSiteOutFull = 4,
-    kSiteOutFree = 5,
+    kSiteChunkDone = 4,
 };
 
 struct LaunchArgs {
@@ -49,6 +48,7 @@ struct LaunchArgs {
 int param_class(int R, size_t nseg);
 
 cudaError_t launch_latency(const LaunchArgs &a);
+cudaError_t launch_empty(cudaStream_t stream);
 cudaError_t launch_throughput(const LaunchArgs &a);
 
 // Largest dynamic shared memory the throughput kernels may use; set once.
@@ -57,7 +57,8 @@ cudaError_t configure_kernels(int max_dyn_smem);
 cudaError_t throughput_occupancy(int dtype, int pclass, int block, size_t smem, int *per_sm);
 
 // Shared-memory bytes a throughput launch needs for `stages` ring slots of
-// `slot_stride` bytes plus two output tiles of `out_tile` bytes.
-uint32_t throughput_smem(uint32_t stages, uint32_t slot_stride, uint32_t out_tile);
+// `slot_stride` bytes, their three mbarriers each, and the staged segment
+// table.
+uint32_t throughput_smem(uint32_t stages, uint32_t slot_stride);
 
 }  // namespace purlin

@@ -132,11 +132,10 @@ extern "C" purlin_status purlin_all_reduce_noalloc(int R, const void *const src[
         return PURLIN_ERR_CUDA;
 
     const uint32_t slot_stride = (pl.slot_bytes + 127u) & ~127u;
-    const uint32_t out_tile = pl.has_reduce ? pl.red_chunk : 0;
     const uint32_t limit = (uint32_t)ds.max_smem - 1024;
     uint32_t stages = kStages;
-    while (stages > 2 && throughput_smem(stages, slot_stride, out_tile) > limit) --stages;
-    const uint32_t smem = throughput_smem(stages, slot_stride, out_tile);
+    while (stages > 2 && throughput_smem(stages, slot_stride) > limit) --stages;
+    const uint32_t smem = throughput_smem(stages, slot_stride);
     if (smem > limit) return PURLIN_ERR_UNSUPPORTED;
     const int block = 32 * (2 + kConsumerWarps);
     int per_sm = 0;

@@ -328,7 +328,10 @@ purlin_status compile_plan(const CallDesc &c, int variant, int ar_mode, uint32_t
         s.chunk_begin = (uint32_t)chunk;
         s.unit_begin = unit;
         uint64_t body = 0;
-        if (variant == kVariantThroughput && ((r.src_off - r.dst_off) & 15u) == 0) {
+        if (variant == kVariantThroughput) {
+            // The body is cut on the destination side (16-byte aligned stores);
+            // a source at another 16-byte phase is staged as its aligned hull,
+            // 16 bytes longer, and shifted into place by the consumer warps.
             uint64_t head = std::min<uint64_t>((16u - (r.dst_off & 15u)) & 15u, r.bytes);
             uint64_t rest = r.bytes - head;
             uint64_t tail = rest & 15u;
@@ -337,8 +340,11 @@ purlin_status compile_plan(const CallDesc &c, int variant, int ar_mode, uint32_t
                 s.tma = 1;
                 s.head = (uint8_t)head;
                 s.tail = (uint8_t)tail;
+                s.shift = (uint8_t)((r.src_off - r.dst_off) & 15u);
             }
         }
+        p.total_bytes += r.bytes;
+        p.loose_bytes += r.bytes - body;
         if (s.tma) {
             uint64_t nch = (body + s.chunk_bytes - 1) / s.chunk_bytes;
             chunk += nch;
@@ -362,11 +368,13 @@ purlin_status compile_plan(const CallDesc &c, int variant, int ar_mode, uint32_t
     if (chunk > 0xFFFFFFF0ull) return PURLIN_ERR_INVALID_ARG;
     p.nchunks = chunk;
     p.nunits = unit;
+    // A stage holds one tile per source; a shifted tile is 16 bytes longer.
     uint32_t slot = 0;
-    if (p.has_reduce) slot = std::max<uint32_t>(slot, red_chunk * (uint32_t)R);
-    if (p.has_copy_chunks) {
-        for (const Seg &s : p.segs)
-            if (s.tma && s.src_rank != kRankAll) slot = std::max<uint32_t>(slot, s.chunk_bytes);
+    for (const Seg &s : p.segs) {
+        if (!s.tma) continue;
+        const uint32_t tile = s.chunk_bytes + (s.shift ? 16u : 0u);
+        const uint32_t nsrc = s.src_rank == kRankAll ? (uint32_t)R : 1u;
+        slot = std::max<uint32_t>(slot, tile * nsrc);
     }
     p.slot_bytes = slot;
     return PURLIN_OK;

@@ -55,6 +55,8 @@ struct Seg {
     uint8_t src_is_dst;    // the source buffers are the destination buffers
     uint8_t sync;          // SyncKind
     uint8_t tma;           // the body goes through the TMA ring
+    uint8_t shift;         // tma: 16-byte phase of the source relative to the destination
+    uint8_t pad[3];
 };
 static_assert(sizeof(Seg) == 56, "Seg layout is part of the kernel parameter block");
 
@@ -63,6 +65,8 @@ struct Plan {
     uint64_t nchunks = 0;        // TMA chunks over all segments
     uint64_t nunits = 0;         // vector units over all segments
     uint64_t notify_chunks = 0;  // chunks that publish a flag (composed AllReduce)
+    uint64_t total_bytes = 0;    // bytes per source over all segments
+    uint64_t loose_bytes = 0;    // of those, bytes outside the TMA ring
     uint32_t slot_bytes = 0;     // largest shared-memory stage one chunk needs
     uint32_t red_chunk = 0;      // bytes per source per reduce chunk
     uint32_t copy_chunk = 0;     // bytes per copy chunk

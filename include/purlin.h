@@ -190,6 +190,13 @@ purlin_status purlin_all_reduce_noalloc(int R, const void *const src[], void *co
                                         size_t n, purlin_dtype dtype, purlin_op op,
                                         purlin_layout layout, purlin_stream stream);
 
+/* ------------------------------------------------------------ measurement */
+
+/* Enqueue one empty kernel (<<<1, 32>>>, no parameters) on `stream`: the
+ * launch floor that small-message latency is compared against, timed the
+ * same way as a collective.  Returns CUDA if the launch fails. */
+purlin_status purlin_empty_launch(purlin_stream stream);
+
 /* ----------------------------------------------------------------- status */
 
 /* Wait for the context's stream, then read and clear the device error word.
@@ -205,7 +212,10 @@ const char *purlin_status_string(purlin_status status);
 
 /* Codesign policy knobs (paper summary §4.2: crossover, chunk sizes, CTA
  * allocation, pipeline depth, tuned per collective and GPU; applications
- * may override).  0 means "the built-in policy" for every knob. */
+ * may override).  0 means "the built-in policy" for every knob.
+ * purlin_init also reads PURLIN_VARIANT, PURLIN_CROSSOVER_BYTES,
+ * PURLIN_STAGES, PURLIN_CHUNK_BYTES, PURLIN_CTAS and PURLIN_AR_MODE from the
+ * environment as initial values of the matching knobs. */
 typedef enum {
     PURLIN_OPT_VARIANT = 0,          /* 0 auto, 1 latency (vector ld/st), 2 throughput (TMA ring) */
     PURLIN_OPT_CROSSOVER_BYTES = 1,  /* per-rank message bytes at or below which auto picks latency */
@@ -215,7 +225,8 @@ typedef enum {
     PURLIN_OPT_CTAS = 5,             /* CTAs of a throughput launch */
     PURLIN_OPT_SPIN_TIMEOUT_NS = 6,  /* bound on a cross-CTA flag wait (default 100 ms) */
     PURLIN_OPT_DROP_NOTIFY = 7,      /* host-side fault injection: chunk whose notify is skipped; -1 off */
-    PURLIN_OPT_LAT_CTAS = 8          /* max CTAs of a latency launch */
+    PURLIN_OPT_LAT_CTAS = 8,         /* max CTAs of a latency launch */
+    PURLIN_OPT_LAT_BLOCK = 9         /* threads per CTA of a latency launch (32..256, multiple of 32) */
 } purlin_option;
 
 /* Set one knob; INVALID_ARG for an unknown knob or a value out of range. */
@@ -262,6 +273,7 @@ typedef struct {
     int32_t src_is_dst;    /* 1: the source buffers are the destination array */
     int32_t sync;          /* 0 none, 1 notify a flag after writing, 2 wait on a flag before reading */
     int32_t tma;           /* 1 if the 16-byte-aligned body goes through the TMA ring */
+    int32_t shift;         /* tma: 16-byte phase of the source relative to the destination */
     uint64_t head_bytes;   /* bytes before the aligned body (vector path) */
     uint64_t tail_bytes;   /* bytes after it (vector path) */
     uint64_t chunk_begin;  /* index of the segment's first TMA chunk */

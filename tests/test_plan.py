@@ -173,16 +173,17 @@ def test_cut_invariants(coll, R, dtype):
                     body = sg["bytes"] - sg["head_bytes"] - sg["tail_bytes"]
                     assert body > 0 and body % 16 == 0
                     assert sg["head_bytes"] < 16 and sg["tail_bytes"] < 16
-                    assert (sg["src_off"] + sg["head_bytes"]) % 16 == 0
                     assert (sg["dst_off"] + sg["head_bytes"]) % 16 == 0
+                    assert (sg["src_off"] + sg["head_bytes"]) % 16 == sg["shift"]
+                    assert (sg["src_off"] - sg["dst_off"]) % 16 == sg["shift"]
                     assert sg["chunk_bytes"] % 16 == 0
                     chunk_total += -(-body // sg["chunk_bytes"])
                     unit_total += (sg["head_bytes"] > 0) + (sg["tail_bytes"] > 0)
                 else:
                     a, b = sg["dst_off"], sg["dst_off"] + sg["bytes"]
                     unit_total += -(-b // 16) - a // 16
-                    if variant == 2:   # only misaligned or tiny transfers skip the ring
-                        assert (sg["src_off"] - sg["dst_off"]) % 16 != 0 or sg["bytes"] < 32
+                    if variant == 2:   # only transfers without a whole aligned window skip the ring
+                        assert sg["bytes"] < 32
             assert chunk_total == nch and unit_total == nun
             # every access stays inside its buffer
             ib, ob = sizes_of(coll, R, n, counts, es)
@@ -198,6 +199,15 @@ def test_cut_invariants(coll, R, dtype):
                 if sg["tma"]:
                     assert max(sg["chunk_bytes"] * (R if sg["src_rank"] < 0 else 1),
                                sg["chunk_bytes"]) <= 1 << 20
+                    # the staged source hull starts on the 16-byte boundary at or
+                    # before the first body byte and ends on the one at or after
+                    # the last: never past the granule holding the buffer's end
+                    h0 = sg["src_off"] + sg["head_bytes"] - sg["shift"]
+                    body = sg["bytes"] - sg["head_bytes"] - sg["tail_bytes"]
+                    h1 = h0 + body + (16 if sg["shift"] else 0)
+                    assert h0 >= 0 and h0 % 16 == 0
+                    for s_ in srcs:
+                        assert h1 <= -(-src_len[s_] // 16) * 16
             notify = [s for s in segs if s["sync"] == 1]
             wait = [s for s in segs if s["sync"] == 2]
             assert len(notify) == len(wait)
