@@ -33,7 +33,8 @@ PURLIN_ERR_TIMEOUT = 7
 
 (PURLIN_OPT_VARIANT, PURLIN_OPT_CROSSOVER_BYTES, PURLIN_OPT_AR_MODE, PURLIN_OPT_CHUNK_BYTES,
  PURLIN_OPT_STAGES, PURLIN_OPT_CTAS, PURLIN_OPT_SPIN_TIMEOUT_NS, PURLIN_OPT_DROP_NOTIFY,
- PURLIN_OPT_LAT_CTAS, PURLIN_OPT_LAT_BLOCK) = range(10)
+ PURLIN_OPT_LAT_CTAS, PURLIN_OPT_LAT_BLOCK, PURLIN_OPT_CONSUMER_WARPS,
+ PURLIN_OPT_COPY_STORES) = range(12)
 
 (PURLIN_COLL_ALL_REDUCE, PURLIN_COLL_REDUCE_SCATTER, PURLIN_COLL_ALL_GATHER,
  PURLIN_COLL_ALL_TO_ALL, PURLIN_COLL_ALL_GATHER_V, PURLIN_COLL_REDUCE_SCATTER_V,

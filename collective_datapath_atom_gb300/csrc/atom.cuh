@@ -193,6 +193,23 @@ __device__ __forceinline__ uint4 lds_v4(const void *p) {
     return v;
 }
 
+__device__ __forceinline__ uint32_t lds_u32(const void *p) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)));
+    return v;
+}
+
+// 16 bytes of shared memory starting at p + sh (p 16-byte aligned, sh < 16
+// and even): five aligned 32-bit words, funnel-shifted into place.
+__device__ __forceinline__ uint4 lds_v4_shifted(const unsigned char *p, uint32_t sh) {
+    const unsigned char *q = p + (sh & ~3u);
+    const uint32_t r = (sh & 3u) * 8u;
+    const uint32_t w0 = lds_u32(q), w1 = lds_u32(q + 4), w2 = lds_u32(q + 8),
+                   w3 = lds_u32(q + 12), w4 = lds_u32(q + 16);
+    return make_uint4(__funnelshift_r(w0, w1, r), __funnelshift_r(w1, w2, r),
+                      __funnelshift_r(w2, w3, r), __funnelshift_r(w3, w4, r));
+}
+
 __device__ __forceinline__ void sts_v4(void *p, uint4 v) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(p)), "r"(v.x),
                  "r"(v.y), "r"(v.z), "r"(v.w)

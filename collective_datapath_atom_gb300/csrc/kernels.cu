@@ -65,6 +65,7 @@ struct KParams {
     uint32_t slot_stride;
     int32_t nseg;
     int32_t R;
+    int32_t vector_copies;   // aligned copy chunks are stored by the consumer warps too
 };
 
 template <class P>
@@ -437,7 +438,7 @@ __global__ void __launch_bounds__(kTputMaxThreads, 1) purlin_throughput_kernel(
             const ChunkGeo g = chunk_geo(segs, p.nseg, c);
             const Seg &sg = *g.sg;
             const uint32_t slot = k % S;
-            if (sg.src_rank < 0 || sg.shift) {
+            if (sg.src_rank < 0 || sg.shift || p.vector_copies) {
                 // A chunk the consumer warps store.  Settle the owed release
                 // first (never hold a stage while waiting on another), pass
                 // the chunk's full phase, then release it -- after publishing
@@ -504,7 +505,7 @@ __global__ void __launch_bounds__(kTputMaxThreads, 1) purlin_throughput_kernel(
             // Every lane waits (bounded) and the warp leaves together.
             const bool ok = ring_wait(&full[slot], (k / S) & 1u, &ctl, p.err, kSiteRingFull, true);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
-            if (!reduce && !sg.shift) {   // an aligned copy: the writer lane stores it
+            if (!reduce && !sg.shift && !p.vector_copies) {   // the writer lane stores it
                 __syncwarp();
                 if (lane == 0) atom::mbar_arrive(&empty[slot]);
                 continue;
@@ -514,11 +515,17 @@ __global__ void __launch_bounds__(kTputMaxThreads, 1) purlin_throughput_kernel(
             const uint32_t tile = sg.chunk_bytes + (sh ? 16u : 0u);
             const int nvec = (int)(g.bytes >> 4);
             const uint64_t doff = sg.dst_off + g.off;
+            // in-place AllGather: the destination block that is the source itself
+            const char *self =
+                reduce ? nullptr
+                       : static_cast<const char *>(sg.src_is_dst ? p.dst[sg.src_rank]
+                                                                 : p.src[sg.src_rank]) +
+                             sg.src_off + g.off;
             // 16 destination bytes of source tile s at vector v
             auto tile_v4 = [&](int s, int v) -> uint4 {
                 const unsigned char *t = sp + (size_t)s * tile + 16 * (size_t)v;
                 if (!sh) return atom::lds_v4(t);
-                return atom::shift_pair(atom::lds_v4(t), atom::lds_v4(t + 16), sh);
+                return atom::lds_v4_shifted(t, sh);
             };
             for (int v = ctid; v < nvec; v += nct) {
                 uint4 out;
@@ -539,10 +546,12 @@ __global__ void __launch_bounds__(kTputMaxThreads, 1) purlin_throughput_kernel(
                 }
                 const uint64_t o = doff + 16 * (uint64_t)v;
                 if (sg.dst_rank >= 0) {
-                    atom::st_v4(static_cast<char *>(p.dst[sg.dst_rank]) + o, out);
+                    if (static_cast<const char *>(p.dst[sg.dst_rank]) + doff != self)
+                        atom::st_v4(static_cast<char *>(p.dst[sg.dst_rank]) + o, out);
                 } else {
                     for (int d = 0; d < R; ++d)
-                        if (d != sg.skip_rank) atom::st_v4(static_cast<char *>(p.dst[d]) + o, out);
+                        if (d != sg.skip_rank && static_cast<const char *>(p.dst[d]) + doff != self)
+                            atom::st_v4(static_cast<char *>(p.dst[d]) + o, out);
                 }
             }
             if (sg.sync == kSyncNotify) {
@@ -581,6 +590,7 @@ void fill_params(KParams<MAXR, MAXSEG> &p, const LaunchArgs &a) {
     p.slot_stride = a.slot_stride;
     p.nseg = (int32_t)nseg;
     p.R = a.R;
+    p.vector_copies = a.vector_copies ? 1 : 0;
 }
 
 template <int DT, int MAXR, int MAXSEG>

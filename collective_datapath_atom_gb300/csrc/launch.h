@@ -40,6 +40,7 @@ struct LaunchArgs {
     uint32_t stages = 0;
     uint32_t slot_stride = 0;
     bool cooperative = false;
+    bool vector_copies = false;   // aligned copy chunks stored by the consumer warps
     cudaStream_t stream = nullptr;
 };
 

@@ -351,6 +351,7 @@ purlin_status compile_plan(const CallDesc &c, int variant, int ar_mode, uint32_t
             unit += (s.head ? 1 : 0) + (s.tail ? 1 : 0);
             if (reduce) p.has_reduce = true;
             else p.has_copy_chunks = true;
+            if (!reduce && s.shift) p.has_shifted_copies = true;
             if (r.sync == kSyncNotify) {
                 notify_begin.push_back(s.chunk_begin);
                 p.notify_chunks += nch;

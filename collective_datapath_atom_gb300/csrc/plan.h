@@ -72,6 +72,7 @@ struct Plan {
     uint32_t copy_chunk = 0;     // bytes per copy chunk
     bool has_reduce = false;
     bool has_copy_chunks = false;
+    bool has_shifted_copies = false;  // copies the consumer warps shift into place
     bool composed = false;
     int variant = kVariantNone;
 };
