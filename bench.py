@@ -308,6 +308,29 @@ def _workload_by_name(name):
     raise SystemExit(f"unknown workload {name}")
 
 
+# ------------------------------------------------------- multi-rank ------
+# Replicas only: every rank runs its own in-HBM collective on its own GPU;
+# ranks meet only at the barriers around the timed region and in the max.
+
+def max_over_ranks(x: float) -> float:
+    """The largest `x` over all ranks (x itself when not distributed)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    dev = (torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl"
+           else torch.device("cpu"))
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step_per_rank: int, steps: int, world: int, slowest_ms: float) -> float:
+    """Units all ranks processed divided by the slowest rank's time, in GB/s."""
+    return world * bytes_per_step_per_rank * steps / (slowest_ms / 1e3) / 1e9
+
+
 # ------------------------------------------------------------ GPU arm ----
 
 def time_steps(torch, stream, run, src, dst, steps, flush_buf, events_out):
@@ -345,6 +368,7 @@ def run_gpu(args, rank, world, local_rank):
         args.workload, device, args.elements)
     run = make_runner(P, ctx, w, call)
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    torch.cuda.synchronize()   # inputs were uploaded on another stream
 
     # warm-up (also checks the first call for device errors)
     with torch.cuda.stream(stream):
@@ -370,13 +394,9 @@ def run_gpu(args, rank, world, local_rank):
     wall = time.perf_counter() - t_wall
     clocks = sampler.stop() if sampler else None
     P.purlin_check(ctx)
-    total_ms = float(np.sum(ms))
-    if dist:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(np.sum(ms)))
     ms_per_step = total_ms / args.steps
-    value = world * algo_bytes * args.steps / (total_ms / 1e3) / 1e9
+    value = whole_job_gbs(algo_bytes, args.steps, world, total_ms)
 
     # roofline of the dominant (only) kernel: one launch per step
     peak, peak_kind = measured_peaks()
@@ -514,6 +534,7 @@ def sweep(args):
         src = [torch.randn(n_in, generator=gen, device=device, dtype=torch.float32).to(tdt)
                for _ in range(8)]
         dst = [torch.empty(n_out, device=device, dtype=tdt) for _ in range(8)]
+        torch.cuda.synchronize()   # drawn on the default stream; the library uses `stream`
         return src, dst
 
     def setopt(variant, mode=0):
@@ -529,6 +550,17 @@ def sweep(args):
         for line in res.stdout.splitlines():
             r = json.loads(line)
             r["row"] = "small"
+            emit(r)
+
+    # ---- the pages' V-collective sweep (paper summary §C.4): Zipf(0.125)
+    # split of a total T per rank, 1 KiB .. 1 GiB, through the C ABI
+    for coll in ("AGV", "RSV", "A2AV"):
+        res = subprocess.run([exe, coll, "1024", str(1 << 30), "10", "10", "2", "42"],
+                             capture_output=True, text=True, check=True)
+        for line in res.stdout.splitlines():
+            r = json.loads(line)
+            r["row"] = "vsweep"
+            r["frac"] = r["eff_gbs"] / peak
             emit(r)
 
     # ---- AllReduce bf16 sweep, batch x 4096, both variants, L2 flushed
@@ -561,6 +593,7 @@ def sweep(args):
     for name in (workloads.AG_BF16_R8_8MI.name, workloads.RS_BF16_R8_128MI.name,
                  workloads.A2AV_BF16_R8_MOE.name, workloads.AR_F32_R8_4096.name):
         w, ins, src, dst, call, algo, _, _ = setup_workload(name, device)
+        torch.cuda.synchronize()
         run = make_runner(P, ctx, w, call)
         for variant in (0, 1, 2):
             setopt(variant)

@@ -33,6 +33,7 @@ constexpr int64_t kDefaultTimeoutNs = 100 * 1000 * 1000; // 100 ms
 constexpr int kLatBlock = 256;
 constexpr int kCopyConsumerWarps = 4;
 constexpr int kReduceConsumerWarps = 8;
+constexpr int kShiftedCopyConsumerWarps = 6;
 
 // Policy per collective (codesign policy, paper summary §4.2), measured on
 // GB300 over 256 B..64 MiB per rank and at the workloads' sizes.
@@ -66,7 +67,8 @@ Policy policy_for(purlin_collective coll, int R) {
         case PURLIN_COLL_REDUCE_SCATTER_V:
             return {clamp16(98304 / (uint64_t)R, 1024, 16384), 2, 8ull << 20, false, 0};
         case PURLIN_COLL_ALL_REDUCE:
-            return {clamp16(32768 / (uint64_t)R, 512, 8192), 3, 8ull << 20, false, 0};
+            // (composed mode: the gather chunks are stored by the consumer warps)
+            return {clamp16(32768 / (uint64_t)R, 512, 8192), 3, 8ull << 20, true, 0};
         case PURLIN_COLL_ALL_GATHER:
             return {16384, 4, 128ull << 10, true, 8};
         case PURLIN_COLL_ALL_GATHER_V:
@@ -251,8 +253,11 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
         ce = launch_latency(a);
     } else {
         const uint32_t slot_stride = (pl.slot_bytes + 127u) & ~127u;
+        const bool shifted_p2p_plan = pl.has_shifted_copies && !shape.vector_copies &&
+                                      (c.coll == PURLIN_COLL_ALL_TO_ALL ||
+                                       c.coll == PURLIN_COLL_ALL_TO_ALL_V);
         uint32_t stages = (uint32_t)(ctx->opt[PURLIN_OPT_STAGES] > 0 ? ctx->opt[PURLIN_OPT_STAGES]
-                                                                     : shape.stages);
+                                     : shifted_p2p_plan ? 4u : shape.stages);
         stages = std::min<uint32_t>(32, std::max<uint32_t>(2, stages));
         const uint32_t limit = (uint32_t)ctx->max_smem - 1024;
         while (stages > 2 && throughput_smem(stages, slot_stride) > limit) --stages;
@@ -261,9 +266,16 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
         const bool vector_copies = ctx->opt[PURLIN_OPT_COPY_STORES] == 0
                                        ? shape.vector_copies
                                        : ctx->opt[PURLIN_OPT_COPY_STORES] == 2;
+        // Point-to-point copies at other 16-byte phases (ragged AllToAllV) go
+        // through the consumer warps: 6 warps and a deeper ring keep two CTAs
+        // per SM (measured +35% over 8 warps).
+        const bool shifted_p2p = pl.has_shifted_copies && !shape.vector_copies &&
+                                 (c.coll == PURLIN_COLL_ALL_TO_ALL ||
+                                  c.coll == PURLIN_COLL_ALL_TO_ALL_V);
         const int cw = ctx->opt[PURLIN_OPT_CONSUMER_WARPS] > 0
                            ? (int)ctx->opt[PURLIN_OPT_CONSUMER_WARPS]
                        : shape.consumer_warps > 0 ? shape.consumer_warps
+                       : shifted_p2p ? kShiftedCopyConsumerWarps
                        : pl.has_reduce || pl.has_shifted_copies ? kReduceConsumerWarps
                                                                 : kCopyConsumerWarps;
         const int block = 32 * (2 + cw);

@@ -322,27 +322,32 @@ __device__ __forceinline__ bool ring_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
-// SNAC consume-side acquire: wait until the producing chunk's flag holds at
-// least this call's value for it.  Bounded; on expiry the error word is set
-// and later waits of the launch are skipped.
+// SNAC consume-side acquire, warp-wide: lane l waits until notifying chunks
+// d0 + l, d0 + l + 32, ... hold at least this call's value for them, so the
+// flags are polled in parallel rather than one dependent round trip after
+// another.  Each wait is bounded; on expiry the error word is set and later
+// waits of the launch are skipped.  __syncwarp then orders every lane's
+// acquire before the bulk load lane 0 issues next.
 template <class P>
-__device__ void acquire_chunk(const P &p, uint64_t dep) {
-    if (error_set(p.err)) return;
-    const unsigned long long *f = p.flags + (dep % p.flag_slots);
-    const unsigned long long want = p.epoch + dep / p.flag_slots;
-    if (atom::flag_acquire(f) < want) {
+__device__ void acquire_range(const P &p, uint64_t d0, uint64_t d1, int lane) {
+    for (uint64_t d = d0 + (uint64_t)lane; d < d1; d += 32) {
+        if (error_set(p.err)) break;
+        const unsigned long long *f = p.flags + (d % p.flag_slots);
+        const unsigned long long want = p.epoch + d / p.flag_slots;
+        if (atom::flag_acquire(f) >= want) continue;
         const uint64_t t0 = atom::globaltimer_ns();
         uint32_t ns = 32;
         while (atom::flag_acquire(f) < want) {
             if ((int64_t)(atom::globaltimer_ns() - t0) > p.timeout_ns) {
-                record_error(p.err, PURLIN_ERR_TIMEOUT, kSiteFlagWait, dep);
-                return;
+                record_error(p.err, PURLIN_ERR_TIMEOUT, kSiteFlagWait, d);
+                break;
             }
             __nanosleep(ns);
             if (ns < 1024) ns <<= 1;
         }
     }
-    atom::fence_async_global();   // the staged reads below are async-proxy reads
+    __syncwarp();
+    atom::fence_async_global();   // the staged reads that follow are async-proxy reads
 }
 
 // SNAC notify: publish a completed chunk (its stores are complete and
@@ -402,7 +407,15 @@ __global__ void __launch_bounds__(kTputMaxThreads, 1) purlin_throughput_kernel(
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             const ChunkGeo g = chunk_geo(segs, p.nseg, c);
             const Seg &sg = *g.sg;
-            if (sg.sync == kSyncWait && lane == 0) acquire_chunk(p, sg.dep_chunk + g.ci);
+            if (sg.sync == kSyncWait) {
+                // the notifying chunks this one covers, polled by the whole warp
+                const uint32_t ratio = sg.dep_ratio ? sg.dep_ratio : 1u;
+                const uint32_t rc = sg.chunk_bytes / ratio;
+                const uint64_t nred = (sg.bytes - sg.head - sg.tail + rc - 1) / rc;
+                const uint64_t d0 = g.ci * ratio;
+                const uint64_t d1 = d0 + ratio < nred ? d0 + ratio : nred;
+                acquire_range(p, sg.dep_chunk + d0, sg.dep_chunk + d1, lane);
+            }
             unsigned char *sp = ring + (size_t)slot * p.slot_stride;
             const int nsrc = sg.src_rank < 0 ? R : 1;
             // A shifted source is staged as its 16-byte aligned hull.
@@ -454,6 +467,7 @@ __global__ void __launch_bounds__(kTputMaxThreads, 1) purlin_throughput_kernel(
                                        p.err, kSiteChunkDone, true);
                         if (ok) {
                             cd_phase ^= 1ull << slot;
+                            __threadfence();   // the consumer warps' stores, at GPU scope
                             notify_chunk(p, c);
                             atom::mbar_arrive_count(&empty[slot], (uint32_t)ncw + 1u);
                         }
@@ -555,9 +569,10 @@ __global__ void __launch_bounds__(kTputMaxThreads, 1) purlin_throughput_kernel(
                 }
             }
             if (sg.sync == kSyncNotify) {
-                // Others will read this chunk: make the stores visible at GPU
-                // scope before the writer lane publishes it.
-                __threadfence();
+                // Others will read this chunk.  The stores are ordered before
+                // the writer lane's publication by this mbarrier (release at
+                // CTA scope), its wait (acquire), its GPU-scope fence and its
+                // release-store: the pattern of a grid-wide barrier.
                 __syncwarp();
                 if (lane == 0) atom::mbar_arrive(&cdone[slot]);
             } else {

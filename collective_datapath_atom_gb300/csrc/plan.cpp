@@ -324,7 +324,10 @@ purlin_status compile_plan(const CallDesc &c, int variant, int ar_mode, uint32_t
         s.src_is_dst = r.src_is_dst ? 1 : 0;
         s.sync = r.sync;
         const bool reduce = r.src_rank == kRankAll;
-        s.chunk_bytes = (reduce || r.sync == kSyncWait) ? red_chunk : copy_chunk;
+        // A gathering chunk of the composed AllReduce spans R reducing
+        // chunks, so it fills a stage (R tiles) and waits on R flags.
+        s.chunk_bytes = reduce ? red_chunk : r.sync == kSyncWait ? red_chunk * (uint32_t)R : copy_chunk;
+        if (r.sync == kSyncWait) s.dep_ratio = (uint8_t)R;
         s.chunk_begin = (uint32_t)chunk;
         s.unit_begin = unit;
         uint64_t body = 0;
@@ -362,7 +365,8 @@ purlin_status compile_plan(const CallDesc &c, int variant, int ar_mode, uint32_t
         p.segs.push_back(s);
     }
     // Each gather segment waits on the reduce segment of the same slice; the
-    // two have equal length and chunk size, so chunk i depends on chunk i.
+    // two have equal length, and gather chunk i covers reduce chunks
+    // [i*R, (i+1)*R) of it.
     size_t k = 0;
     for (Seg &s : p.segs)
         if (s.sync == kSyncWait) s.dep_chunk = k < notify_begin.size() ? notify_begin[k++] : 0;

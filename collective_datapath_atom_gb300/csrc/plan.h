@@ -56,7 +56,8 @@ struct Seg {
     uint8_t sync;          // SyncKind
     uint8_t tma;           // the body goes through the TMA ring
     uint8_t shift;         // tma: 16-byte phase of the source relative to the destination
-    uint8_t pad[3];
+    uint8_t dep_ratio;     // kSyncWait: notifying chunks covered by one chunk of this segment
+    uint8_t pad[2];
 };
 static_assert(sizeof(Seg) == 56, "Seg layout is part of the kernel parameter block");
 

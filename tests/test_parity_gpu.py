@@ -216,6 +216,35 @@ def test_allreduce_composed_mode(P, dtype, R):
         ctx.close()
 
 
+def test_allreduce_composed_flag_generations(P, ctx8):
+    """Composed AllReduce with more reducing chunks than flag slots per
+    parity (256 MiB per rank, 65536 chunks of 4 KiB): chunk c publishes
+    epoch + floor(c / F) into slot c mod F.  Compared with the fused mode
+    bit for bit and with the oracle at sampled points, twice in a row."""
+    n = 128 << 20
+    ins = workloads.ar_sweep_inputs(n // workloads.HIDDEN)
+    src = [torch.from_numpy(x.view(np.int16)).cuda() for x in ins]
+    fused = [torch.empty(n, dtype=torch.int16, device="cuda") for _ in range(8)]
+    P.purlin_set_option(ctx8, P.PURLIN_OPT_VARIANT, 2)
+    P.purlin_set_option(ctx8, P.PURLIN_OPT_AR_MODE, 1)
+    P.purlin_all_reduce(ctx8, src, fused, n, 1)
+    P.purlin_check(ctx8)
+    rng = np.random.default_rng(5)
+    idx = np.unique(np.concatenate([rng.integers(0, n, 1000), [0, n - 1]]))
+    want = np.array([oracle.reduce_at(ins, 1, int(i)) for i in idx], dtype=np.uint16)
+    assert np.array_equal(fused[0][torch.from_numpy(idx).cuda()].cpu().numpy().view(np.uint16), want)
+    P.purlin_set_option(ctx8, P.PURLIN_OPT_AR_MODE, 2)
+    for call in range(2):
+        dst = [torch.zeros(n, dtype=torch.int16, device="cuda") for _ in range(8)]
+        P.purlin_all_reduce(ctx8, src, dst, n, 1)
+        P.purlin_check(ctx8)
+        info = P.purlin_last_launch(ctx8)
+        assert info["variant"] == 3 and info["epoch_next"] - info["epoch"] >= 3   # two generations
+        for d in range(8):
+            assert torch.equal(dst[d], fused[d]), f"call {call} rank {d}"
+        del dst
+
+
 def test_repeated_calls_need_no_reset(P, ctx8):
     """Epoch parity and monotonic flags (paper summary §4.3): many calls in a
     row, no flag reset, each correct; the epoch advances by an odd amount."""
@@ -359,6 +388,29 @@ def test_nan_and_signed_zero_copies_are_bitwise(P, ctx8):
         C = np.full((8, 8), n // 8)
         got, _ = run(P, ctx8, "all_to_all", ins, [n * 4] * 8, 0, n)
         assert_same(got, oracle.all_to_all(ins, 0), "NaN AllToAll")
+
+
+# ----------------------------------------- the pages' V-collective workload --
+
+@pytest.mark.parametrize("total_bytes", [1024, 2048, 8192, 1 << 20, 16 << 20])
+def test_v_collectives_zipf_partition(P, ctx8, total_bytes):
+    """AllGatherV / ReduceScatterV / AllToAllV on the Zipf(s = 0.125) split of
+    a total T over 8 ranks (uniform at 1 and 2 KiB; AllToAllV rotates the
+    split so every rank sends and receives T), paper summary §C.4."""
+    T = total_bytes // 2
+    part = workloads.zipf_partition(T)
+    assert sum(part) == T
+    for variant in (0, 1, 2):
+        P.purlin_set_option(ctx8, P.PURLIN_OPT_VARIANT, variant)
+        ins = gen_inputs(part, 1, seed=T + 1)
+        got, _ = run(P, ctx8, "all_gather_v", ins, [T * 2] * 8, 1, counts=part)
+        assert_same(got, oracle.all_gather_v(ins, part, 1), f"AGV T={T} v={variant}")
+        ins = gen_inputs([T] * 8, 1, seed=T + 2)
+        got, _ = run(P, ctx8, "reduce_scatter_v", ins, [c * 2 for c in part], 1, counts=part)
+        assert_same(got, oracle.reduce_scatter_v(ins, part, 1), f"RSV T={T} v={variant}")
+        C = workloads.rotated_counts(part)
+        got, _ = run(P, ctx8, "all_to_all_v", ins, [T * 2] * 8, 1, counts=C.reshape(-1).tolist())
+        assert_same(got, oracle.all_to_all_v(ins, C, 1), f"A2AV T={T} v={variant}")
 
 
 # ------------------------------------------------------- full-size configs --

@@ -214,7 +214,7 @@ def test_cut_invariants(coll, R, dtype):
             for a, b in zip(notify, wait):
                 assert a["bytes"] == b["bytes"] and a["src_off"] == b["src_off"]
                 assert a["dst_rank"] == b["src_rank"] == b["skip_rank"] and b["src_is_dst"] == 1
-                assert a["chunk_bytes"] == b["chunk_bytes"] and a["tma"] and b["tma"]
+                assert b["chunk_bytes"] == a["chunk_bytes"] * R and a["tma"] and b["tma"]
             if notify:
                 assert coll == "all_reduce" and variant == 2 and ar_mode == 2
                 last_notify = max(s["chunk_begin"] for s in notify)

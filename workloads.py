@@ -114,6 +114,30 @@ def moe_dispatch(seed: int = 3, R: int = 8, tokens: int = MOE_TOKENS, hidden: in
     return C, inputs
 
 
+def zipf_partition(total: int, R: int = 8, s: float = 0.125) -> list[int]:
+    """The V-collective split of the paper summary §C.4: rank r's share of a
+    total of `total` elements has weight (r+1)^-s; floor each share and give
+    the remainder to rank 0, so the split preserves the total.  Totals of at
+    most 2 KiB of bf16 (1024 elements) are split uniformly, as the section
+    states.  (With s = 0.125 the largest share is 1.176x the mean; the page
+    quotes 1.125x, which these weights do not give.)"""
+    if total <= 1024:
+        part = [total // R] * R
+        part[0] += total - sum(part)
+        return part
+    w = (np.arange(R, dtype=np.float64) + 1.0) ** (-s)
+    part = [int(np.floor(total * (x / w.sum()))) for x in w]
+    part[0] += total - sum(part)
+    return part
+
+
+def rotated_counts(part: list[int]) -> np.ndarray:
+    """AllToAllV count matrix that rotates a partition: C[s][d] = part[(d - s) mod R], so every
+    rank sends and receives the whole total (§C.4)."""
+    R = len(part)
+    return np.array([[part[(d - src) % R] for d in range(R)] for src in range(R)], dtype=np.int64)
+
+
 def ar_sweep_inputs(batch: int, R: int = 8, seed: int = 4, max_batch: int | None = None):
     """AllReduce sweep input for one batch size: the first R*n values of the
     workload's single stream, split rank-major (n = batch x 4096)."""
