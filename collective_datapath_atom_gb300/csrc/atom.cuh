@@ -131,6 +131,12 @@ __device__ __forceinline__ void fence_async_global() {
 
 // ---------------------------------------------------------------- flags --
 
+// Acquire-release fence at GPU scope (lighter than a sequentially consistent
+// one): orders everything this thread has observed before the stores after it.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
 __device__ __forceinline__ void flag_release(unsigned long long *f, unsigned long long v) {
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(f), "l"(v) : "memory");
 }

@@ -45,6 +45,7 @@ namespace purlin {
 namespace {
 
 constexpr int kTputMaxThreads = 512;
+constexpr int kNotifyBatch = 8;     // flags published behind one fence
 constexpr uint64_t kRingWaitNs = 2000000000ull;   // 2 s bound on a ring wait
 
 template <int MAXR, int MAXSEG>
@@ -374,20 +375,23 @@ __global__ void __launch_bounds__(kTputMaxThreads, 1) purlin_throughput_kernel(
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)S * p.slot_stride);
     uint64_t *full = bars;           // S: producer arrive + transaction bytes
     uint64_t *empty = bars + S;      // S: ncw + 1 arrivals: every consumer warp and the writer
-    uint64_t *cdone = bars + 2 * S;  // S: ncw arrivals: a chunk to publish has been stored
+    uint64_t *cdone = bars + 2 * S;  // 2S: ncw arrivals: chunk k (entry k mod 2S) to publish
+                                     //     has been stored
     // Every role waits on full[] for EVERY chunk, in order, and arrives once
-    // per chunk on empty[] (or, for a chunk to publish, the consumer warps on
-    // cdone[] and the writer on their behalf): a parity wait is only sound if
-    // the slot's previous phase is known complete, and a slot is refilled
-    // only after every role has passed it.
-    const Seg *segs = stage_segs(p, reinterpret_cast<Seg *>(bars + 3 * S));
+    // per chunk on empty[]: a parity wait is only sound if the slot's
+    // previous phase is known complete, and a slot is refilled only after
+    // every role has passed it.  cdone[] has 2S entries: the writer's arrival
+    // on empty[] for chunk k + S comes after its wait on cdone for chunk k,
+    // so the consumer warps are never 2S chunks ahead of that wait.
+    const uint32_t C = 2 * S;
+    const Seg *segs = stage_segs(p, reinterpret_cast<Seg *>(bars + 4 * S));
 
     if (threadIdx.x == 0) {
         for (uint32_t i = 0; i < S; ++i) {
             atom::mbar_init(&full[i], 1);
             atom::mbar_init(&empty[i], (uint32_t)ncw + 1u);
-            atom::mbar_init(&cdone[i], (uint32_t)ncw);
         }
+        for (uint32_t i = 0; i < C; ++i) atom::mbar_init(&cdone[i], (uint32_t)ncw);
         ctl.abort = 0;
         atom::mbar_init_fence();
     }
@@ -447,36 +451,49 @@ __global__ void __launch_bounds__(kTputMaxThreads, 1) purlin_throughput_kernel(
         uint32_t k = 0;
         int owed = -1;             // slot whose release waits on the newest bulk group
         uint64_t cd_phase = 0;     // per-slot phase bit of cdone (lane 0)
+        // Chunks seen stored (cdone) whose flags are not yet published: one
+        // GPU-scope fence covers a whole batch, off the stage-release path.
+        uint64_t pend[kNotifyBatch];
+        int npend = 0;
+        auto publish = [&]() {
+            if (lane == 0 && npend > 0) {
+                atom::fence_acq_rel_gpu();   // the consumer warps' stores, at GPU scope
+                for (int i = 0; i < npend; ++i) notify_chunk(p, pend[i]);
+            }
+            npend = 0;
+        };
         for (uint64_t c = blockIdx.x; c < p.nchunks; c += gridDim.x, ++k) {
             const ChunkGeo g = chunk_geo(segs, p.nseg, c);
             const Seg &sg = *g.sg;
             const uint32_t slot = k % S;
+            // Never wait on a chunk that depends on flags with flags of our own
+            // still unpublished.
+            if (sg.sync == kSyncWait) publish();
             if (sg.src_rank < 0 || sg.shift || p.vector_copies) {
                 // A chunk the consumer warps store.  Settle the owed release
                 // first (never hold a stage while waiting on another), pass
-                // the chunk's full phase, then release it -- after publishing
-                // it if others wait on it.
+                // the chunk's full phase, then release it -- for a chunk others
+                // wait on, once the consumer warps report it stored.
                 atom::bulk_wait_read<0>();
                 __syncwarp();
                 bool ok = true;
                 if (lane == 0) {
                     if (owed >= 0) atom::mbar_arrive(&empty[owed]);
                     ok = ring_wait(&full[slot], (k / S) & 1u, &ctl, p.err, kSiteRingFull, true);
+                    if (ok) atom::mbar_arrive(&empty[slot]);
                     if (ok && sg.sync == kSyncNotify) {
-                        ok = ring_wait(&cdone[slot], (uint32_t)(cd_phase >> slot) & 1u, &ctl,
-                                       p.err, kSiteChunkDone, true);
+                        const uint32_t e = k % C;
+                        ok = ring_wait(&cdone[e], (uint32_t)(cd_phase >> e) & 1u, &ctl, p.err,
+                                       kSiteChunkDone, true);
                         if (ok) {
-                            cd_phase ^= 1ull << slot;
-                            __threadfence();   // the consumer warps' stores, at GPU scope
-                            notify_chunk(p, c);
-                            atom::mbar_arrive_count(&empty[slot], (uint32_t)ncw + 1u);
+                            cd_phase ^= 1ull << e;
+                            pend[npend] = c;
                         }
-                    } else if (ok) {
-                        atom::mbar_arrive(&empty[slot]);
                     }
                 }
                 owed = -1;
-                if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                if (!__shfl_sync(0xFFFFFFFFu, (int)ok, 0)) break;   // lane 0 decided
+                if (sg.sync == kSyncNotify && ++npend == kNotifyBatch) publish();
                 continue;
             }
             const bool ok = ring_wait(&full[slot], (k / S) & 1u, &ctl, p.err, kSiteRingFull, true);
@@ -505,6 +522,7 @@ __global__ void __launch_bounds__(kTputMaxThreads, 1) purlin_throughput_kernel(
         atom::bulk_wait_all<0>();
         __syncwarp();
         if (lane == 0 && owed >= 0) atom::mbar_arrive(&empty[owed]);
+        publish();
     } else {
         // --------------------------------------------- Consume (reduce) --
         const int ctid = (int)threadIdx.x - 64;
@@ -574,7 +592,10 @@ __global__ void __launch_bounds__(kTputMaxThreads, 1) purlin_throughput_kernel(
                 // CTA scope), its wait (acquire), its GPU-scope fence and its
                 // release-store: the pattern of a grid-wide barrier.
                 __syncwarp();
-                if (lane == 0) atom::mbar_arrive(&cdone[slot]);
+                if (lane == 0) {
+                    atom::mbar_arrive(&cdone[k % C]);
+                    atom::mbar_arrive(&empty[slot]);
+                }
             } else {
                 __syncwarp();
                 if (lane == 0) atom::mbar_arrive(&empty[slot]);
@@ -656,7 +677,7 @@ int param_class(int R, size_t nseg) {
 }
 
 uint32_t throughput_smem(uint32_t stages, uint32_t slot_stride) {
-    return stages * slot_stride + 3 * stages * 8 + kBigMaxSeg * (uint32_t)sizeof(Seg);
+    return stages * slot_stride + 4 * stages * 8 + kBigMaxSeg * (uint32_t)sizeof(Seg);
 }
 
 cudaError_t launch_latency(const LaunchArgs &a) {

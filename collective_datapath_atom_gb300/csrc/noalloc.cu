@@ -17,9 +17,10 @@
 //   g_noalloc_scratch holds 2 x kStaticFlagSlots u64 flags (one set per
 //   epoch parity) and one u64 error word: 128 KiB + 8 bytes, kept by every
 //   GPU that loads the library until the process exits.  The largest call
-//   therefore has at most kStaticFlagSlots reduce chunks of 32 KiB / R bytes
-//   per source: n * element_size <= 8192 * (32768 / R) bytes per rank
-//   (32 MiB per rank at R = 8).  Larger calls return PURLIN_ERR_INVALID_ARG.
+//   therefore has at most kStaticFlagSlots reduce chunks of 96 KiB / R bytes
+//   per source (rounded down to 16): n * element_size <= 8192 * (98304 / R)
+//   bytes per rank (96 MiB per rank at R = 8).  Larger calls return
+//   PURLIN_ERR_INVALID_ARG.
 //   R is limited to 31 so the compiled plan fits the kernel parameters.
 //
 // First call on a device: with that device current it looks up the array's
@@ -50,10 +51,10 @@ using namespace purlin;
 constexpr uint32_t kStaticFlagSlots = 8192;   // per parity
 constexpr int kMaxDevices = 64;
 constexpr int kMaxStaticRanks = 31;           // 2R + 1 segments fit the big parameter block
-constexpr uint32_t kSlotBytes = 32 * 1024;
-constexpr uint32_t kStages = 6;
+constexpr uint32_t kSlotBytes = 96 * 1024;   // R reduce tiles per stage, as in composed mode
+constexpr uint32_t kStages = 2;
 constexpr int64_t kTimeoutNs = 100 * 1000 * 1000;
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 12;
 
 }  // namespace
 

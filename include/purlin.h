@@ -177,8 +177,9 @@ purlin_status purlin_all_to_all_v(purlin_ctx *ctx, const void *const src[], void
  * `stream`.  Its scratch (per-chunk flags and an error word, 128 KiB + 8
  * bytes) is a fixed device array inside the library, held by every GPU that
  * loads it until the process exits.  Limit: at most 8192 reduce chunks of
- * 32 KiB / R bytes per source, i.e. n * element size <= 8192 * (32768 / R)
- * bytes per rank (32 MiB at R = 8); larger calls and R > 31 return
+ * 96 KiB / R bytes per source (rounded down to a multiple of 16), i.e.
+ * n * element size <= 8192 * (98304 / R) bytes per rank (96 MiB at R = 8);
+ * larger calls and R > 31 return
  * INVALID_ARG.  The first call on a device looks up the array's address,
  * sets kernel attributes and zeroes the array with a blocking cudaMemset:
  * make it before any stream capture.  Every call shares the array (it keeps

@@ -234,15 +234,27 @@ def test_allreduce_composed_flag_generations(P, ctx8):
     want = np.array([oracle.reduce_at(ins, 1, int(i)) for i in idx], dtype=np.uint16)
     assert np.array_equal(fused[0][torch.from_numpy(idx).cuda()].cpu().numpy().view(np.uint16), want)
     P.purlin_set_option(ctx8, P.PURLIN_OPT_AR_MODE, 2)
-    for call in range(2):
+    P.purlin_set_option(ctx8, P.PURLIN_OPT_CHUNK_BYTES, 4096)   # 65536 reducing chunks
+    try:
+        for call in range(2):
+            dst = [torch.zeros(n, dtype=torch.int16, device="cuda") for _ in range(8)]
+            P.purlin_all_reduce(ctx8, src, dst, n, 1)
+            P.purlin_check(ctx8)
+            info = P.purlin_last_launch(ctx8)
+            assert info["variant"] == 3 and info["epoch_next"] - info["epoch"] >= 3   # two generations
+            for d in range(8):
+                assert torch.equal(dst[d], fused[d]), f"call {call} rank {d}"
+            del dst
+        # the default composed ring (fewer, larger chunks) gives the same bits
+        P.purlin_set_option(ctx8, P.PURLIN_OPT_CHUNK_BYTES, 0)
         dst = [torch.zeros(n, dtype=torch.int16, device="cuda") for _ in range(8)]
         P.purlin_all_reduce(ctx8, src, dst, n, 1)
         P.purlin_check(ctx8)
-        info = P.purlin_last_launch(ctx8)
-        assert info["variant"] == 3 and info["epoch_next"] - info["epoch"] >= 3   # two generations
+        assert P.purlin_last_launch(ctx8)["variant"] == 3
         for d in range(8):
-            assert torch.equal(dst[d], fused[d]), f"call {call} rank {d}"
-        del dst
+            assert torch.equal(dst[d], fused[d]), f"default ring, rank {d}"
+    finally:
+        P.purlin_set_option(ctx8, P.PURLIN_OPT_CHUNK_BYTES, 0)
 
 
 def test_repeated_calls_need_no_reset(P, ctx8):

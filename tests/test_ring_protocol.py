@@ -74,7 +74,8 @@ def run_model(kinds, S, ncw=2, seed=0, old_order=False, max_steps=200000):
     rng = random.Random(seed)
     full = [Barrier(f"full[{i}]", 1) for i in range(S)]
     empty = [Barrier(f"empty[{i}]", (ncw if old_order else ncw + 1)) for i in range(S)]
-    cdone = [Barrier(f"cdone[{i}]", ncw) for i in range(S)]
+    C = S if old_order else 2 * S          # cdone ring entries
+    cdone = [Barrier(f"cdone[{i}]", ncw) for i in range(C)]
     slot_chunk = [None] * S          # which chunk's data a stage holds
     readers = [set() for _ in range(S)]
     inflight_loads = []              # (slot, chunk)
@@ -115,7 +116,9 @@ def run_model(kinds, S, ncw=2, seed=0, old_order=False, max_steps=200000):
                 raise ProtocolError(f"stage {slot} changed under consumer {w}")
             readers[slot].discard(("c", w))
             if kind == "notify":
-                cdone[slot].arrive()
+                cdone[k % C].arrive()
+                if not old_order:
+                    empty[slot].arrive()
             else:
                 empty[slot].arrive()
             yield
@@ -123,7 +126,7 @@ def run_model(kinds, S, ncw=2, seed=0, old_order=False, max_steps=200000):
     def writer():
         owed = None
         group = 0
-        cd_phase = [0] * S
+        cd_phase = [0] * C
         for k in range(n):
             slot = k % S
             kind = kinds[k]
@@ -143,13 +146,12 @@ def run_model(kinds, S, ncw=2, seed=0, old_order=False, max_steps=200000):
                     owed = None
                 while not full[slot].test_wait(k // S):
                     yield
+                empty[slot].arrive()
                 if kind == "notify":
-                    while not cdone[slot].test_wait(cd_phase[slot]):
+                    e = k % C
+                    while not cdone[e].test_wait(cd_phase[e]):
                         yield
-                    cd_phase[slot] += 1
-                    empty[slot].arrive(ncw + 1)
-                else:
-                    empty[slot].arrive()
+                    cd_phase[e] += 1
                 yield
                 continue
             while not full[slot].test_wait(k // S):

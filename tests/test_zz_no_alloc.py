@@ -97,8 +97,8 @@ def test_noalloc_allocates_no_device_memory(P):
 def test_noalloc_rejects_sizes_past_its_scratch(P):
     stream = torch.cuda.current_stream()
     R = 8
-    # 8192 chunks of 4 KiB per source is the limit at R = 8: 32 MiB per rank
-    limit_elems = 8192 * (32768 // R) // 2            # bf16 elements per rank
+    # 8192 chunks of 12 KiB per source is the limit at R = 8: 96 MiB per rank
+    limit_elems = 8192 * ((98304 // R) & ~15) // 2    # bf16 elements per rank
     src = [torch.empty(limit_elems + 4096, dtype=torch.int16, device="cuda") for _ in range(R)]
     dst = [torch.empty(limit_elems + 4096, dtype=torch.int16, device="cuda") for _ in range(R)]
     st = _call_noalloc(P, R, src, dst, limit_elems + 4096, 1, stream)
