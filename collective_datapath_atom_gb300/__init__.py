@@ -80,6 +80,23 @@ class purlin_segment(ctypes.Structure):
         return {name: getattr(self, name) for name, _ in self._fields_}
 
 
+class purlin_device_coll(ctypes.Structure):
+    """A collective compiled for device-side calls (include/purlin.h)."""
+    _fields_ = [("src", ctypes.c_void_p * PURLIN_MAX_RANKS),
+                ("dst", ctypes.c_void_p * PURLIN_MAX_RANKS),
+                ("segs", ctypes.c_void_p), ("flags", ctypes.c_void_p),
+                ("epochs", ctypes.c_void_p), ("err", ctypes.c_void_p),
+                ("nchunks", ctypes.c_uint64), ("nunits", ctypes.c_uint64),
+                ("epoch_inc", ctypes.c_uint64), ("timeout_ns", ctypes.c_int64),
+                ("drop_notify", ctypes.c_int64), ("flag_slots", ctypes.c_uint32),
+                ("stages", ctypes.c_uint32), ("slot_stride", ctypes.c_uint32),
+                ("workspace_bytes", ctypes.c_uint32), ("nseg", ctypes.c_int32),
+                ("R", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("vector_copies", ctypes.c_int32), ("blocks", ctypes.c_int32),
+                ("threads", ctypes.c_int32), ("composed", ctypes.c_int32),
+                ("coll", ctypes.c_int32), ("owner", ctypes.c_void_p)]
+
+
 class PurlinError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = int(status)
@@ -122,6 +139,12 @@ _SIGNATURES = {
         purlin_layout, ctypes.c_int, ctypes.c_int, ctypes.c_uint64,
         ctypes.POINTER(purlin_segment), ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t),
         ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
+    "purlin_device_prepare": (ctypes.c_int, [
+        _CTX, ctypes.c_int, _VPP, _VPP, ctypes.c_size_t, _SZP, ctypes.c_int, ctypes.c_int,
+        purlin_layout, ctypes.c_int, ctypes.c_uint32, ctypes.POINTER(purlin_device_coll)]),
+    "purlin_device_check": (ctypes.c_int, [ctypes.POINTER(purlin_device_coll), ctypes.c_void_p]),
+    "purlin_device_release": (ctypes.c_int, [_CTX, ctypes.POINTER(purlin_device_coll)]),
+    "purlin_device_coll_size": (ctypes.c_size_t, []),
 }
 
 
@@ -335,3 +358,38 @@ def purlin_plan_inspect(coll: int, R: int, src, dst, n: int, counts, dtype: int,
                                  ctypes.byref(nun))
     out = [segs[i].as_dict() for i in range(min(nseg.value, cap))] if st == PURLIN_OK else []
     return int(st), out, nch.value, nun.value
+
+
+# ------------------------------------------------------ device-side API ---
+
+COLL_NAMES = ["all_reduce", "reduce_scatter", "all_gather", "all_to_all", "all_gather_v",
+              "reduce_scatter_v", "all_to_all_v"]
+
+
+def purlin_device_prepare(ctx, coll: int, src, dst, n: int = 0, counts=None, dtype: int = 0,
+                          op=None, layout=None, blocks: int = 1,
+                          max_workspace_bytes: int = 0) -> purlin_device_coll:
+    """Compile a collective for kernels that call it themselves; returns the
+    descriptor to pass to them (see include/purlin.h)."""
+    dflt_op, dflt_layout = LAYOUTS[COLL_NAMES[int(coll)]]
+    op = dflt_op if op is None else op
+    layout = dflt_layout if layout is None else layout
+    ps, _k1 = _ptr_array(src)
+    pd, _k2 = _ptr_array(dst)
+    pc, _k3 = (None, None) if counts is None else _size_array(counts)
+    d = purlin_device_coll()
+    _ok(lib.purlin_device_prepare(ctx.handle, int(coll), ps, pd, int(n), pc, int(dtype), int(op),
+                                  _layout(layout), int(blocks), int(max_workspace_bytes),
+                                  ctypes.byref(d)), "purlin_device_prepare")
+    return d
+
+
+def purlin_device_check(desc: purlin_device_coll, stream=None) -> int:
+    """Wait for the stream, then read and clear the descriptor's error word
+    (returns the status; does not raise)."""
+    return int(lib.purlin_device_check(ctypes.byref(desc),
+                                       ctypes.c_void_p(_stream_handle(stream))))
+
+
+def purlin_device_release(ctx, desc: purlin_device_coll):
+    _ok(lib.purlin_device_release(ctx.handle, ctypes.byref(desc)), "purlin_device_release")

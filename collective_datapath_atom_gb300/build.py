@@ -2,7 +2,9 @@
 
 Each translation unit is compiled in its own nvcc process, in parallel, then
 linked into one shared library beside this file.  ``-Xptxas -v`` resource
-reports go to ``_build/ptxas_<unit>.txt``.
+reports go to ``_build/ptxas_<unit>.txt``.  The example kernels written
+against the device-side API (``examples/``) are compiled in the same round
+into ``libpurlin_examples.so``.
 """
 from __future__ import annotations
 
@@ -16,7 +18,10 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpurlin.so")
 BENCH = os.path.join(HERE, "purlin_bench")
+EXAMPLES_DIR = os.path.join(HERE, "examples")
+EXAMPLES_LIB = os.path.join(HERE, "libpurlin_examples.so")
 SOURCES = ["plan.cpp", "api.cpp", "kernels.cu", "noalloc.cu"]
+EXAMPLE_SOURCES = ["device_examples.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -28,11 +33,14 @@ def _nvcc() -> str:
 
 
 def _stale() -> bool:
-    if not os.path.exists(LIB) or not os.path.exists(BENCH):
+    outs = (LIB, BENCH, EXAMPLES_LIB)
+    if not all(os.path.exists(o) for o in outs):
         return True
-    t = min(os.path.getmtime(LIB), os.path.getmtime(BENCH))
+    t = min(os.path.getmtime(o) for o in outs)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    deps.append(os.path.join(HERE, "..", "include", "purlin.h"))
+    deps += [os.path.join(EXAMPLES_DIR, f) for f in os.listdir(EXAMPLES_DIR)]
+    inc = os.path.join(HERE, "..", "include")
+    deps += [os.path.join(inc, f) for f in os.listdir(inc)]
     deps.append(__file__)
     return any(os.path.getmtime(d) > t for d in deps if os.path.exists(d))
 
@@ -46,14 +54,17 @@ def build(force: bool = False, verbose: bool = False) -> str:
               "-I", os.path.join(HERE, "..", "include"), *ARCH]
     procs = []
     objs = []
-    for src in SOURCES:
+    ex_objs = []
+    units = [(CSRC, src, objs) for src in SOURCES] + \
+            [(EXAMPLES_DIR, src, ex_objs) for src in EXAMPLE_SOURCES]
+    for where, src, into in units:
         obj = os.path.join(BUILD, src.rsplit(".", 1)[0] + ".o")
-        objs.append(obj)
-        cmd = [nvcc, *common, "-c", os.path.join(CSRC, src), "-o", obj]
+        into.append(obj)
+        cmd = [nvcc, *common, "-c", os.path.join(where, src), "-o", obj]
         if src.endswith(".cu"):
             cmd += ["-Xptxas", "-v"]
         else:
-            cmd = [nvcc, *common, "-x", "cu", "-c", os.path.join(CSRC, src), "-o", obj]
+            cmd = [nvcc, *common, "-x", "cu", "-c", os.path.join(where, src), "-o", obj]
         log = open(os.path.join(BUILD, f"ptxas_{src}.txt"), "w")
         procs.append((src, subprocess.Popen(cmd, stdout=log, stderr=subprocess.STDOUT), log))
     failed = []
@@ -77,6 +88,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
                            os.path.join(CSRC, "purlin_bench.c"), "-o", tmp, "-L", HERE,
                            "-lpurlin", "-Xlinker", "-rpath,$ORIGIN", "-lm"])
     os.replace(tmp, BENCH)
+    tmp = EXAMPLES_LIB + f".tmp{os.getpid()}"
+    subprocess.check_call([nvcc, *ARCH, "-shared", "-o", tmp, *ex_objs])
+    os.replace(tmp, EXAMPLES_LIB)
     if verbose:
         with open(os.path.join(BUILD, "ptxas_kernels.cu.txt")) as f:
             sys.stdout.write(f.read())

@@ -88,6 +88,22 @@ Policy composed_all_reduce_policy(int R) {
     return {chunk, 2, 8ull << 20, true, 12};
 }
 
+// Device memory behind one purlin_device_coll.
+struct DeviceCollMem {
+    Seg *segs = nullptr;
+    unsigned long long *flags = nullptr;
+    unsigned long long *epochs = nullptr;
+    unsigned long long *err = nullptr;
+};
+
+void free_device_coll(DeviceCollMem &m) {
+    if (m.segs) cudaFree(m.segs);
+    if (m.flags) cudaFree(m.flags);
+    if (m.epochs) cudaFree(m.epochs);
+    if (m.err) cudaFree(m.err);
+    m = DeviceCollMem{};
+}
+
 struct CacheEntry {
     std::string key;
     Plan plan;
@@ -115,6 +131,7 @@ struct purlin_ctx {
     purlin_launch_info last = {};
     std::list<CacheEntry> lru;
     std::unordered_map<std::string, std::list<CacheEntry>::iterator> index;
+    std::list<DeviceCollMem> device_colls;   // memory of purlin_device_prepare descriptors
 };
 
 namespace {
@@ -186,6 +203,61 @@ uint64_t message_bytes(const CallDesc &c) {
     return m;
 }
 
+// Ring shape of a throughput launch: stages (reduced until the shared
+// memory fits `limit`), stage stride, consumer warps and copy stores.
+struct RingShape {
+    uint32_t stages = 0;
+    uint32_t slot_stride = 0;
+    uint32_t smem = 0;
+    int consumer_warps = 0;
+    bool vector_copies = false;
+};
+
+purlin_status ring_shape(const purlin_ctx *ctx, const CallDesc &c, const Policy &shape,
+                         const Plan &pl, uint32_t limit, RingShape *out) {
+    RingShape r;
+    r.slot_stride = (pl.slot_bytes + 127u) & ~127u;
+    // Point-to-point copies at other 16-byte phases (ragged AllToAllV) go
+    // through the consumer warps: 6 warps and a deeper ring keep two CTAs
+    // per SM (measured +35% over 8 warps).
+    const bool shifted_p2p = pl.has_shifted_copies && !shape.vector_copies &&
+                             (c.coll == PURLIN_COLL_ALL_TO_ALL ||
+                              c.coll == PURLIN_COLL_ALL_TO_ALL_V);
+    uint32_t stages = (uint32_t)(ctx->opt[PURLIN_OPT_STAGES] > 0 ? ctx->opt[PURLIN_OPT_STAGES]
+                                 : shifted_p2p ? 4u : shape.stages);
+    stages = std::min<uint32_t>(32, std::max<uint32_t>(2, stages));
+    while (stages > 2 && throughput_smem(stages, r.slot_stride) > limit) --stages;
+    r.stages = stages;
+    r.smem = throughput_smem(stages, r.slot_stride);
+    if (r.smem > limit) return PURLIN_ERR_UNSUPPORTED;
+    r.vector_copies = ctx->opt[PURLIN_OPT_COPY_STORES] == 0 ? shape.vector_copies
+                                                            : ctx->opt[PURLIN_OPT_COPY_STORES] == 2;
+    r.consumer_warps = ctx->opt[PURLIN_OPT_CONSUMER_WARPS] > 0
+                           ? (int)ctx->opt[PURLIN_OPT_CONSUMER_WARPS]
+                       : shape.consumer_warps > 0 ? shape.consumer_warps
+                       : shifted_p2p ? kShiftedCopyConsumerWarps
+                       : pl.has_reduce || pl.has_shifted_copies ? kReduceConsumerWarps
+                                                                : kCopyConsumerWarps;
+    *out = r;
+    return PURLIN_OK;
+}
+
+// Per-parity flag slots for a grid of `grid` CTAs (a multiple of the grid,
+// so a slot is always reused by the CTA that owns its chunks) and the odd
+// epoch increment that keeps every generation of a call distinct.
+void flag_geometry(uint64_t notify_chunks, int64_t grid, uint32_t *slots, uint64_t *epoch_inc) {
+    *slots = (kFlagSlots / (uint32_t)grid) * (uint32_t)grid;
+    uint64_t gens = (notify_chunks + *slots - 1) / *slots;
+    if (gens == 0) gens = 1;
+    *epoch_inc = gens | 1ull;   // odd: the parity flips every call
+}
+
+Policy call_policy(const purlin_ctx *ctx, const CallDesc &c) {
+    return c.coll == PURLIN_COLL_ALL_REDUCE && ctx->opt[PURLIN_OPT_AR_MODE] == 2
+               ? composed_all_reduce_policy(c.R)
+               : policy_for(c.coll, c.R);
+}
+
 purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], void *const dst[]) {
     if (ctx == nullptr) return PURLIN_ERR_INVALID_ARG;
     if (c.R != ctx->R) return PURLIN_ERR_INVALID_ARG;
@@ -194,9 +266,7 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
 
     // ---- policy (§4.2)
     const int ar_mode = (int)ctx->opt[PURLIN_OPT_AR_MODE];
-    const Policy shape = c.coll == PURLIN_COLL_ALL_REDUCE && ar_mode == 2
-                             ? composed_all_reduce_policy(c.R)
-                             : policy_for(c.coll, c.R);
+    const Policy shape = call_policy(ctx, c);
     int variant = (int)ctx->opt[PURLIN_OPT_VARIANT];
     if (variant == 0) {
         const uint64_t xo = ctx->opt[PURLIN_OPT_CROSSOVER_BYTES] > 0
@@ -264,33 +334,12 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
         info.variant = kVariantLatency;
         ce = launch_latency(a);
     } else {
-        const uint32_t slot_stride = (pl.slot_bytes + 127u) & ~127u;
-        const bool shifted_p2p_plan = pl.has_shifted_copies && !shape.vector_copies &&
-                                      (c.coll == PURLIN_COLL_ALL_TO_ALL ||
-                                       c.coll == PURLIN_COLL_ALL_TO_ALL_V);
-        uint32_t stages = (uint32_t)(ctx->opt[PURLIN_OPT_STAGES] > 0 ? ctx->opt[PURLIN_OPT_STAGES]
-                                     : shifted_p2p_plan ? 4u : shape.stages);
-        stages = std::min<uint32_t>(32, std::max<uint32_t>(2, stages));
-        const uint32_t limit = (uint32_t)ctx->max_smem - 1024;
-        while (stages > 2 && throughput_smem(stages, slot_stride) > limit) --stages;
-        const uint32_t smem = throughput_smem(stages, slot_stride);
-        if (smem > limit) return PURLIN_ERR_UNSUPPORTED;
-        const bool vector_copies = ctx->opt[PURLIN_OPT_COPY_STORES] == 0
-                                       ? shape.vector_copies
-                                       : ctx->opt[PURLIN_OPT_COPY_STORES] == 2;
-        // Point-to-point copies at other 16-byte phases (ragged AllToAllV) go
-        // through the consumer warps: 6 warps and a deeper ring keep two CTAs
-        // per SM (measured +35% over 8 warps).
-        const bool shifted_p2p = pl.has_shifted_copies && !shape.vector_copies &&
-                                 (c.coll == PURLIN_COLL_ALL_TO_ALL ||
-                                  c.coll == PURLIN_COLL_ALL_TO_ALL_V);
-        const int cw = ctx->opt[PURLIN_OPT_CONSUMER_WARPS] > 0
-                           ? (int)ctx->opt[PURLIN_OPT_CONSUMER_WARPS]
-                       : shape.consumer_warps > 0 ? shape.consumer_warps
-                       : shifted_p2p ? kShiftedCopyConsumerWarps
-                       : pl.has_reduce || pl.has_shifted_copies ? kReduceConsumerWarps
-                                                                : kCopyConsumerWarps;
-        const int block = 32 * (2 + cw);
+        RingShape rs;
+        st = ring_shape(ctx, c, shape, pl, (uint32_t)ctx->max_smem - 1024, &rs);
+        if (st != PURLIN_OK) return st;
+        const uint32_t stages = rs.stages, slot_stride = rs.slot_stride, smem = rs.smem;
+        const bool vector_copies = rs.vector_copies;
+        const int block = 32 * (2 + rs.consumer_warps);
         const int pclass = e->segs_dev ? 1 : param_class(c.R, pl.segs.size());
         int per_sm = 0;
         if (throughput_occupancy(c.dtype, pclass, block, smem, &per_sm) != cudaSuccess ||
@@ -310,10 +359,7 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
         if (pl.composed) {
             // flag slot reuse stays on one CTA (slots a multiple of the grid),
             // so a later generation of a slot implies the earlier one landed.
-            a.flag_slots = (kFlagSlots / (uint32_t)grid) * (uint32_t)grid;
-            uint64_t gens = (pl.notify_chunks + a.flag_slots - 1) / a.flag_slots;
-            if (gens == 0) gens = 1;
-            epoch_inc = gens | 1ull;   // odd: the parity flips every call
+            flag_geometry(pl.notify_chunks, grid, &a.flag_slots, &epoch_inc);
         }
         info.variant = pl.composed ? 3 : kVariantThroughput;
         info.stages = (int32_t)stages;
@@ -394,6 +440,7 @@ purlin_status purlin_finalize(purlin_ctx *ctx) {
     purlin_status st = PURLIN_OK;
     if (cudaStreamSynchronize(ctx->stream) != cudaSuccess) st = PURLIN_ERR_CUDA;
     for (CacheEntry &e : ctx->lru) drop_entry(e);
+    for (DeviceCollMem &m : ctx->device_colls) free_device_coll(m);
     if (ctx->flags) cudaFree(ctx->flags);
     if (ctx->err) cudaFree(ctx->err);
     delete ctx;
@@ -579,5 +626,134 @@ purlin_status purlin_plan_inspect(purlin_collective coll, int R, const void *con
     }
     return PURLIN_OK;
 }
+
+purlin_status purlin_device_prepare(purlin_ctx *ctx, purlin_collective coll,
+                                    const void *const src[], void *const dst[], size_t n,
+                                    const size_t counts[], purlin_dtype dtype, purlin_op op,
+                                    purlin_layout layout, int blocks,
+                                    uint32_t max_workspace_bytes, purlin_device_coll *out) {
+    if (ctx == nullptr || out == nullptr) return PURLIN_ERR_INVALID_ARG;
+    if ((int)coll < 0 || (int)coll > (int)PURLIN_COLL_ALL_TO_ALL_V) return PURLIN_ERR_INVALID_ARG;
+    if (blocks < 1 || blocks > 65535) return PURLIN_ERR_INVALID_ARG;
+    const bool is_v = coll == PURLIN_COLL_ALL_GATHER_V || coll == PURLIN_COLL_REDUCE_SCATTER_V ||
+                      coll == PURLIN_COLL_ALL_TO_ALL_V;
+    const CallDesc c = make_desc(coll, ctx->R, is_v ? 0 : n, is_v ? counts : nullptr, dtype, op,
+                                 layout);
+    purlin_status st = validate_call(c, src, dst);
+    if (st != PURLIN_OK) return st;
+
+    // The launch's CTA budget for the workspace: the caller's cap, else the
+    // device maximum less room for the kernel's own static shared memory.
+    const uint32_t dev_limit = (uint32_t)ctx->max_smem - 4096u;
+    const uint32_t limit = max_workspace_bytes ? std::min(max_workspace_bytes, dev_limit) : dev_limit;
+    const uint32_t ctl_bytes = 128;   // snac::Ctl, padded to the workspace alignment
+    if (limit <= ctl_bytes) return PURLIN_ERR_UNSUPPORTED;
+
+    const Policy shape = call_policy(ctx, c);
+    const int64_t chunk_opt = ctx->opt[PURLIN_OPT_CHUNK_BYTES];
+    uint32_t chunk = (uint32_t)(chunk_opt > 0 ? chunk_opt : shape.chunk);
+    Plan pl;
+    RingShape rs;
+    for (;;) {   // halve the chunk until the ring fits the cap
+        st = compile_plan(c, kVariantThroughput, (int)ctx->opt[PURLIN_OPT_AR_MODE],
+                          chunk * (uint32_t)c.R, chunk, &pl);
+        if (st != PURLIN_OK) return st;
+        st = ring_shape(ctx, c, shape, pl, limit - ctl_bytes, &rs);
+        if (st == PURLIN_OK) break;
+        if (st != PURLIN_ERR_UNSUPPORTED || chunk <= 256) return st;
+        chunk = std::max<uint32_t>(256, (chunk / 2) & ~15u);
+    }
+    if (pl.composed && pl.notify_chunks > (uint64_t)kFlagSlots * 0xFFFFull)
+        return PURLIN_ERR_INVALID_ARG;
+
+    purlin_device_coll d;
+    std::memset(&d, 0, sizeof d);
+    for (int r = 0; r < c.R; ++r) {
+        d.src[r] = src[r];
+        d.dst[r] = dst[r];
+    }
+    d.nchunks = pl.nchunks;
+    d.nunits = pl.nunits;
+    d.epoch_inc = 1;
+    d.timeout_ns = ctx->opt[PURLIN_OPT_SPIN_TIMEOUT_NS] > 0 ? ctx->opt[PURLIN_OPT_SPIN_TIMEOUT_NS]
+                                                            : kDefaultTimeoutNs;
+    d.drop_notify = ctx->opt[PURLIN_OPT_DROP_NOTIFY];
+    d.flag_slots = 1;
+    d.stages = rs.stages;
+    d.slot_stride = rs.slot_stride;
+    d.workspace_bytes = rs.smem + ctl_bytes;
+    d.nseg = (int32_t)pl.segs.size();
+    d.R = c.R;
+    d.dtype = dtype;
+    d.vector_copies = rs.vector_copies ? 1 : 0;
+    d.blocks = blocks;
+    d.threads = 32 * (2 + rs.consumer_warps);
+    d.composed = pl.composed ? 1 : 0;
+    d.coll = coll;
+
+    DeviceCollMem m;
+    auto fail = [&](purlin_status s) {
+        free_device_coll(m);
+        return s;
+    };
+    const size_t seg_bytes = std::max<size_t>(1, pl.segs.size()) * sizeof(Seg);
+    if (cudaMalloc(&m.segs, seg_bytes) != cudaSuccess ||
+        cudaMalloc(&m.epochs, (size_t)blocks * sizeof(unsigned long long)) != cudaSuccess ||
+        cudaMalloc(&m.err, sizeof(unsigned long long)) != cudaSuccess)
+        return fail(PURLIN_ERR_OOM);
+    if (pl.composed) {
+        flag_geometry(pl.notify_chunks, blocks, &d.flag_slots, &d.epoch_inc);
+        if (cudaMalloc(&m.flags, 2 * (size_t)d.flag_slots * sizeof(unsigned long long)) !=
+            cudaSuccess)
+            return fail(PURLIN_ERR_OOM);
+        if (cudaMemset(m.flags, 0, 2 * (size_t)d.flag_slots * sizeof(unsigned long long)) !=
+            cudaSuccess)
+            return fail(PURLIN_ERR_CUDA);
+    }
+    // Every CTA starts at epoch 1: flags start at 0, below any epoch.
+    std::vector<unsigned long long> ep((size_t)blocks, 1ull);
+    if ((!pl.segs.empty() &&
+         cudaMemcpy(m.segs, pl.segs.data(), pl.segs.size() * sizeof(Seg),
+                    cudaMemcpyHostToDevice) != cudaSuccess) ||
+        cudaMemcpy(m.epochs, ep.data(), ep.size() * sizeof(unsigned long long),
+                   cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemset(m.err, 0, sizeof(unsigned long long)) != cudaSuccess)
+        return fail(PURLIN_ERR_CUDA);
+    d.segs = m.segs;
+    d.flags = m.flags;
+    d.epochs = m.epochs;
+    d.err = m.err;
+    ctx->device_colls.push_back(m);
+    d.owner = &ctx->device_colls.back();
+    *out = d;
+    return PURLIN_OK;
+}
+
+purlin_status purlin_device_check(const purlin_device_coll *coll, purlin_stream stream) {
+    if (coll == nullptr || coll->err == nullptr) return PURLIN_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return PURLIN_ERR_CUDA;
+    unsigned long long word = 0;
+    if (cudaMemcpy(&word, coll->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PURLIN_ERR_CUDA;
+    if (word == 0) return PURLIN_OK;
+    if (cudaMemset(coll->err, 0, sizeof word) != cudaSuccess) return PURLIN_ERR_CUDA;
+    return static_cast<purlin_status>(word & 0xFF);
+}
+
+purlin_status purlin_device_release(purlin_ctx *ctx, purlin_device_coll *coll) {
+    if (ctx == nullptr || coll == nullptr) return PURLIN_ERR_INVALID_ARG;
+    if (coll->owner == nullptr) return PURLIN_OK;
+    for (auto it = ctx->device_colls.begin(); it != ctx->device_colls.end(); ++it) {
+        if (&*it != coll->owner) continue;
+        free_device_coll(*it);
+        ctx->device_colls.erase(it);
+        std::memset(coll, 0, sizeof *coll);
+        return PURLIN_OK;
+    }
+    return PURLIN_ERR_INVALID_ARG;
+}
+
+size_t purlin_device_coll_size(void) { return sizeof(purlin_device_coll); }
 
 }  // extern "C"

@@ -32,6 +32,12 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
                  : "memory");
 }
 
+// Retire a barrier whose every phase has completed, before its shared
+// memory is used for anything else (including a new mbarrier).
+__device__ __forceinline__ void mbar_inval(uint64_t *bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // Make barrier initialisation visible to the bulk-copy engine.
 __device__ __forceinline__ void mbar_init_fence() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

@@ -13,14 +13,6 @@ constexpr int kSmallMaxSeg = 16;
 constexpr int kBigMaxR = PURLIN_MAX_RANKS;  // ... and big
 constexpr int kBigMaxSeg = 64;
 
-// Error word layout: bits 0..7 status, 8..15 site, 16..63 chunk or unit.
-enum ErrSite : uint64_t {
-    kSiteFlagWait = 1,
-    kSiteRingFull = 2,
-    kSiteRingEmpty = 3,
-    kSiteChunkDone = 4,
-};
-
 struct LaunchArgs {
     const Plan *plan = nullptr;
     const Seg *segs_dev = nullptr;   // device copy of plan->segs, or null (inline)
@@ -58,8 +50,7 @@ cudaError_t configure_kernels(int max_dyn_smem);
 cudaError_t throughput_occupancy(int dtype, int pclass, int block, size_t smem, int *per_sm);
 
 // Shared-memory bytes a throughput launch needs for `stages` ring slots of
-// `slot_stride` bytes, their three mbarriers each, and the staged segment
-// table.
+// `slot_stride` bytes, their mbarriers and the staged segment table.
 uint32_t throughput_smem(uint32_t stages, uint32_t slot_stride);
 
 }  // namespace purlin

@@ -35,15 +35,6 @@ bool ranges_overlap(uintptr_t a, uint64_t la, uintptr_t b, uint64_t lb) {
     return a < b + lb && b < a + la;
 }
 
-// Vector units covering the destination bytes [dst_off + a, dst_off + b):
-// one unit per 16-byte window of the destination address space.
-uint64_t units_in(uint64_t dst_off, uint64_t a, uint64_t b) {
-    if (b <= a) return 0;
-    uint64_t first = (dst_off + a) / 16;
-    uint64_t last = (dst_off + b + 15) / 16;
-    return last - first;
-}
-
 struct RawSeg {
     uint64_t src_off, dst_off, bytes;
     int src_rank, dst_rank, skip_rank;
@@ -335,15 +326,13 @@ purlin_status compile_plan(const CallDesc &c, int variant, int ar_mode, uint32_t
             // The body is cut on the destination side (16-byte aligned stores);
             // a source at another 16-byte phase is staged as its aligned hull,
             // 16 bytes longer, and shifted into place by the consumer warps.
-            uint64_t head = std::min<uint64_t>((16u - (r.dst_off & 15u)) & 15u, r.bytes);
-            uint64_t rest = r.bytes - head;
-            uint64_t tail = rest & 15u;
-            body = rest - tail;
+            const Cut cut = cut_transfer(r.src_off, r.dst_off, r.bytes);
+            body = cut.body;
             if (body > 0) {
                 s.tma = 1;
-                s.head = (uint8_t)head;
-                s.tail = (uint8_t)tail;
-                s.shift = (uint8_t)((r.src_off - r.dst_off) & 15u);
+                s.head = (uint8_t)cut.head;
+                s.tail = (uint8_t)cut.tail;
+                s.shift = (uint8_t)cut.shift;
             }
         }
         p.total_bytes += r.bytes;

@@ -20,6 +20,12 @@
 
 #include "../../include/purlin.h"
 
+#if defined(__CUDACC__)
+#define PURLIN_HD __host__ __device__
+#else
+#define PURLIN_HD
+#endif
+
 namespace purlin {
 
 constexpr int kRankAll = -1;
@@ -60,6 +66,38 @@ struct Seg {
     uint8_t pad[2];
 };
 static_assert(sizeof(Seg) == 56, "Seg layout is part of the kernel parameter block");
+
+// The ring's cut of one transfer: the bytes before the destination's first
+// 16-byte boundary (head) and after its last (tail) go through the vector
+// path; the aligned body goes through the ring in chunks.  A source at
+// another 16-byte phase (shift != 0) is staged as its aligned hull and
+// shifted into place.  Used by the host plan compiler and by the device-side
+// Atom, so both cut a transfer the same way.
+struct Cut {
+    uint64_t body;
+    uint32_t head, tail, shift;
+};
+
+PURLIN_HD inline Cut cut_transfer(uint64_t src_off, uint64_t dst_off, uint64_t bytes) {
+    Cut c;
+    const uint64_t lead = (16u - (dst_off & 15u)) & 15u;
+    const uint64_t head = lead < bytes ? lead : bytes;
+    const uint64_t rest = bytes - head;
+    c.head = (uint32_t)head;
+    c.tail = (uint32_t)(rest & 15u);
+    c.body = rest - c.tail;
+    c.shift = (uint32_t)((src_off - dst_off) & 15u);
+    return c;
+}
+
+// Vector units covering the destination bytes [dst_off + a, dst_off + b):
+// one unit per 16-byte window of the destination address space.
+PURLIN_HD inline uint64_t units_in(uint64_t dst_off, uint64_t a, uint64_t b) {
+    if (b <= a) return 0;
+    const uint64_t first = (dst_off + a) / 16;
+    const uint64_t last = (dst_off + b + 15) / 16;
+    return last - first;
+}
 
 struct Plan {
     std::vector<Seg> segs;

@@ -1,0 +1,612 @@
+// snac.cuh -- the device side of SNAC (stage, notify, consume) over the
+// Atom primitives, as device functions.  The library's own kernels call them
+// with their launch's CTA index and count; kernels written against the
+// device API (include/purlin_device.cuh) call the same functions with the
+// CTAs they hand to a collective.
+//
+// "Purlin: Separating Orchestration from the Datapath of Collectives":
+//   §3.2  SNAC: chunks are staged, their readiness is notified, consumers
+//         then copy or reduce them; composed AllReduce overlaps staging,
+//         reduction and gathering on chunks.
+//   §3.3  the Atom pipeline stages data in CTA-local shared memory so
+//         fetches overlap with processing; SCORE reductions.
+//   §4.3  a monotonic 64-bit epoch is the notification value and its
+//         parity selects the buffer set.
+// "Purlin" project README, "Device-side": Atoms and collectives are callable
+// from inside a user kernel; exactly `blocks` CTAs enter a collective.
+//
+// Vector units (do_unit): one 16-byte destination window each; 128-bit
+// loads of every source, ordered binary32 accumulation, 128-bit stores.
+//
+// The ring (run_ring): persistent CTAs with three warp roles over a ring of
+// shared-memory stages.
+//   warp 0     Stage: lane s issues cp.async.bulk global -> shared for
+//              source s of the chunk (R tiles for a reduce, one for a
+//              copy); completion on the stage's mbarrier.  A chunk that
+//              depends on another CTA's chunk first acquires that chunk's
+//              flag (bounded spin, whole warp).
+//   warp 1     Consume (copy): lane d issues cp.async.bulk shared -> global
+//              to destination d.  Notify: for a chunk other CTAs wait on,
+//              once the consumer warps report it stored, release-store
+//              epoch + generation into its flag (batched behind one
+//              GPU-scope fence).
+//   warps 2..  Consume (reduce, and copies that are shifted or stored with
+//              vector stores): SCORE over the R tiles, each thread storing
+//              its 16-byte results straight to one or all destinations;
+//              also the ragged head/tail units.
+// Every wait is bounded; an expired wait records PURLIN_ERR_TIMEOUT in the
+// error word and the CTA winds down (its own bulk copies are waited for).
+//
+// Parameter objects (class P) expose: src[] and dst[] (rank buffer bases),
+// segs / segs_dev (segment table), flags, err, nchunks, nunits, epoch,
+// timeout_ns, drop_notify, flag_slots, stages, slot_stride, nseg, R and
+// vector_copies.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "atom.cuh"
+#include "plan.h"
+
+namespace purlin {
+namespace snac {
+
+constexpr int kNotifyBatch = 8;                   // flags published behind one fence
+constexpr uint64_t kRingWaitNs = 2000000000ull;   // 2 s bound on a ring wait
+constexpr int kSmemSegs = 64;                     // segment table entries staged in the ring's workspace
+
+// Error word layout: bits 0..7 status, 8..15 site, 16..63 chunk, unit or CTA.
+enum ErrSite : uint64_t {
+    kSiteFlagWait = 1,
+    kSiteRingFull = 2,
+    kSiteRingEmpty = 3,
+    kSiteChunkDone = 4,
+    kSiteDeviceArgs = 5,   // a device-API call with arguments that do not match its descriptor
+};
+
+struct Ctl {
+    int abort;
+    int pad;
+    unsigned long long epoch;   // device API: this CTA's epoch for the call
+};
+
+// Bytes of the ring's workspace: S stages of slot_stride bytes, 4*S
+// mbarriers (full, empty, a 2*S completion ring) and the staged segment
+// table.  Callers that keep a Ctl in the workspace add it after this.
+__host__ __device__ constexpr uint32_t ring_workspace_bytes(uint32_t stages, uint32_t slot_stride) {
+    return stages * slot_stride + 4 * stages * 8 + kSmemSegs * (uint32_t)sizeof(Seg);
+}
+
+template <class P>
+__device__ __forceinline__ const Seg *seg_table(const P &p) {
+    return p.segs_dev != nullptr ? p.segs_dev : p.segs;
+}
+
+// Copy the segment table (from the parameter block or device memory) into
+// shared memory with every thread of the CTA: one round of parallel loads
+// instead of a chain of dependent reads in each lookup.  Tables of more than
+// `cap` segments stay where they are.  The caller synchronises the CTA
+// before the table is read.
+template <class P>
+__device__ __forceinline__ const Seg *stage_segs(const P &p, Seg *sm, int cap) {
+    if (p.nseg > cap) return seg_table(p);
+    const uint64_t *from = reinterpret_cast<const uint64_t *>(seg_table(p));
+    uint64_t *to = reinterpret_cast<uint64_t *>(sm);
+    const int words = p.nseg * (int)(sizeof(Seg) / sizeof(uint64_t));
+    for (int i = threadIdx.x; i < words; i += blockDim.x) to[i] = from[i];
+    return sm;
+}
+
+// Last segment whose first chunk (unit) index is <= x: the one holding x.
+__device__ __forceinline__ int seg_of_chunk(const Seg *segs, int nseg, uint64_t x) {
+    int lo = 0, hi = nseg;   // answer in [lo, hi)
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if ((uint64_t)segs[mid].chunk_begin <= x) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ int seg_of_unit(const Seg *segs, int nseg, uint64_t x) {
+    int lo = 0, hi = nseg;
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (segs[mid].unit_begin <= x) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ void record_error(unsigned long long *err, uint64_t code, uint64_t site,
+                                             uint64_t where) {
+    unsigned long long v = (unsigned long long)((code & 0xFF) | ((site & 0xFF) << 8) |
+                                                ((where & 0xFFFFFFFFFFFFull) << 16));
+    atomicCAS(err, 0ull, v);
+}
+
+__device__ __forceinline__ bool error_set(const unsigned long long *err) {
+    return *reinterpret_cast<const volatile unsigned long long *>(err) != 0ull;
+}
+
+// ------------------------------------------------------------ vector unit --
+
+// One 16-byte destination window of a segment: copy or reduce it to every
+// destination.  A full window whose source is 16-byte aligned uses 128-bit
+// accesses; anything else goes element by element.
+template <int DT, int MAXR, class P>
+__device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
+    using V = atom::Vec<DT>;
+    constexpr int ES = DT == PURLIN_F32 ? 4 : 2;
+    uint64_t lo, hi;
+    if (sg.tma) {
+        if (k == 0 && sg.head) {
+            lo = 0;
+            hi = sg.head;
+        } else {
+            lo = sg.bytes - sg.tail;
+            hi = sg.bytes;
+        }
+    } else {
+        const uint64_t a = (sg.dst_off / 16 + k) * 16;
+        lo = (a > sg.dst_off ? a : sg.dst_off) - sg.dst_off;
+        const uint64_t b = a + 16, e = sg.dst_off + sg.bytes;
+        hi = (b < e ? b : e) - sg.dst_off;
+    }
+    const int R = p.R;
+    // A full destination window is written with one 128-bit store.  Its 16
+    // source bytes are one aligned vector (same phase), or two aligned
+    // vectors shifted into place when both lie inside the segment's source
+    // range (so no byte outside the segment is read); else element by element.
+    const bool full = hi - lo == 16;
+    const uint64_t sx = sg.src_off + lo;
+    const uint32_t sh = (uint32_t)(sx & 15u);
+    const uint64_t sxa = sx - sh;
+    const bool vec = full && sh == 0;
+    const bool shifted = full && sh != 0 && sxa >= sg.src_off && sxa + 32 <= sg.src_off + sg.bytes;
+    const uint64_t doff = sg.dst_off + lo;
+
+    if (sg.src_rank >= 0) {   // copy, bitwise
+        const char *s = static_cast<const char *>(sg.src_is_dst ? p.dst[sg.src_rank]
+                                                                : p.src[sg.src_rank]) +
+                        sg.src_off + lo;
+        // Read the window once (16 bytes, as a vector or element by element),
+        // then write it to every destination.
+        constexpr int NE = 16 / ES;
+        const int ne = (int)((hi - lo) / ES);
+        uint4 v = make_uint4(0, 0, 0, 0);
+        uint32_t e[NE];
+        if (vec) {
+            v = atom::ld_v4(s);
+        } else if (shifted) {
+            const char *a = s - sh;
+            v = atom::shift_pair(atom::ld_v4_l1(a), atom::ld_v4_l1(a + 16), sh);
+        } else {
+#pragma unroll
+            for (int j = 0; j < NE; ++j)
+                e[j] = j < ne ? (ES == 4 ? *reinterpret_cast<const uint32_t *>(s + j * ES)
+                                         : *reinterpret_cast<const uint16_t *>(s + j * ES))
+                              : 0u;
+        }
+        auto put = [&](char *d) {
+            if (d == s) return;   // in-place AllGather: the block is already there
+            if (vec || shifted) {
+                atom::st_v4(d, v);
+            } else {
+#pragma unroll
+                for (int j = 0; j < NE; ++j) {
+                    if (j >= ne) break;
+                    if (ES == 4) *reinterpret_cast<uint32_t *>(d + j * ES) = e[j];
+                    else *reinterpret_cast<uint16_t *>(d + j * ES) = (uint16_t)e[j];
+                }
+            }
+        };
+        if (sg.dst_rank >= 0) {
+            put(static_cast<char *>(p.dst[sg.dst_rank]) + doff);
+        } else {
+            for (int d = 0; d < R; ++d)
+                if (d != sg.skip_rank) put(static_cast<char *>(p.dst[d]) + doff);
+        }
+        return;
+    }
+
+    // reduce (SCORE): rank order 0..R-1, binary32, one rounding at the end
+    const uint64_t soff = sg.src_off + lo;
+    if (vec || shifted) {
+        // source j's 16 bytes: one aligned vector, or two shifted into place
+        auto load = [&](int j) -> uint4 {
+            const char *b = static_cast<const char *>(p.src[j]) + soff;
+            if (vec) return atom::ld_v4(b);
+            return atom::shift_pair(atom::ld_v4_l1(b - sh), atom::ld_v4_l1(b - sh + 16), sh);
+        };
+        float acc[V::VE];
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j < R) v[j] = load(j);
+        V::init(acc, v[0]);
+#pragma unroll
+        for (int j = 1; j < 8; ++j)
+            if (j < R) V::add(acc, v[j]);
+        if (MAXR > 8) {
+            for (int s0 = 8; s0 < R; s0 += 8) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (s0 + j < R) v[j] = load(s0 + j);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (s0 + j < R) V::add(acc, v[j]);
+            }
+        }
+        const uint4 out = V::pack(acc);
+        if (sg.dst_rank >= 0) {
+            atom::st_v4(static_cast<char *>(p.dst[sg.dst_rank]) + doff, out);
+        } else {
+            for (int d = 0; d < R; ++d)
+                if (d != sg.skip_rank) atom::st_v4(static_cast<char *>(p.dst[d]) + doff, out);
+        }
+        return;
+    }
+    for (uint64_t j = 0; j < hi - lo; j += ES) {
+        float acc = atom::load_elem<DT>(static_cast<const char *>(p.src[0]) + soff + j);
+        for (int s = 1; s < R; ++s)
+            acc = __fadd_rn(acc, atom::load_elem<DT>(static_cast<const char *>(p.src[s]) + soff + j));
+        if (sg.dst_rank >= 0) {
+            atom::store_elem<DT>(static_cast<char *>(p.dst[sg.dst_rank]) + doff + j, acc);
+        } else {
+            for (int d = 0; d < R; ++d)
+                if (d != sg.skip_rank)
+                    atom::store_elem<DT>(static_cast<char *>(p.dst[d]) + doff + j, acc);
+        }
+    }
+}
+
+// Units u0, u0 + stride, ... of the plan: the first one's segment is found by
+// binary search, later ones by walking forward (units only increase), so
+// the search cost fades for threads that own many units.
+template <int DT, int MAXR, class P>
+__device__ __forceinline__ void units_loop(const P &p, const Seg *segs, uint64_t u0,
+                                           uint64_t stride) {
+    if (u0 >= p.nunits) return;
+    int si = seg_of_unit(segs, p.nseg, u0);
+    for (uint64_t u = u0; u < p.nunits; u += stride) {
+        while (si + 1 < p.nseg && segs[si + 1].unit_begin <= u) ++si;
+        do_unit<DT, MAXR>(p, segs[si], u - segs[si].unit_begin);
+    }
+}
+
+// ------------------------------------------------------------------ ring --
+
+struct ChunkGeo {
+    const Seg *sg;
+    uint64_t ci;      // chunk index within the segment
+    uint64_t off;     // byte offset of the chunk within the segment
+    uint32_t bytes;   // bytes per source
+};
+
+__device__ __forceinline__ ChunkGeo chunk_geo(const Seg *segs, int nseg, uint64_t c) {
+    ChunkGeo g;
+    g.sg = &segs[seg_of_chunk(segs, nseg, c)];
+    const Seg &sg = *g.sg;
+    g.ci = c - sg.chunk_begin;
+    const uint64_t body = sg.bytes - sg.head - sg.tail;
+    const uint64_t done = g.ci * sg.chunk_bytes;
+    g.off = sg.head + done;
+    const uint64_t rem = body - done;
+    g.bytes = (uint32_t)(rem < sg.chunk_bytes ? rem : sg.chunk_bytes);
+    return g;
+}
+
+// Bounded wait on an mbarrier phase.  `abortable`: give up as soon as
+// another role of the CTA has given up.
+__device__ __forceinline__ bool ring_wait(uint64_t *bar, uint32_t parity, volatile Ctl *ctl,
+                                          unsigned long long *err, uint64_t site, bool abortable) {
+    if (atom::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = atom::globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (atom::mbar_try_wait(bar, parity)) return true;
+        if ((it & 31u) == 0) {
+            if (abortable && ctl->abort) return false;
+            if (atom::globaltimer_ns() - t0 > kRingWaitNs) {
+                record_error(err, PURLIN_ERR_TIMEOUT, site, blockIdx.x);
+                ctl->abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// SNAC consume-side acquire, warp-wide: lane l waits until notifying chunks
+// d0 + l, d0 + l + 32, ... hold at least this call's value for them, so the
+// flags are polled in parallel rather than one dependent round trip after
+// another.  Each wait is bounded; on expiry the error word is set and later
+// waits of the launch are skipped.  __syncwarp then orders every lane's
+// acquire before the bulk load lane 0 issues next.
+template <class P>
+__device__ void acquire_range(const P &p, uint64_t d0, uint64_t d1, int lane) {
+    for (uint64_t d = d0 + (uint64_t)lane; d < d1; d += 32) {
+        if (error_set(p.err)) break;
+        const unsigned long long *f = p.flags + (d % p.flag_slots);
+        const unsigned long long want = p.epoch + d / p.flag_slots;
+        if (atom::flag_acquire(f) >= want) continue;
+        const uint64_t t0 = atom::globaltimer_ns();
+        uint32_t ns = 32;
+        while (atom::flag_acquire(f) < want) {
+            if ((int64_t)(atom::globaltimer_ns() - t0) > p.timeout_ns) {
+                record_error(p.err, PURLIN_ERR_TIMEOUT, kSiteFlagWait, d);
+                break;
+            }
+            __nanosleep(ns);
+            if (ns < 1024) ns <<= 1;
+        }
+    }
+    __syncwarp();
+    atom::fence_async_global();   // the staged reads that follow are async-proxy reads
+}
+
+// SNAC notify: publish a completed chunk (its stores are complete and
+// ordered before this store by the caller).
+template <class P>
+__device__ __forceinline__ void notify_chunk(const P &p, uint64_t c) {
+    if ((int64_t)c == p.drop_notify) return;   // host-side fault injection
+    atom::flag_release(p.flags + (c % p.flag_slots), p.epoch + c / p.flag_slots);
+}
+
+template <int DT, int MAXR, class P>
+__device__ void run_ring(const P &p, unsigned char *smem, Ctl *ctl_p, uint32_t bidx,
+                         uint32_t nblk) {
+    using V = atom::Vec<DT>;
+    Ctl &ctl = *ctl_p;
+    // Generic-proxy writes made before this call (by this CTA, or by others
+    // and ordered by the caller's grid barrier) precede the bulk loads below.
+    atom::fence_async_global();
+
+    const uint32_t S = p.stages;
+    const int R = p.R;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ncw = (int)(blockDim.x >> 5) - 2;   // consumer warps
+
+    unsigned char *ring = smem;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)S * p.slot_stride);
+    uint64_t *full = bars;           // S: producer arrive + transaction bytes
+    uint64_t *empty = bars + S;      // S: ncw + 1 arrivals: every consumer warp and the writer
+    uint64_t *cdone = bars + 2 * S;  // 2S: ncw arrivals: chunk k (entry k mod 2S) to publish
+                                     //     has been stored
+    // Every role waits on full[] for EVERY chunk, in order, and arrives once
+    // per chunk on empty[]: a parity wait is only sound if the slot's
+    // previous phase is known complete, and a slot is refilled only after
+    // every role has passed it.  cdone[] has 2S entries: the writer's arrival
+    // on empty[] for chunk k + S comes after its wait on cdone for chunk k,
+    // so the consumer warps are never 2S chunks ahead of that wait.
+    const uint32_t C = 2 * S;
+    const Seg *segs = stage_segs(p, reinterpret_cast<Seg *>(bars + 4 * S), kSmemSegs);
+
+    if (threadIdx.x == 0) {
+        for (uint32_t i = 0; i < S; ++i) {
+            atom::mbar_init(&full[i], 1);
+            atom::mbar_init(&empty[i], (uint32_t)ncw + 1u);
+        }
+        for (uint32_t i = 0; i < C; ++i) atom::mbar_init(&cdone[i], (uint32_t)ncw);
+        ctl.abort = 0;
+        atom::mbar_init_fence();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- Stage --
+        // The whole warp walks the chunk list; lane s issues the bulk load
+        // of source s, so the R loads of a chunk go out in parallel.
+        const uint64_t pol = atom::policy_evict_first();
+        uint32_t k = 0;
+        for (uint64_t c = bidx; c < p.nchunks; c += nblk, ++k) {
+            const uint32_t slot = k % S;
+            bool ok = true;
+            if (k >= S)
+                ok = ring_wait(&empty[slot], ((k / S) & 1u) ^ 1u, &ctl, p.err, kSiteRingEmpty, true);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            const ChunkGeo g = chunk_geo(segs, p.nseg, c);
+            const Seg &sg = *g.sg;
+            if (sg.sync == kSyncWait) {
+                // the notifying chunks this one covers, polled by the whole warp
+                const uint32_t ratio = sg.dep_ratio ? sg.dep_ratio : 1u;
+                const uint32_t rc = sg.chunk_bytes / ratio;
+                const uint64_t nred = (sg.bytes - sg.head - sg.tail + rc - 1) / rc;
+                const uint64_t d0 = g.ci * ratio;
+                const uint64_t d1 = d0 + ratio < nred ? d0 + ratio : nred;
+                acquire_range(p, sg.dep_chunk + d0, sg.dep_chunk + d1, lane);
+            }
+            unsigned char *sp = ring + (size_t)slot * p.slot_stride;
+            const int nsrc = sg.src_rank < 0 ? R : 1;
+            // A shifted source is staged as its 16-byte aligned hull.
+            const uint32_t extra = sg.shift ? 16u : 0u;
+            const uint32_t tile = sg.chunk_bytes + extra;
+            const uint32_t ld_bytes = g.bytes + extra;
+            if (lane == 0) atom::mbar_arrive_expect_tx(&full[slot], ld_bytes * (uint32_t)nsrc);
+            __syncwarp();
+            for (int s = lane; s < nsrc; s += 32) {
+                const char *base =
+                    sg.src_rank < 0 ? static_cast<const char *>(p.src[s])
+                                    : static_cast<const char *>(sg.src_is_dst ? p.dst[sg.src_rank]
+                                                                              : p.src[sg.src_rank]);
+                atom::bulk_load(sp + (size_t)s * tile, base + sg.src_off + g.off - sg.shift,
+                                ld_bytes, &full[slot], pol);
+            }
+        }
+        // Every load this warp issued must land before the CTA exits.
+        const uint32_t issued = k;
+        if (lane == 0)
+            for (uint32_t j = issued > S ? issued - S : 0; j < issued; ++j)
+                ring_wait(&full[j % S], (j / S) & 1u, &ctl, p.err, kSiteRingFull, false);
+    } else if (warp == 1) {
+        // ------------------------- Consume (copy): write-back; Notify --
+        // Lane d issues the bulk store to destination d; each lane tracks its
+        // own bulk groups, and lane 0 hands a stage back once every lane's
+        // stores have read it.
+        const uint64_t pol = atom::policy_evict_first();
+        uint32_t k = 0;
+        int owed = -1;             // slot whose release waits on the newest bulk group
+        uint64_t cd_phase = 0;     // per-slot phase bit of cdone (lane 0)
+        // Chunks seen stored (cdone) whose flags are not yet published: one
+        // GPU-scope fence covers a whole batch, off the stage-release path.
+        uint64_t pend[kNotifyBatch];
+        int npend = 0;
+        auto publish = [&]() {
+            if (lane == 0 && npend > 0) {
+                atom::fence_acq_rel_gpu();   // the consumer warps' stores, at GPU scope
+                for (int i = 0; i < npend; ++i) notify_chunk(p, pend[i]);
+            }
+            npend = 0;
+        };
+        for (uint64_t c = bidx; c < p.nchunks; c += nblk, ++k) {
+            const ChunkGeo g = chunk_geo(segs, p.nseg, c);
+            const Seg &sg = *g.sg;
+            const uint32_t slot = k % S;
+            // Never wait on a chunk that depends on flags with flags of our own
+            // still unpublished.
+            if (sg.sync == kSyncWait) publish();
+            if (sg.src_rank < 0 || sg.shift || p.vector_copies) {
+                // A chunk the consumer warps store.  Settle the owed release
+                // first (never hold a stage while waiting on another), pass
+                // the chunk's full phase, then release it -- for a chunk others
+                // wait on, once the consumer warps report it stored.
+                atom::bulk_wait_read<0>();
+                __syncwarp();
+                bool ok = true;
+                if (lane == 0) {
+                    if (owed >= 0) atom::mbar_arrive(&empty[owed]);
+                    ok = ring_wait(&full[slot], (k / S) & 1u, &ctl, p.err, kSiteRingFull, true);
+                    if (ok) atom::mbar_arrive(&empty[slot]);
+                    if (ok && sg.sync == kSyncNotify) {
+                        const uint32_t e = k % C;
+                        ok = ring_wait(&cdone[e], (uint32_t)(cd_phase >> e) & 1u, &ctl, p.err,
+                                       kSiteChunkDone, true);
+                        if (ok) {
+                            cd_phase ^= 1ull << e;
+                            pend[npend] = c;
+                        }
+                    }
+                }
+                owed = -1;
+                if (!__shfl_sync(0xFFFFFFFFu, (int)ok, 0)) break;   // lane 0 decided
+                if (sg.sync == kSyncNotify && ++npend == kNotifyBatch) publish();
+                continue;
+            }
+            const bool ok = ring_wait(&full[slot], (k / S) & 1u, &ctl, p.err, kSiteRingFull, true);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            const unsigned char *from = ring + (size_t)slot * p.slot_stride;
+            const char *self = static_cast<const char *>(sg.src_is_dst ? p.dst[sg.src_rank]
+                                                                       : p.src[sg.src_rank]) +
+                               sg.src_off + g.off;
+            const uint64_t doff = sg.dst_off + g.off;
+            if (sg.dst_rank >= 0) {
+                char *d = static_cast<char *>(p.dst[sg.dst_rank]) + doff;
+                if (lane == 0 && d != self) atom::bulk_store(d, from, g.bytes, pol);
+            } else {
+                for (int d = lane; d < R; d += 32) {
+                    char *dp = static_cast<char *>(p.dst[d]) + doff;
+                    if (d != sg.skip_rank && dp != self) atom::bulk_store(dp, from, g.bytes, pol);
+                }
+            }
+            atom::bulk_commit();
+            // The previous group has finished reading its stage: hand it back.
+            atom::bulk_wait_read<1>();
+            __syncwarp();
+            if (lane == 0 && owed >= 0) atom::mbar_arrive(&empty[owed]);
+            owed = (int)slot;
+        }
+        atom::bulk_wait_all<0>();
+        atom::fence_async_global();   // the bulk stores, before generic accesses that follow
+        __syncwarp();
+        if (lane == 0 && owed >= 0) atom::mbar_arrive(&empty[owed]);
+        publish();
+    } else {
+        // --------------------------------------------- Consume (reduce) --
+        const int ctid = (int)threadIdx.x - 64;
+        const int nct = (int)blockDim.x - 64;
+        units_loop<DT, MAXR>(p, segs, (uint64_t)bidx * nct + ctid, (uint64_t)nblk * nct);
+        uint32_t k = 0;
+        for (uint64_t c = bidx; c < p.nchunks; c += nblk, ++k) {
+            const ChunkGeo g = chunk_geo(segs, p.nseg, c);
+            const Seg &sg = *g.sg;
+            const bool reduce = sg.src_rank < 0;
+            const uint32_t slot = k % S;
+            // Every lane waits (bounded) and the warp leaves together.
+            const bool ok = ring_wait(&full[slot], (k / S) & 1u, &ctl, p.err, kSiteRingFull, true);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            if (!reduce && !sg.shift && !p.vector_copies) {   // the writer lane stores it
+                __syncwarp();
+                if (lane == 0) atom::mbar_arrive(&empty[slot]);
+                continue;
+            }
+            const unsigned char *sp = ring + (size_t)slot * p.slot_stride;
+            const uint32_t sh = sg.shift;
+            const uint32_t tile = sg.chunk_bytes + (sh ? 16u : 0u);
+            const int nvec = (int)(g.bytes >> 4);
+            const uint64_t doff = sg.dst_off + g.off;
+            // in-place AllGather: the destination block that is the source itself
+            const char *self =
+                reduce ? nullptr
+                       : static_cast<const char *>(sg.src_is_dst ? p.dst[sg.src_rank]
+                                                                 : p.src[sg.src_rank]) +
+                             sg.src_off + g.off;
+            // 16 destination bytes of source tile s at vector v
+            auto tile_v4 = [&](int s, int v) -> uint4 {
+                const unsigned char *t = sp + (size_t)s * tile + 16 * (size_t)v;
+                if (!sh) return atom::lds_v4(t);
+                return atom::lds_v4_shifted(t, sh);
+            };
+            for (int v = ctid; v < nvec; v += nct) {
+                uint4 out;
+                if (reduce) {
+                    float acc[V::VE];
+                    V::init(acc, tile_v4(0, v));
+                    if (MAXR <= 8) {
+#pragma unroll
+                        for (int s = 1; s < MAXR; ++s)
+                            if (s < R) V::add(acc, tile_v4(s, v));
+                    } else {
+#pragma unroll 8
+                        for (int s = 1; s < R; ++s) V::add(acc, tile_v4(s, v));
+                    }
+                    out = V::pack(acc);
+                } else {
+                    out = tile_v4(0, v);
+                }
+                const uint64_t o = doff + 16 * (uint64_t)v;
+                if (sg.dst_rank >= 0) {
+                    if (static_cast<const char *>(p.dst[sg.dst_rank]) + doff != self)
+                        atom::st_v4(static_cast<char *>(p.dst[sg.dst_rank]) + o, out);
+                } else {
+                    for (int d = 0; d < R; ++d)
+                        if (d != sg.skip_rank && static_cast<const char *>(p.dst[d]) + doff != self)
+                            atom::st_v4(static_cast<char *>(p.dst[d]) + o, out);
+                }
+            }
+            if (sg.sync == kSyncNotify) {
+                // Others will read this chunk.  The stores are ordered before
+                // the writer lane's publication by this mbarrier (release at
+                // CTA scope), its wait (acquire), its GPU-scope fence and its
+                // release-store: the pattern of a grid-wide barrier.
+                __syncwarp();
+                if (lane == 0) {
+                    atom::mbar_arrive(&cdone[k % C]);
+                    atom::mbar_arrive(&empty[slot]);
+                }
+            } else {
+                __syncwarp();
+                if (lane == 0) atom::mbar_arrive(&empty[slot]);
+            }
+        }
+    }
+    // Every role is done with the ring: retire its barriers so the caller
+    // may reuse the workspace (another call, or its own data).
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (uint32_t i = 0; i < 2 * S; ++i) atom::mbar_inval(&bars[i]);
+        for (uint32_t i = 0; i < C; ++i) atom::mbar_inval(&cdone[i]);
+    }
+    __syncthreads();
+}
+
+}  // namespace snac
+}  // namespace purlin

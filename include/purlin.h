@@ -298,6 +298,92 @@ purlin_status purlin_plan_inspect(purlin_collective coll, int R, const void *con
                                   purlin_segment *segs, size_t cap, size_t *nseg,
                                   uint64_t *nchunks, uint64_t *nunits);
 
+/* ----------------------------------------------------- device-side API */
+
+/* A collective compiled for kernels that run it themselves (the "Purlin"
+ * project README, "Device-side": a user kernel calls a collective, or an
+ * Atom, from inside itself, so communication fuses with its other work;
+ * paper summary §3: applications invoke the Atom directly).
+ *
+ * purlin_device_prepare fills one of these for one call shape: the
+ * collective, its R rank buffers, counts and dtype, and the number of CTAs
+ * (`blocks`) that will enter it.  The user kernel receives it by value
+ * (a __grid_constant__ parameter) or through a pointer to device memory and
+ * calls purlin::device::collective(coll, args) from include/purlin_device.cuh
+ * in exactly `blocks` CTAs, each with:
+ *   - a 1-D block whose size is a multiple of 32 and at least 96 (warp 0
+ *     stages, warp 1 writes back and publishes, the rest consume; `threads`
+ *     is the size the library's policy would pick);
+ *   - `workspace_bytes` of shared memory, 128-byte aligned, that the
+ *     collective may overwrite (the kernel's dynamic shared memory, usually).
+ * Every call through the same descriptor runs the same collective on the
+ * same buffers; the data may change between calls.  Any number of calls may
+ * follow one another (one per kernel, or several in one kernel): each CTA
+ * keeps its epoch in device memory and advances it by `epoch_inc` per call,
+ * so the CTAs agree as long as all `blocks` of them enter every call.
+ * When `composed` is 1 (AllReduce with PURLIN_OPT_AR_MODE = composed), CTAs
+ * wait on one another's chunk flags: all `blocks` CTAs must be resident at
+ * once (launch cooperatively), or the waits expire and report TIMEOUT.
+ * Pointers in it name device memory that the library owns (segment table,
+ * flags, per-CTA epochs, error word) until purlin_device_release or
+ * purlin_finalize; the caller must not write them. */
+typedef struct purlin_device_coll {
+    const void *src[PURLIN_MAX_RANKS];   /* rank input buffers (device), R used */
+    void *dst[PURLIN_MAX_RANKS];         /* rank output buffers (device), R used */
+    const void *segs;                    /* compiled segment table (device) */
+    unsigned long long *flags;           /* 2 x flag_slots chunk flags, or NULL (not composed) */
+    unsigned long long *epochs;          /* `blocks` per-CTA epochs (device) */
+    unsigned long long *err;             /* error word (device): see purlin_device_check */
+    uint64_t nchunks;                    /* ring chunks of the plan */
+    uint64_t nunits;                     /* vector units of the plan */
+    uint64_t epoch_inc;                  /* odd; added to each CTA's epoch per call */
+    int64_t timeout_ns;                  /* bound on one flag wait */
+    int64_t drop_notify;                 /* PURLIN_OPT_DROP_NOTIFY at prepare time (testing), else -1 */
+    uint32_t flag_slots;                 /* flags per parity (a multiple of blocks) */
+    uint32_t stages;                     /* ring stages */
+    uint32_t slot_stride;                /* bytes per ring stage */
+    uint32_t workspace_bytes;            /* shared memory each entering CTA provides */
+    int32_t nseg;                        /* segments in the table */
+    int32_t R;                           /* rank buffers */
+    int32_t dtype;                       /* purlin_dtype */
+    int32_t vector_copies;               /* aligned copies stored by the consumer warps */
+    int32_t blocks;                      /* CTAs that enter every call */
+    int32_t threads;                     /* suggested block size */
+    int32_t composed;                    /* 1: CTAs wait on one another (all must be resident) */
+    int32_t coll;                        /* purlin_collective */
+    void *owner;                         /* library bookkeeping (host address) */
+} purlin_device_coll;
+
+/* Compile a device-side collective for the context's R.  Arguments as for
+ * the matching host call: `n` for the uniform collectives, `counts` (R or
+ * R*R entries, host memory) for the V ones, NULL otherwise.  `blocks` >= 1
+ * CTAs will enter it.  `max_workspace_bytes` caps the shared memory it may
+ * ask of each CTA (0: the device's opt-in maximum less 4 KiB); the ring
+ * shape follows the host call's policy and the context's options, reduced
+ * to fit.  Allocates device memory and copies the plan there with blocking
+ * calls (not during graph capture).  Errors: those of the host call, plus
+ * INVALID_ARG (blocks < 1 or > 65535, or too many notifying chunks for the
+ * flag array), UNSUPPORTED (no ring fits the cap), OOM and CUDA. */
+purlin_status purlin_device_prepare(purlin_ctx *ctx, purlin_collective coll,
+                                    const void *const src[], void *const dst[], size_t n,
+                                    const size_t counts[], purlin_dtype dtype, purlin_op op,
+                                    purlin_layout layout, int blocks,
+                                    uint32_t max_workspace_bytes, purlin_device_coll *out);
+
+/* Wait for `stream`, then read and clear the descriptor's error word.
+ * Returns OK, INVALID_ARG (a kernel entered with a CTA count, index, block
+ * shape, workspace alignment or dtype that does not match the descriptor),
+ * TIMEOUT (a bounded device wait expired) or CUDA. */
+purlin_status purlin_device_check(const purlin_device_coll *coll, purlin_stream stream);
+
+/* Free the device memory of a descriptor (synchronises the device) and
+ * clear it.  Releasing a cleared descriptor is a no-op.  INVALID_ARG if it
+ * was not prepared on this context. */
+purlin_status purlin_device_release(purlin_ctx *ctx, purlin_device_coll *coll);
+
+/* sizeof(purlin_device_coll) as this library was built (for bindings). */
+size_t purlin_device_coll_size(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -71,3 +71,32 @@ def test_init_without_a_gpu_fails_cleanly(P):
 def test_library_does_not_link_the_oracle(P):
     deps = subprocess.run(["nm", "-D", P.LIB_PATH], capture_output=True, text=True).stdout
     assert "oracle_" not in deps
+
+
+def test_device_coll_layout_matches_the_library(P):
+    """The binding's purlin_device_coll has the size the library was built with."""
+    assert ctypes.sizeof(P.purlin_device_coll) == P.lib.purlin_device_coll_size()
+    # the C layout: two pointer arrays of PURLIN_MAX_RANKS, then the fields
+    assert P.purlin_device_coll.segs.offset == 2 * 8 * P.PURLIN_MAX_RANKS
+
+
+EXAMPLES_HEADER = os.path.join(ROOT, "collective_datapath_atom_gb300", "examples",
+                               "device_examples.h")
+
+
+def test_examples_library_exports_its_header():
+    """The device-API example kernels' library exports what its header declares,
+    and its binding marshals exactly that set."""
+    import __graft_entry__
+
+    __graft_entry__.build()
+    from collective_datapath_atom_gb300 import examples
+
+    text = re.sub(r"/\*.*?\*/", "", open(EXAMPLES_HEADER).read(), flags=re.S)
+    names = sorted(set(re.findall(r"\b(purlin_[a-z_0-9]+)\s*\(", text)))
+    assert names, "no declarations found"
+    nm = subprocess.run(["nm", "-D", "--defined-only", examples.LIB_PATH], capture_output=True,
+                        text=True, check=True).stdout
+    exported = set(line.split()[-1] for line in nm.splitlines() if line.strip())
+    assert set(names) <= exported
+    assert set(examples._SIGNATURES) == set(names)
