@@ -42,6 +42,7 @@ import workloads  # noqa: E402
 L2_FLUSH_BYTES = 512 << 20
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = ["collective_datapath_atom_gb300/csrc/kernels.cu",
+                  "collective_datapath_atom_gb300/csrc/snac.cuh",
                   "collective_datapath_atom_gb300/csrc/atom.cuh"]
 
 
@@ -607,6 +608,56 @@ def sweep(args):
                   "grid": info["grid"], "block": info["block"], "stages": info["stages"]})
         del ins, src, dst
         torch.cuda.empty_cache()
+
+    # ---- the device-side API: the same collectives entered from a user
+    # kernel (examples/), and the Atom's copy bandwidth against CTA count
+    from collective_datapath_atom_gb300 import examples as X
+
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    dev_cases = [(workloads.AG_BF16_R8_8MI.name, 0), (workloads.RS_BF16_R8_128MI.name, 0),
+                 (workloads.ar_sweep_workload(32768).name, 1),
+                 (workloads.ar_sweep_workload(32768).name, 2)]
+    for name, mode in dev_cases:
+        w, ins, src, dst, call, algo, _, _ = setup_workload(name, device)
+        torch.cuda.synchronize()
+        setopt(2, mode)
+        coll = {"all_gather": P.PURLIN_COLL_ALL_GATHER, "reduce_scatter": P.PURLIN_COLL_REDUCE_SCATTER,
+                "all_reduce": P.PURLIN_COLL_ALL_REDUCE}[w.collective]
+        run = make_runner(P, ctx, w, call)
+        run(src, dst)
+        P.purlin_check(ctx)
+        host_us = _events_us(torch, stream, lambda: run(src, dst), 20, flush)[0]
+        grid = P.purlin_last_launch(ctx)["grid"]
+        d = P.purlin_device_prepare(ctx, coll, src, dst, n=w.n, dtype=w.dtype, blocks=grid)
+        fn = lambda: X.collective(d, stream=stream)   # noqa: E731
+        fn()
+        assert P.purlin_device_check(d, stream) == P.PURLIN_OK
+        med, p10, p90 = _events_us(torch, stream, fn, 20, flush)
+        emit({"row": "device_api", "workload": w.name,
+              "mode": {0: "", 1: "fused", 2: "composed"}[mode], "blocks": grid,
+              "threads": d.threads, "us": med, "p10": p10, "p90": p90,
+              "gbs": algo / (med * 1e-6) / 1e9, "frac": algo / (med * 1e-6) / 1e9 / peak,
+              "host_call_us": host_us})
+        P.purlin_device_release(ctx, d)
+        del ins, src, dst
+        torch.cuda.empty_cache()
+    setopt(0)
+    nbytes = 1 << 30
+    a = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    b = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    for ctas in (1, 2, 4, 8, 16, 38, 76, sms, 2 * sms, 3 * sms):
+        per = (nbytes + ctas - 1) // ctas
+        per = (per + 15) // 16 * 16
+        fn = lambda: X.atom_copy(b, a, nbytes, per, status, stream=stream)   # noqa: E731
+        fn()
+        stream.synchronize()
+        assert int(status.item()) == 0
+        med = _events_us(torch, stream, fn, 5 if ctas < 16 else 20, flush)[0]
+        emit({"row": "atom_copy", "ctas": ctas, "bytes": nbytes, "us": med,
+              "gbs": 2 * nbytes / (med * 1e-6) / 1e9,
+              "frac": 2 * nbytes / (med * 1e-6) / 1e9 / peak})
+    del a, b
     ctx.close()
     if args.report:
         with open(args.report, "w") as f:
