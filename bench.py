@@ -642,6 +642,50 @@ def sweep(args):
         del ins, src, dst
         torch.cuda.empty_cache()
     setopt(0)
+
+    # ---- V collectives with device-resident counts: the MoE dispatch with
+    # the count matrix already on the GPU, against the host-count call and
+    # against what a host-count caller must do with GPU counts (copy them
+    # to the host first); also a decode-size dispatch (64 tokens per rank)
+    w, ins, src, dst, call, algo, _, _ = setup_workload(workloads.A2AV_BF16_R8_MOE.name, device)
+    H = workloads.MOE_HIDDEN
+    for label, tokens in (("moe_16384tok", workloads.MOE_TOKENS), ("moe_64tok", 64)):
+        if tokens == workloads.MOE_TOKENS:
+            counts = call[1]
+            s_in = src
+        else:
+            Cs = np.stack([np.random.default_rng(7 + r).multinomial(tokens, workloads.zipf_weights(8))
+                           for r in range(8)])
+            counts = (Cs * H).reshape(-1).tolist()
+            s_in = [x[:tokens * H] for x in src]
+        Cm = np.asarray(counts).reshape(8, 8)
+        in_cap, out_cap = int(Cm.sum(1).max()), int(Cm.sum(0).max())
+        d_out = [torch.empty(out_cap, dtype=torch.int16, device=device) for _ in range(8)]
+        d_counts = torch.tensor(counts, dtype=torch.int64, device=device)
+        torch.cuda.synchronize()
+        algo_c = 2 * int(Cm.sum()) * 2
+        for path, fn in (
+                ("host_counts", lambda: P.purlin_all_to_all_v(ctx, s_in, d_out, counts, 1)),
+                ("device_counts", lambda: P.purlin_all_to_all_v_device_counts(
+                    ctx, s_in, d_out, d_counts, in_cap, out_cap, 1)),
+                ("device_counts_copied_to_host", lambda: P.purlin_all_to_all_v(
+                    ctx, s_in, d_out, d_counts.cpu().tolist(), 1))):
+            fn()
+            P.purlin_check(ctx)
+            med, p10, p90 = _events_us(torch, stream, fn, 30, flush)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(30):
+                fn()
+            torch.cuda.synchronize()
+            wall = (time.perf_counter() - t0) / 30 * 1e6
+            emit({"row": "device_counts", "workload": label, "path": path, "us": med, "p10": p10,
+                  "p90": p90, "wall_us_per_call": wall, "gbs": algo_c / (med * 1e-6) / 1e9,
+                  "frac": algo_c / (med * 1e-6) / 1e9 / peak})
+        del d_out
+    del ins, src, dst
+    torch.cuda.empty_cache()
+
     nbytes = 1 << 30
     a = torch.empty(nbytes, dtype=torch.uint8, device=device)
     b = torch.empty(nbytes, dtype=torch.uint8, device=device)

@@ -125,6 +125,15 @@ _SIGNATURES = {
                                                ctypes.c_int, purlin_layout]),
     "purlin_all_to_all_v": (ctypes.c_int, [_CTX, _VPP, _VPP, _SZP, ctypes.c_int, ctypes.c_int,
                                            purlin_layout]),
+    "purlin_all_gather_v_device_counts": (ctypes.c_int, [
+        _CTX, _VPP, _VPP, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_size_t, ctypes.c_int,
+        ctypes.c_int, purlin_layout]),
+    "purlin_reduce_scatter_v_device_counts": (ctypes.c_int, [
+        _CTX, _VPP, _VPP, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_size_t, ctypes.c_int,
+        ctypes.c_int, purlin_layout]),
+    "purlin_all_to_all_v_device_counts": (ctypes.c_int, [
+        _CTX, _VPP, _VPP, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_size_t, ctypes.c_int,
+        ctypes.c_int, purlin_layout]),
     "purlin_all_reduce_noalloc": (ctypes.c_int, [ctypes.c_int, _VPP, _VPP, ctypes.c_size_t,
                                                  ctypes.c_int, ctypes.c_int, purlin_layout,
                                                  ctypes.c_void_p]),
@@ -291,6 +300,39 @@ def purlin_reduce_scatter_v(ctx, src, dst, counts, dtype, op=None, layout=None):
 def purlin_all_to_all_v(ctx, src, dst, counts, dtype, op=None, layout=None):
     """``counts``: R*R element counts, row s = source, column d = destination."""
     _varlen(lib.purlin_all_to_all_v, "all_to_all_v", ctx, src, dst, counts, dtype, op, layout)
+
+
+def _device_counts(fn, name, ctx, src, dst, counts, in_capacity, out_capacity, dtype, op,
+                   layout):
+    dflt_op, dflt_layout = LAYOUTS[name]
+    op = dflt_op if op is None else op
+    layout = dflt_layout if layout is None else layout
+    ps, _keep1 = _ptr_array(src)
+    pd, _keep2 = _ptr_array(dst)
+    _ok(fn(ctx.handle, ps, pd, ctypes.c_void_p(_addr(counts)), int(in_capacity),
+           int(out_capacity), int(dtype), int(op), _layout(layout)),
+        f"purlin_{name}_device_counts")
+
+
+def purlin_all_gather_v_device_counts(ctx, src, dst, counts, in_capacity, out_capacity, dtype,
+                                      op=None, layout=None):
+    """AllGatherV with the R counts in device memory (a tensor of int64 or a
+    device address)."""
+    _device_counts(lib.purlin_all_gather_v_device_counts, "all_gather_v", ctx, src, dst, counts,
+                   in_capacity, out_capacity, dtype, op, layout)
+
+
+def purlin_reduce_scatter_v_device_counts(ctx, src, dst, counts, in_capacity, out_capacity,
+                                          dtype, op=None, layout=None):
+    _device_counts(lib.purlin_reduce_scatter_v_device_counts, "reduce_scatter_v", ctx, src, dst,
+                   counts, in_capacity, out_capacity, dtype, op, layout)
+
+
+def purlin_all_to_all_v_device_counts(ctx, src, dst, counts, in_capacity, out_capacity, dtype,
+                                      op=None, layout=None):
+    """AllToAllV with the R*R count matrix (row = source) in device memory."""
+    _device_counts(lib.purlin_all_to_all_v_device_counts, "all_to_all_v", ctx, src, dst, counts,
+                   in_capacity, out_capacity, dtype, op, layout)
 
 
 def purlin_all_reduce_noalloc(R, src, dst, n, dtype, op=None, layout=None, stream=None):

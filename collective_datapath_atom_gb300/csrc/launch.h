@@ -36,6 +36,37 @@ struct LaunchArgs {
     cudaStream_t stream = nullptr;
 };
 
+// V collectives with device-resident counts (vcounts.cu).
+constexpr int kVcMaxRanks = 16;   // R*R <= 256 segments per CTA's table
+
+struct VcLaunch {
+    const void *const *src = nullptr;
+    void *const *dst = nullptr;
+    const unsigned long long *counts = nullptr;   // device
+    unsigned long long *err = nullptr;
+    uint64_t in_cap = 0;      // elements
+    uint64_t out_cap = 0;     // elements
+    uint64_t crossover = 0;   // bytes: largest per-rank input run by vector units alone
+    int64_t timeout_ns = 0;
+    uint32_t red_chunk = 0;
+    uint32_t copy_chunk = 0;
+    uint32_t stages = 0;
+    uint32_t slot_stride = 0;
+    int R = 0;
+    int coll = 0;
+    int dtype = 0;
+    bool vector_copies = false;
+    int grid = 0;
+    int block = 0;
+    uint32_t smem = 0;
+    cudaStream_t stream = nullptr;
+};
+
+uint32_t vcounts_smem(int coll, int R, uint32_t stages, uint32_t slot_stride);
+cudaError_t launch_vcounts(const VcLaunch &a);
+cudaError_t configure_vcounts(int max_dyn_smem);
+cudaError_t vcounts_occupancy(int dtype, int R, int block, size_t smem, int *per_sm);
+
 // Which parameter block a call needs (0 small, 1 big), -1 if the plan must
 // live in device memory (more segments than the big block holds).
 int param_class(int R, size_t nseg);

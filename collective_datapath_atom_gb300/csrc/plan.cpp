@@ -105,7 +105,7 @@ uint64_t algorithmic_bytes(const CallDesc &c) {
     return t;
 }
 
-purlin_status validate_call(const CallDesc &c, const void *const src[], void *const dst[]) {
+purlin_status validate_shape(const CallDesc &c, const void *const src[], void *const dst[]) {
     if (c.R < 1 || c.R > PURLIN_MAX_RANKS) return PURLIN_ERR_INVALID_ARG;
     const int es = elem_bytes(c.dtype);
     if (es == 0) return PURLIN_ERR_INVALID_ARG;
@@ -132,6 +132,43 @@ purlin_status validate_call(const CallDesc &c, const void *const src[], void *co
             return PURLIN_ERR_INVALID_ARG;
     }
     if (c.op != want_op || !layout_is(c.layout, want_in, want_out)) return PURLIN_ERR_UNSUPPORTED;
+    return PURLIN_OK;
+}
+
+purlin_status validate_extents(const CallDesc &c, const void *const src[], void *const dst[],
+                               const std::vector<uint64_t> &in_b,
+                               const std::vector<uint64_t> &out_b) {
+    const uint64_t es64 = (uint64_t)elem_bytes(c.dtype);
+    for (int r = 0; r < c.R; ++r) {
+        if (in_b[r] && src[r] == nullptr) return PURLIN_ERR_INVALID_ARG;
+        if (out_b[r] && dst[r] == nullptr) return PURLIN_ERR_INVALID_ARG;
+        if (in_b[r] && ((uintptr_t)src[r] & 15u)) return PURLIN_ERR_ALIGNMENT;
+        if (out_b[r] && ((uintptr_t)dst[r] & 15u)) return PURLIN_ERR_ALIGNMENT;
+    }
+
+    // Outputs never overlap one another.
+    for (int a = 0; a < c.R; ++a)
+        for (int b = a + 1; b < c.R; ++b)
+            if (ranges_overlap((uintptr_t)dst[a], out_b[a], (uintptr_t)dst[b], out_b[b]))
+                return PURLIN_ERR_ALIAS;
+    // An input overlaps no output, except the in-place forms.
+    for (int s = 0; s < c.R; ++s) {
+        for (int d = 0; d < c.R; ++d) {
+            if (!ranges_overlap((uintptr_t)src[s], in_b[s], (uintptr_t)dst[d], out_b[d])) continue;
+            if (s == d && c.coll == PURLIN_COLL_ALL_REDUCE && src[s] == dst[d]) continue;
+            if (s == d && c.coll == PURLIN_COLL_ALL_GATHER &&
+                (uintptr_t)src[s] == (uintptr_t)dst[d] + (uint64_t)s * c.n * es64)
+                continue;
+            return PURLIN_ERR_ALIAS;
+        }
+    }
+    return PURLIN_OK;
+}
+
+purlin_status validate_call(const CallDesc &c, const void *const src[], void *const dst[]) {
+    purlin_status st = validate_shape(c, src, dst);
+    if (st != PURLIN_OK) return st;
+    const int es = elem_bytes(c.dtype);
 
     const bool is_v = c.coll == PURLIN_COLL_ALL_GATHER_V || c.coll == PURLIN_COLL_REDUCE_SCATTER_V ||
                       c.coll == PURLIN_COLL_ALL_TO_ALL_V;
@@ -153,31 +190,7 @@ purlin_status validate_call(const CallDesc &c, const void *const src[], void *co
 
     std::vector<uint64_t> in_b, out_b;
     buffer_bytes(c, in_b, out_b);
-    for (int r = 0; r < c.R; ++r) {
-        if (in_b[r] && src[r] == nullptr) return PURLIN_ERR_INVALID_ARG;
-        if (out_b[r] && dst[r] == nullptr) return PURLIN_ERR_INVALID_ARG;
-        if (in_b[r] && ((uintptr_t)src[r] & 15u)) return PURLIN_ERR_ALIGNMENT;
-        if (out_b[r] && ((uintptr_t)dst[r] & 15u)) return PURLIN_ERR_ALIGNMENT;
-    }
-
-    // Outputs never overlap one another.
-    for (int a = 0; a < c.R; ++a)
-        for (int b = a + 1; b < c.R; ++b)
-            if (ranges_overlap((uintptr_t)dst[a], out_b[a], (uintptr_t)dst[b], out_b[b]))
-                return PURLIN_ERR_ALIAS;
-    // An input overlaps no output, except the in-place forms.
-    const uint64_t es64 = (uint64_t)es;
-    for (int s = 0; s < c.R; ++s) {
-        for (int d = 0; d < c.R; ++d) {
-            if (!ranges_overlap((uintptr_t)src[s], in_b[s], (uintptr_t)dst[d], out_b[d])) continue;
-            if (s == d && c.coll == PURLIN_COLL_ALL_REDUCE && src[s] == dst[d]) continue;
-            if (s == d && c.coll == PURLIN_COLL_ALL_GATHER &&
-                (uintptr_t)src[s] == (uintptr_t)dst[d] + (uint64_t)s * c.n * es64)
-                continue;
-            return PURLIN_ERR_ALIAS;
-        }
-    }
-    return PURLIN_OK;
+    return validate_extents(c, src, dst, in_b, out_b);
 }
 
 namespace {

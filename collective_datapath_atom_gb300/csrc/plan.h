@@ -134,6 +134,14 @@ int elem_bytes(int dtype);
 // overlaps between the byte ranges of the buffers.
 purlin_status validate_call(const CallDesc &c, const void *const src[], void *const dst[]);
 
+// The two halves of validate_call.  validate_shape: R, dtype, op, layout
+// pair and the array pointers.  validate_extents: pointer nulls and
+// alignment, and overlaps, for the given byte extent of each buffer.
+purlin_status validate_shape(const CallDesc &c, const void *const src[], void *const dst[]);
+purlin_status validate_extents(const CallDesc &c, const void *const src[], void *const dst[],
+                               const std::vector<uint64_t> &in_bytes,
+                               const std::vector<uint64_t> &out_bytes);
+
 // Byte lengths of each input and output buffer of a call (after validation
 // of R and counts).
 void buffer_bytes(const CallDesc &c, std::vector<uint64_t> &in_bytes,

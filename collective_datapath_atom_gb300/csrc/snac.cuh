@@ -62,6 +62,7 @@ enum ErrSite : uint64_t {
     kSiteRingEmpty = 3,
     kSiteChunkDone = 4,
     kSiteDeviceArgs = 5,   // a device-API call with arguments that do not match its descriptor
+    kSiteDeviceCounts = 6, // device-resident counts that exceed the declared capacities
 };
 
 struct Ctl {
@@ -89,7 +90,7 @@ __device__ __forceinline__ const Seg *seg_table(const P &p) {
 // before the table is read.
 template <class P>
 __device__ __forceinline__ const Seg *stage_segs(const P &p, Seg *sm, int cap) {
-    if (p.nseg > cap) return seg_table(p);
+    if (p.nseg > cap || seg_table(p) == sm) return seg_table(p);   // too large, or already there
     const uint64_t *from = reinterpret_cast<const uint64_t *>(seg_table(p));
     uint64_t *to = reinterpret_cast<uint64_t *>(sm);
     const int words = p.nseg * (int)(sizeof(Seg) / sizeof(uint64_t));

@@ -167,6 +167,41 @@ purlin_status purlin_all_to_all_v(purlin_ctx *ctx, const void *const src[], void
                                   const size_t counts[], purlin_dtype dtype, purlin_op op,
                                   purlin_layout layout);
 
+/* The three V collectives with their counts in DEVICE memory, e.g. written
+ * by an MoE router kernel earlier on the context's stream (§C.4; the paper
+ * summary notes the prefix sums are taken on the device).  No host round
+ * trip: one kernel reads the counts, derives the displacements (exclusive
+ * prefix sums, as in the host calls above), checks them and runs the
+ * collective.  counts: device array of size_t, R entries (AllGatherV,
+ * ReduceScatterV) or R*R (AllToAllV, row = source), 8-byte aligned, read
+ * by the kernel in stream order.  The buffers' extents are declared
+ * instead of derived: every src[r] holds in_capacity elements and every
+ * dst[r] out_capacity elements (pointers, alignment and overlaps are
+ * checked on the host against these extents, as for the host-count calls;
+ * no in-place form).  The kernel checks that the counts fit: each rank's
+ * input extent (AGV: counts[r]; RSV: the total; A2AV: row r's sum) at most
+ * in_capacity, each output extent (AGV: the total; RSV: counts[r]; A2AV:
+ * column r's sum) at most out_capacity, and every count below 2^40;
+ * otherwise it writes nothing and records INVALID_ARG in the context's
+ * error word (purlin_check).  The variant is decided on the device from
+ * the largest per-rank input against the crossover (PURLIN_OPT_VARIANT and
+ * PURLIN_OPT_CROSSOVER_BYTES apply).  R <= 16, else UNSUPPORTED. */
+purlin_status purlin_all_gather_v_device_counts(purlin_ctx *ctx, const void *const src[],
+                                                void *const dst[], const size_t counts[],
+                                                size_t in_capacity, size_t out_capacity,
+                                                purlin_dtype dtype, purlin_op op,
+                                                purlin_layout layout);
+purlin_status purlin_reduce_scatter_v_device_counts(purlin_ctx *ctx, const void *const src[],
+                                                    void *const dst[], const size_t counts[],
+                                                    size_t in_capacity, size_t out_capacity,
+                                                    purlin_dtype dtype, purlin_op op,
+                                                    purlin_layout layout);
+purlin_status purlin_all_to_all_v_device_counts(purlin_ctx *ctx, const void *const src[],
+                                                void *const dst[], const size_t counts[],
+                                                size_t in_capacity, size_t out_capacity,
+                                                purlin_dtype dtype, purlin_op op,
+                                                purlin_layout layout);
+
 /* AllReduce without any device allocation.  The pages have no counterpart
  * to this entry point; it is an addition of this library for callers that
  * cannot call cudaMalloc at the time they reduce: code running while a CUDA
@@ -238,7 +273,7 @@ purlin_status purlin_get_option(purlin_ctx *ctx, purlin_option opt, int64_t *val
 
 /* What the last collective call of this context enqueued. */
 typedef struct {
-    int32_t variant;      /* 0 nothing launched, 1 latency, 2 throughput, 3 throughput composed AllReduce */
+    int32_t variant;      /* 0 nothing launched, 1 latency, 2 throughput, 3 throughput composed AllReduce, 4 decided on the device (device counts) */
     int32_t grid;         /* CTAs */
     int32_t block;        /* threads per CTA */
     int32_t stages;       /* TMA ring depth (throughput) */
