@@ -570,8 +570,10 @@ def sweep(args):
         src, dst = bufs(n, n)
         algo = 2 * 8 * n * 2
         reps = 200 if n <= (1 << 20) else 30
-        for variant, mode in ((1, 0), (2, 1), (2, 2), (0, 0)):
+        for variant, mode in ((1, 0), (2, 1), (2, 2), (0, 3), (0, 0)):
             if variant == 1 and n > (16 << 20):
+                continue
+            if mode == 3 and 2 * n > (1 << 20):   # packets: up to 1 MiB per rank
                 continue
             setopt(variant, mode)
             call = lambda: P.purlin_all_reduce(ctx, src, dst, n, 1)   # noqa: E731
@@ -582,7 +584,8 @@ def sweep(args):
             warm = _events_us(torch, stream, call, reps)[0] if n <= (8 << 20) else None
             emit({"row": "ar_sweep", "batch": b, "bytes_per_rank": 2 * n,
                   "mode": {(1, 0): "latency", (2, 1): "throughput fused",
-                           (2, 2): "throughput composed", (0, 0): "auto"}[(variant, mode)],
+                           (2, 2): "throughput composed", (0, 3): "composed packets",
+                           (0, 0): "auto"}[(variant, mode)],
                   "chosen_variant": info["variant"], "us_cold": med, "p10": p10, "p90": p90,
                   "us_warm": warm, "gbs_cold": algo / (med * 1e-6) / 1e9,
                   "frac_cold": algo / (med * 1e-6) / 1e9 / peak})

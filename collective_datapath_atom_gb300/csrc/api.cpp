@@ -125,6 +125,7 @@ struct purlin_ctx {
     int sms = 0;
     int max_smem = 0;
     unsigned long long *flags = nullptr;   // 2 x kFlagSlots
+    unsigned char *packets = nullptr;      // 2 x kPacketStagingBytes (latency-path staging)
     unsigned long long *err = nullptr;
     uint64_t epoch = 1;
     int64_t opt[kNumOptions] = {};
@@ -252,10 +253,48 @@ void flag_geometry(uint64_t notify_chunks, int64_t grid, uint32_t *slots, uint64
     *epoch_inc = gens | 1ull;   // odd: the parity flips every call
 }
 
+// AllReduce mode for the ring: the packet mode (3) runs the ring's composed
+// mode where packets do not apply.
+int ring_ar_mode(const purlin_ctx *ctx) {
+    const int m = (int)ctx->opt[PURLIN_OPT_AR_MODE];
+    return m == 3 ? 2 : m;
+}
+
 Policy call_policy(const purlin_ctx *ctx, const CallDesc &c) {
-    return c.coll == PURLIN_COLL_ALL_REDUCE && ctx->opt[PURLIN_OPT_AR_MODE] == 2
+    return c.coll == PURLIN_COLL_ALL_REDUCE && ring_ar_mode(ctx) == 2
                ? composed_all_reduce_policy(c.R)
                : policy_for(c.coll, c.R);
+}
+
+purlin_status run_packets(purlin_ctx *ctx, const CallDesc &c, const void *const src[],
+                          void *const dst[], uint64_t nbytes) {
+    PktLaunch a;
+    a.src = src;
+    a.dst = dst;
+    a.staging = ctx->packets + (ctx->epoch & 1ull) * kPacketStagingBytes;
+    a.err = ctx->err;
+    a.nbytes = nbytes;
+    a.timeout_ns = ctx->opt[PURLIN_OPT_SPIN_TIMEOUT_NS] > 0 ? ctx->opt[PURLIN_OPT_SPIN_TIMEOUT_NS]
+                                                            : kDefaultTimeoutNs;
+    a.drop_unit = ctx->opt[PURLIN_OPT_DROP_NOTIFY];
+    a.flag = (uint32_t)ctx->epoch;
+    a.R = c.R;
+    a.dtype = c.dtype;
+    a.stream = ctx->stream;
+    const uint64_t units = (nbytes + 7) / 8;
+    const uint64_t per = (uint64_t)packet_threads();
+    a.G = (int)std::max<uint64_t>(1, std::min<uint64_t>((units + per - 1) / per, (uint64_t)ctx->sms));
+    if (launch_packet_all_reduce(a) != cudaSuccess) return PURLIN_ERR_CUDA;
+    purlin_launch_info info = {};
+    info.variant = 5;
+    info.grid = 2 * a.G;
+    info.block = (int32_t)per;
+    info.units = (int64_t)units;
+    info.epoch = ctx->epoch;
+    ctx->epoch += 1;   // odd: the parity (staging buffer) flips every call
+    info.epoch_next = ctx->epoch;
+    ctx->last = info;
+    return PURLIN_OK;
 }
 
 purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], void *const dst[]) {
@@ -264,9 +303,19 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
     purlin_status st = validate_call(c, src, dst);
     if (st != PURLIN_OK) return st;
 
+    // ---- composed AllReduce on the latency path: packets (§3.2, §4.1)
+    int ar_mode = (int)ctx->opt[PURLIN_OPT_AR_MODE];
+    if (c.coll == PURLIN_COLL_ALL_REDUCE && ar_mode == 3) {
+        const uint64_t nbytes = (uint64_t)c.n * (uint64_t)elem_bytes(c.dtype);
+        if (nbytes > 0 && c.R > 1 && nbytes <= kPacketPayloadBytes)
+            return run_packets(ctx, c, src, dst, nbytes);
+        ar_mode = 2;   // past the staging buffer: the ring's composed mode
+    }
+
     // ---- policy (§4.2)
-    const int ar_mode = (int)ctx->opt[PURLIN_OPT_AR_MODE];
-    const Policy shape = call_policy(ctx, c);
+    const Policy shape = ar_mode == 2 && c.coll == PURLIN_COLL_ALL_REDUCE
+                             ? composed_all_reduce_policy(c.R)
+                             : policy_for(c.coll, c.R);
     int variant = (int)ctx->opt[PURLIN_OPT_VARIANT];
     if (variant == 0) {
         const uint64_t xo = ctx->opt[PURLIN_OPT_CROSSOVER_BYTES] > 0
@@ -507,6 +556,7 @@ purlin_status purlin_init(int R, purlin_stream stream, purlin_ctx **out) {
     ctx->opt[PURLIN_OPT_AR_MODE] = env_or("PURLIN_AR_MODE", 0);
     auto fail = [&](purlin_status s) {
         if (ctx->flags) cudaFree(ctx->flags);
+        if (ctx->packets) cudaFree(ctx->packets);
         if (ctx->err) cudaFree(ctx->err);
         delete ctx;
         return s;
@@ -522,8 +572,11 @@ purlin_status purlin_init(int R, purlin_stream stream, purlin_ctx **out) {
         return fail(PURLIN_ERR_CUDA);
     if (cudaMalloc(&ctx->flags, 2 * (size_t)kFlagSlots * sizeof(unsigned long long)) !=
             cudaSuccess ||
+        cudaMalloc(&ctx->packets, 2 * kPacketStagingBytes) != cudaSuccess ||
         cudaMalloc(&ctx->err, sizeof(unsigned long long)) != cudaSuccess)
         return fail(PURLIN_ERR_OOM);
+    if (cudaMemsetAsync(ctx->packets, 0, 2 * kPacketStagingBytes, ctx->stream) != cudaSuccess)
+        return fail(PURLIN_ERR_CUDA);
     if (cudaMemsetAsync(ctx->flags, 0, 2 * (size_t)kFlagSlots * sizeof(unsigned long long),
                         ctx->stream) != cudaSuccess ||
         cudaMemsetAsync(ctx->err, 0, sizeof(unsigned long long), ctx->stream) != cudaSuccess)
@@ -540,6 +593,7 @@ purlin_status purlin_finalize(purlin_ctx *ctx) {
     for (CacheEntry &e : ctx->lru) drop_entry(e);
     for (DeviceCollMem &m : ctx->device_colls) free_device_coll(m);
     if (ctx->flags) cudaFree(ctx->flags);
+    if (ctx->packets) cudaFree(ctx->packets);
     if (ctx->err) cudaFree(ctx->err);
     delete ctx;
     return st;
@@ -669,7 +723,7 @@ purlin_status purlin_set_option(purlin_ctx *ctx, purlin_option opt, int64_t valu
             if (value < 0 || value > 2) return PURLIN_ERR_INVALID_ARG;
             break;
         case PURLIN_OPT_AR_MODE:
-            if (value < 0 || value > 2) return PURLIN_ERR_INVALID_ARG;
+            if (value < 0 || value > 3) return PURLIN_ERR_INVALID_ARG;
             break;
         case PURLIN_OPT_CHUNK_BYTES:
             if (value < 0 || (value > 0 && (value < 16 || value % 16 != 0 || value > (1 << 20))))
@@ -780,8 +834,8 @@ purlin_status purlin_device_prepare(purlin_ctx *ctx, purlin_collective coll,
     Plan pl;
     RingShape rs;
     for (;;) {   // halve the chunk until the ring fits the cap
-        st = compile_plan(c, kVariantThroughput, (int)ctx->opt[PURLIN_OPT_AR_MODE],
-                          chunk * (uint32_t)c.R, chunk, &pl);
+        st = compile_plan(c, kVariantThroughput, ring_ar_mode(ctx), chunk * (uint32_t)c.R, chunk,
+                          &pl);
         if (st != PURLIN_OK) return st;
         st = ring_shape(ctx, c, shape, pl, limit - ctl_bytes, &rs);
         if (st == PURLIN_OK) break;

@@ -153,6 +153,33 @@ __device__ __forceinline__ unsigned long long flag_acquire(const unsigned long l
     return v;
 }
 
+// ------------------------------------------------------------- packets --
+//
+// The latency path's payload+notification packet (paper summary §3.2): 16
+// bytes holding 8 payload bytes and the call's 32-bit flag twice, as two
+// 8-byte lines {payload word, flag}.  The store is one v2.u64 access whose
+// two 64-bit elements are each single-copy atomic (aligned 64-bit accesses),
+// so a reader that sees a line's flag sees that line's payload: no fence
+// and no separate flag store.  Half of every packet is flag, which doubles
+// the bytes moved, as the pages say of their packets.
+
+__device__ __forceinline__ void packet_store(void *p, uint64_t payload, uint32_t flag) {
+    const uint64_t a = (payload & 0xFFFFFFFFull) | ((uint64_t)flag << 32);
+    const uint64_t b = (payload >> 32) | ((uint64_t)flag << 32);
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b)
+                 : "memory");
+}
+
+// True, with the payload, once both lines of the packet carry `flag`.
+__device__ __forceinline__ bool packet_load(const void *p, uint32_t flag, uint64_t *payload) {
+    uint64_t a, b;
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p)
+                 : "memory");
+    if ((uint32_t)(a >> 32) != flag || (uint32_t)(b >> 32) != flag) return false;
+    *payload = (a & 0xFFFFFFFFull) | (b << 32);
+    return true;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

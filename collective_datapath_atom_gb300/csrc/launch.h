@@ -67,6 +67,28 @@ cudaError_t launch_vcounts(const VcLaunch &a);
 cudaError_t configure_vcounts(int max_dyn_smem);
 cudaError_t vcounts_occupancy(int dtype, int R, int block, size_t smem, int *per_sm);
 
+// Composed AllReduce on the latency path (packets.cu).
+constexpr uint64_t kPacketStagingBytes = 2ull << 20;   // per parity: 16-byte packets
+constexpr uint64_t kPacketPayloadBytes = kPacketStagingBytes / 2;   // 8 payload bytes per packet
+
+struct PktLaunch {
+    const void *const *src = nullptr;
+    void *const *dst = nullptr;
+    unsigned char *staging = nullptr;   // this call's parity
+    unsigned long long *err = nullptr;
+    uint64_t nbytes = 0;
+    int64_t timeout_ns = 0;
+    int64_t drop_unit = -1;
+    uint32_t flag = 0;
+    int R = 0;
+    int dtype = 0;
+    int G = 0;                          // reducing CTAs; as many gather
+    cudaStream_t stream = nullptr;
+};
+
+int packet_threads();
+cudaError_t launch_packet_all_reduce(const PktLaunch &a);
+
 // Which parameter block a call needs (0 small, 1 big), -1 if the plan must
 // live in device memory (more segments than the big block holds).
 int param_class(int R, size_t nseg);

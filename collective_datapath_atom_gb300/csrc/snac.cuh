@@ -63,6 +63,7 @@ enum ErrSite : uint64_t {
     kSiteChunkDone = 4,
     kSiteDeviceArgs = 5,   // a device-API call with arguments that do not match its descriptor
     kSiteDeviceCounts = 6, // device-resident counts that exceed the declared capacities
+    kSitePacketWait = 7,   // a latency-path packet that never arrived
 };
 
 struct Ctl {

@@ -93,9 +93,11 @@ typedef enum {
 /* Create a context for R rank buffers whose work is enqueued on `stream`
  * (the pages' `initialize(rank, world, stream, memory)`, project README,
  * "Host-side", reshaped for one process holding all R ranks).  Allocates the
- * device flag array (2 parities x 65536 u64, zeroed once here) and a device
- * error word on the current CUDA device, and reads the device's SM count
- * and shared-memory limit.  The epoch (paper summary §4.3) starts at 1.
+ * device flag array (2 parities x 65536 u64, zeroed once here), the
+ * latency path's packet staging (2 parities x 2 MiB, zeroed once here;
+ * paper summary §4.1) and a device error word on the current CUDA device,
+ * and reads the device's SM count and shared-memory limit.  The epoch
+ * (paper summary §4.3) starts at 1.
  * Errors: INVALID_ARG (R out of range, out == NULL), CUDA, OOM. */
 purlin_status purlin_init(int R, purlin_stream stream, purlin_ctx **out);
 
@@ -255,7 +257,9 @@ const char *purlin_status_string(purlin_status status);
 typedef enum {
     PURLIN_OPT_VARIANT = 0,          /* 0 auto, 1 latency (vector ld/st), 2 throughput (TMA ring) */
     PURLIN_OPT_CROSSOVER_BYTES = 1,  /* per-rank message bytes at or below which auto picks latency */
-    PURLIN_OPT_AR_MODE = 2,          /* AllReduce: 0 auto, 1 fused, 2 composed (RS CTAs notify, AG CTAs consume) */
+    PURLIN_OPT_AR_MODE = 2,          /* AllReduce: 0 auto, 1 fused, 2 composed (RS CTAs notify, AG CTAs consume),
+                                        3 composed on the latency path: 16-byte payload+flag packets
+                                        (messages up to 1 MiB per rank; larger ones run mode 2) */
     PURLIN_OPT_CHUNK_BYTES = 3,      /* bytes per source per chunk in the TMA ring */
     PURLIN_OPT_STAGES = 4,           /* TMA ring depth */
     PURLIN_OPT_CTAS = 5,             /* CTAs of a throughput launch */
@@ -273,7 +277,7 @@ purlin_status purlin_get_option(purlin_ctx *ctx, purlin_option opt, int64_t *val
 
 /* What the last collective call of this context enqueued. */
 typedef struct {
-    int32_t variant;      /* 0 nothing launched, 1 latency, 2 throughput, 3 throughput composed AllReduce, 4 decided on the device (device counts) */
+    int32_t variant;      /* 0 nothing launched, 1 latency, 2 throughput, 3 throughput composed AllReduce, 4 decided on the device (device counts), 5 composed AllReduce with packets */
     int32_t grid;         /* CTAs */
     int32_t block;        /* threads per CTA */
     int32_t stages;       /* TMA ring depth (throughput) */
