@@ -419,17 +419,30 @@ def run_gpu(args, rank, world, local_rank):
                 for ho, dd in zip(h_out, dst):
                     ho.copy_(dd, non_blocking=True)
         stream.synchronize()
+        # Steps are pipelined across the two directions of the host link:
+        # step i+1's inputs go up (second stream) while step i's outputs come
+        # down.  Every step still copies its own inputs in and its outputs
+        # out; the upload of step i+1 only waits for step i's call to finish
+        # reading the inputs, and step i+1's call waits for its upload.
+        up = torch.cuda.Stream(stream.device)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for i in range(e2e_steps):
+        read_done = [torch.cuda.Event() for _ in range(e2e_steps)]
+        uploaded = [torch.cuda.Event() for _ in range(e2e_steps)]
+        e0.record(stream)
+        for i in range(e2e_steps):
+            up.wait_event(e0 if i == 0 else read_done[i - 1])
+            with torch.cuda.stream(up):
                 for hs, ds in zip(h_in, src):
                     ds.copy_(hs, non_blocking=True)
+            uploaded[i].record(up)
+            stream.wait_event(uploaded[i])
+            with torch.cuda.stream(stream):
                 run(src, dst)
+                read_done[i].record(stream)
                 for ho, dd in zip(h_out, dst):
                     ho.copy_(dd, non_blocking=True)
-            e1.record(stream)
+        e1.record(stream)
         stream.synchronize()
         e2e_ms = e0.elapsed_time(e1) / e2e_steps
         e2e = {"value": world * algo_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
