@@ -40,6 +40,10 @@ sys.path.insert(0, ROOT)
 import workloads  # noqa: E402
 
 L2_FLUSH_BYTES = 512 << 20
+# purlin_launch_info.variant -> the kernel that ran
+KERNEL_OF_VARIANT = {1: "purlin_latency_kernel", 2: "purlin_throughput_kernel",
+                     3: "purlin_throughput_kernel", 4: "purlin_vcounts_kernel",
+                     5: "purlin_packet_ar_kernel"}
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = ["collective_datapath_atom_gb300/csrc/kernels.cu",
                   "collective_datapath_atom_gb300/csrc/snac.cuh",
@@ -144,7 +148,8 @@ class ClockSampler:
 def setup_workload(name: str, device, elements: int = 0):
     """Device inputs/outputs and a closure that runs one call.  `elements`
     (if set) replaces the elements per rank of the AllGather, ReduceScatter
-    or AllReduce workload: a smaller case of the same kernel for profiling."""
+    or AllReduce workload, or the tokens per rank of the MoE dispatch: a
+    smaller case of the same kernel for profiling."""
     import dataclasses
 
     import torch
@@ -166,7 +171,11 @@ def setup_workload(name: str, device, elements: int = 0):
         call = ("reduce_scatter", w.n)
     elif name == workloads.A2AV_BF16_R8_MOE.name:
         w = workloads.A2AV_BF16_R8_MOE
-        C, ins = workloads.moe_dispatch()
+        tokens = elements or workloads.MOE_TOKENS   # `elements`: tokens per rank here
+        if elements:
+            w = dataclasses.replace(w, n=tokens * workloads.MOE_HIDDEN,
+                                    name=f"alltoallv_bf16_R8_{tokens}tok_x7168_zipf1.2")
+        C, ins = workloads.moe_dispatch(tokens=tokens)
         counts = (C * workloads.MOE_HIDDEN).reshape(-1)
         out_elems = [int(counts.reshape(8, 8)[:, d].sum()) for d in range(8)]
         call = ("all_to_all_v", counts.tolist())
@@ -368,6 +377,19 @@ def run_gpu(args, rank, world, local_rank):
     w, ins, src, dst, call, algo_bytes, in_bytes, out_bytes = setup_workload(
         args.workload, device, args.elements)
     run = make_runner(P, ctx, w, call)
+    if args.device_counts:
+        # the count matrix stays on the GPU: the device-count entry point,
+        # with every output sized for the largest column
+        if w.collective != "all_to_all_v":
+            raise SystemExit("--device-counts applies to the AllToAllV workload")
+        Cm = np.asarray(call[1]).reshape(w.R, w.R)
+        in_cap, out_cap = int(Cm.sum(1).max()), int(Cm.sum(0).max())
+        dst = [torch.empty(out_cap, dtype=d.dtype, device=device) for d in dst]
+        d_counts = torch.tensor(call[1], dtype=torch.int64, device=device)
+
+        def run(src_, dst_):
+            P.purlin_all_to_all_v_device_counts(ctx, src_, dst_, d_counts, in_cap, out_cap,
+                                                w.dtype)
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     torch.cuda.synchronize()   # inputs were uploaded on another stream
 
@@ -468,11 +490,12 @@ def run_gpu(args, rank, world, local_rank):
                    "algorithmic_bytes_per_step": algo_bytes, "l2": "flushed between steps",
                    "variant": info["variant"], "grid": info["grid"], "block": info["block"],
                    "stages": info["stages"], "chunk_bytes": info["chunk_bytes"],
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   **({"counts": "device"} if args.device_counts else {})},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
-                     "kernel": "purlin_throughput_kernel"},
+                     "kernel": KERNEL_OF_VARIANT.get(info["variant"], "none")},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps,
@@ -736,6 +759,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--device-counts", action="store_true",
+                    help="AllToAllV workload: counts in device memory (the device-count call)")
     ap.add_argument("--elements", type=int, default=0,
                     help="elements per rank (a smaller case of the same kernel)")
     ap.add_argument("--sweep", action="store_true",
