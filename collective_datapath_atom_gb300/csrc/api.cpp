@@ -173,10 +173,13 @@ purlin_status get_plan(purlin_ctx *ctx, const CallDesc &c, int variant, int ar_m
     e.key = key;
     purlin_status st = compile_plan(c, variant, ar_mode, red_slot, copy_chunk, &e.plan);
     if (st != PURLIN_OK) return st;
-    if (param_class(c.R, e.plan.segs.size()) < 0) {
-        // Too many segments for the kernel parameter block: keep them in
-        // device memory.  Uploaded from pageable memory, which the runtime
-        // copies before returning.
+    if (param_class(c.R, e.plan.segs.size()) != kClassSmall) {
+        // More segments than the small parameter block holds: the table
+        // lives in device memory (uploaded once per cached plan) and the
+        // kernels stage it into shared memory with coalesced loads.  A large
+        // inline table would be read with divergent constant-cache accesses
+        // and would lengthen every launch.  Uploaded from pageable memory,
+        // which the runtime copies before returning.
         size_t bytes = e.plan.segs.size() * sizeof(Seg);
         if (cudaMalloc(&e.segs_dev, bytes) != cudaSuccess) return PURLIN_ERR_OOM;
         if (cudaMemcpyAsync(e.segs_dev, e.plan.segs.data(), bytes, cudaMemcpyHostToDevice,
@@ -389,7 +392,7 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
         const uint32_t stages = rs.stages, slot_stride = rs.slot_stride, smem = rs.smem;
         const bool vector_copies = rs.vector_copies;
         const int block = 32 * (2 + rs.consumer_warps);
-        const int pclass = e->segs_dev ? 1 : param_class(c.R, pl.segs.size());
+        const int pclass = launch_class(c.R, pl.segs.size(), e->segs_dev != nullptr);
         int per_sm = 0;
         if (throughput_occupancy(c.dtype, pclass, block, smem, &per_sm) != cudaSuccess ||
             per_sm < 1)

@@ -53,8 +53,10 @@ struct KParams {
 template <int DT, int MAXR, int MAXSEG>
 __global__ void __launch_bounds__(256, 2) purlin_latency_kernel(
     const __grid_constant__ KParams<MAXR, MAXSEG> p) {
-    __shared__ Seg s_segs[MAXSEG];
-    const Seg *segs = stage_segs(p, s_segs, MAXSEG);
+    // an inline table of MAXSEG segments, or up to kSmemSegs of a device table
+    constexpr int kStage = MAXSEG > 1 ? MAXSEG : kSmemSegs;
+    __shared__ Seg s_segs[kStage];
+    const Seg *segs = stage_segs(p, s_segs, kStage);
     __syncthreads();
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
     units_loop<DT, MAXR>(p, segs, (uint64_t)blockIdx.x * blockDim.x + threadIdx.x, stride);
@@ -137,61 +139,95 @@ cudaError_t launch_empty(cudaStream_t stream) {
 }
 
 int param_class(int R, size_t nseg) {
-    if (R <= kSmallMaxR && nseg <= (size_t)kSmallMaxSeg) return 0;
-    if (nseg <= (size_t)kBigMaxSeg) return 1;
+    if (R <= kSmallMaxR && nseg <= (size_t)kSmallMaxSeg) return kClassSmall;
+    if (nseg <= (size_t)kBigMaxSeg) return kClassBig;
     return -1;
+}
+
+int launch_class(int R, size_t nseg, bool device_table) {
+    if (device_table) return R <= kSmallMaxR ? kClassDev8 : kClassDev64;
+    return param_class(R, nseg);
 }
 
 uint32_t throughput_smem(uint32_t stages, uint32_t slot_stride) {
     return ring_workspace_bytes(stages, slot_stride);
 }
 
-cudaError_t launch_latency(const LaunchArgs &a) {
-    const int pc = a.segs_dev ? 1 : param_class(a.R, a.plan->segs.size());
-    if (a.dtype == PURLIN_F32)
-        return pc == 0 ? launch_lat_t<PURLIN_F32, kSmallMaxR, kSmallMaxSeg>(a)
-                       : launch_lat_t<PURLIN_F32, kBigMaxR, kBigMaxSeg>(a);
-    return pc == 0 ? launch_lat_t<PURLIN_BF16, kSmallMaxR, kSmallMaxSeg>(a)
-                   : launch_lat_t<PURLIN_BF16, kBigMaxR, kBigMaxSeg>(a);
+namespace {
+
+// Calls f.template run<DT, MAXR, MAXSEG>() for a launch class and dtype.
+template <class F>
+cudaError_t by_class(int pc, int dtype, F &&f) {
+    const bool f32 = dtype == PURLIN_F32;
+    switch (pc) {
+        case kClassSmall:
+            return f32 ? f.template run<PURLIN_F32, kSmallMaxR, kSmallMaxSeg>()
+                       : f.template run<PURLIN_BF16, kSmallMaxR, kSmallMaxSeg>();
+        case kClassBig:
+            return f32 ? f.template run<PURLIN_F32, kBigMaxR, kBigMaxSeg>()
+                       : f.template run<PURLIN_BF16, kBigMaxR, kBigMaxSeg>();
+        case kClassDev8:
+            return f32 ? f.template run<PURLIN_F32, kSmallMaxR, 1>()
+                       : f.template run<PURLIN_BF16, kSmallMaxR, 1>();
+        case kClassDev64:
+            return f32 ? f.template run<PURLIN_F32, kBigMaxR, 1>()
+                       : f.template run<PURLIN_BF16, kBigMaxR, 1>();
+    }
+    return cudaErrorInvalidValue;
 }
 
+struct LatLaunch {
+    const LaunchArgs &a;
+    template <int DT, int MR, int MS>
+    cudaError_t run() { return launch_lat_t<DT, MR, MS>(a); }
+};
+struct TputLaunch {
+    const LaunchArgs &a;
+    template <int DT, int MR, int MS>
+    cudaError_t run() { return launch_tput_t<DT, MR, MS>(a); }
+};
+struct TputConfigure {
+    int max_dyn_smem;
+    template <int DT, int MR, int MS>
+    cudaError_t run() {
+        return cudaFuncSetAttribute(purlin_throughput_kernel<DT, MR, MS>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn_smem);
+    }
+};
+struct TputOccupancy {
+    int block;
+    size_t smem;
+    int *per_sm;
+    template <int DT, int MR, int MS>
+    cudaError_t run() {
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            per_sm, purlin_throughput_kernel<DT, MR, MS>, block, smem);
+    }
+};
+
+int class_of(const LaunchArgs &a) {
+    return launch_class(a.R, a.plan->segs.size(), a.segs_dev != nullptr);
+}
+
+}  // namespace
+
+cudaError_t launch_latency(const LaunchArgs &a) { return by_class(class_of(a), a.dtype, LatLaunch{a}); }
+
 cudaError_t launch_throughput(const LaunchArgs &a) {
-    const int pc = a.segs_dev ? 1 : param_class(a.R, a.plan->segs.size());
-    if (a.dtype == PURLIN_F32)
-        return pc == 0 ? launch_tput_t<PURLIN_F32, kSmallMaxR, kSmallMaxSeg>(a)
-                       : launch_tput_t<PURLIN_F32, kBigMaxR, kBigMaxSeg>(a);
-    return pc == 0 ? launch_tput_t<PURLIN_BF16, kSmallMaxR, kSmallMaxSeg>(a)
-                   : launch_tput_t<PURLIN_BF16, kBigMaxR, kBigMaxSeg>(a);
+    return by_class(class_of(a), a.dtype, TputLaunch{a});
 }
 
 cudaError_t configure_kernels(int max_dyn_smem) {
-    cudaError_t e;
-#define PURLIN_SET(DT, MR, MS)                                                                \
-    e = cudaFuncSetAttribute(purlin_throughput_kernel<DT, MR, MS>,                           \
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn_smem);     \
-    if (e != cudaSuccess) return e;
-    PURLIN_SET(PURLIN_F32, kSmallMaxR, kSmallMaxSeg)
-    PURLIN_SET(PURLIN_F32, kBigMaxR, kBigMaxSeg)
-    PURLIN_SET(PURLIN_BF16, kSmallMaxR, kSmallMaxSeg)
-    PURLIN_SET(PURLIN_BF16, kBigMaxR, kBigMaxSeg)
-#undef PURLIN_SET
+    for (int pc : {kClassSmall, kClassBig, kClassDev8, kClassDev64})
+        for (int dt : {PURLIN_F32, PURLIN_BF16}) {
+            const cudaError_t e = by_class(pc, dt, TputConfigure{max_dyn_smem});
+            if (e != cudaSuccess) return e;
+        }
     return cudaSuccess;
 }
 
 cudaError_t throughput_occupancy(int dtype, int pclass, int block, size_t smem, int *per_sm) {
-    if (dtype == PURLIN_F32)
-        return pclass == 0 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                                 per_sm, purlin_throughput_kernel<PURLIN_F32, kSmallMaxR, kSmallMaxSeg>,
-                                 block, smem)
-                           : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                                 per_sm, purlin_throughput_kernel<PURLIN_F32, kBigMaxR, kBigMaxSeg>,
-                                 block, smem);
-    return pclass == 0 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                             per_sm, purlin_throughput_kernel<PURLIN_BF16, kSmallMaxR, kSmallMaxSeg>,
-                             block, smem)
-                       : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                             per_sm, purlin_throughput_kernel<PURLIN_BF16, kBigMaxR, kBigMaxSeg>,
-                             block, smem);
+    return by_class(pclass, dtype, TputOccupancy{block, smem, per_sm});
 }
 
 }  // namespace purlin

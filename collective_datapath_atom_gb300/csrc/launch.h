@@ -89,9 +89,21 @@ struct PktLaunch {
 int packet_threads();
 cudaError_t launch_packet_all_reduce(const PktLaunch &a);
 
-// Which parameter block a call needs (0 small, 1 big), -1 if the plan must
-// live in device memory (more segments than the big block holds).
+// Kernel parameter blocks ("launch classes"): the segment table inline in
+// the parameters (small: R <= 8 and up to 16 segments; big: up to 64), or in
+// device memory with only the rank pointers inline (R <= 8, or up to 64).
+enum LaunchClass : int {
+    kClassSmall = 0,
+    kClassBig = 1,
+    kClassDev8 = 2,
+    kClassDev64 = 3,
+};
+
+// The inline class a plan fits (small or big), -1 if none.
 int param_class(int R, size_t nseg);
+
+// The class a launch uses: a device table's class, else param_class.
+int launch_class(int R, size_t nseg, bool device_table);
 
 cudaError_t launch_latency(const LaunchArgs &a);
 cudaError_t launch_empty(cudaStream_t stream);
