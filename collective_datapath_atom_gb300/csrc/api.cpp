@@ -126,8 +126,10 @@ struct purlin_ctx {
     int max_smem = 0;
     unsigned long long *flags = nullptr;   // 2 x kFlagSlots
     unsigned char *packets = nullptr;      // 2 x kPacketStagingBytes (latency-path staging)
-    unsigned long long *err = nullptr;
-    uint64_t epoch = 1;
+    unsigned long long *err = nullptr;     // 4 words: error word, pad, device epoch {epoch, done}
+    unsigned long long *dev_epoch = nullptr;   // err + 2
+    uint64_t epoch = 1;   // host count of the increments calls applied (reported in
+                          // purlin_launch_info); the device epoch is the one kernels use
     int64_t opt[kNumOptions] = {};
     purlin_launch_info last = {};
     std::list<CacheEntry> lru;
@@ -274,13 +276,13 @@ purlin_status run_packets(purlin_ctx *ctx, const CallDesc &c, const void *const 
     PktLaunch a;
     a.src = src;
     a.dst = dst;
-    a.staging = ctx->packets + (ctx->epoch & 1ull) * kPacketStagingBytes;
+    a.staging = ctx->packets;
+    a.dev_epoch = ctx->dev_epoch;
     a.err = ctx->err;
     a.nbytes = nbytes;
     a.timeout_ns = ctx->opt[PURLIN_OPT_SPIN_TIMEOUT_NS] > 0 ? ctx->opt[PURLIN_OPT_SPIN_TIMEOUT_NS]
                                                             : kDefaultTimeoutNs;
     a.drop_unit = ctx->opt[PURLIN_OPT_DROP_NOTIFY];
-    a.flag = (uint32_t)ctx->epoch;
     a.R = c.R;
     a.dtype = c.dtype;
     a.stream = ctx->stream;
@@ -369,8 +371,7 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
                                                             : kDefaultTimeoutNs;
     a.drop_notify = ctx->opt[PURLIN_OPT_DROP_NOTIFY];
     a.stream = ctx->stream;
-    a.epoch = ctx->epoch;
-    a.flags = ctx->flags + (ctx->epoch & 1ull) * kFlagSlots;   // parity selects the set
+    a.flags = ctx->flags;   // both parities; the device epoch selects one
 
     uint64_t epoch_inc = 1;
     cudaError_t ce;
@@ -412,6 +413,8 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
             // flag slot reuse stays on one CTA (slots a multiple of the grid),
             // so a later generation of a slot implies the earlier one landed.
             flag_geometry(pl.notify_chunks, grid, &a.flag_slots, &epoch_inc);
+            a.dev_epoch = ctx->dev_epoch;
+            a.epoch_inc = epoch_inc;
         }
         info.variant = pl.composed ? 3 : kVariantThroughput;
         info.stages = (int32_t)stages;
@@ -576,13 +579,20 @@ purlin_status purlin_init(int R, purlin_stream stream, purlin_ctx **out) {
     if (cudaMalloc(&ctx->flags, 2 * (size_t)kFlagSlots * sizeof(unsigned long long)) !=
             cudaSuccess ||
         cudaMalloc(&ctx->packets, 2 * kPacketStagingBytes) != cudaSuccess ||
-        cudaMalloc(&ctx->err, sizeof(unsigned long long)) != cudaSuccess)
+        cudaMalloc(&ctx->err, 4 * sizeof(unsigned long long)) != cudaSuccess)
         return fail(PURLIN_ERR_OOM);
+    ctx->dev_epoch = ctx->err + 2;
     if (cudaMemsetAsync(ctx->packets, 0, 2 * kPacketStagingBytes, ctx->stream) != cudaSuccess)
         return fail(PURLIN_ERR_CUDA);
     if (cudaMemsetAsync(ctx->flags, 0, 2 * (size_t)kFlagSlots * sizeof(unsigned long long),
                         ctx->stream) != cudaSuccess ||
-        cudaMemsetAsync(ctx->err, 0, sizeof(unsigned long long), ctx->stream) != cudaSuccess)
+        cudaMemsetAsync(ctx->err, 0, 4 * sizeof(unsigned long long), ctx->stream) != cudaSuccess)
+        return fail(PURLIN_ERR_CUDA);
+    // the device epoch starts at 1 (flags start at 0, below any epoch)
+    static const unsigned long long kFirstEpoch = 1;
+    if (cudaMemcpyAsync(ctx->dev_epoch, &kFirstEpoch, sizeof kFirstEpoch, cudaMemcpyHostToDevice,
+                        ctx->stream) != cudaSuccess ||
+        cudaStreamSynchronize(ctx->stream) != cudaSuccess)
         return fail(PURLIN_ERR_CUDA);
     ctx->epoch = 1;
     *out = ctx;

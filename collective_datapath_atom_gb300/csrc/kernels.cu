@@ -31,11 +31,12 @@ struct KParams {
     void *dst[MAXR];
     Seg segs[MAXSEG];
     const Seg *segs_dev;
-    unsigned long long *flags;
+    unsigned long long *flags;   // both parities' flag sets (flag_slots each), or null
     unsigned long long *err;
+    DevEpoch *dev_epoch;         // the device epoch, when chunks notify one another
+    uint64_t epoch_inc;          // odd: added to the device epoch by the launch
     uint64_t nchunks;
     uint64_t nunits;
-    uint64_t epoch;
     int64_t timeout_ns;
     int64_t drop_notify;
     uint32_t flag_slots;
@@ -69,7 +70,17 @@ __global__ void __launch_bounds__(kTputMaxThreads, 1) purlin_throughput_kernel(
     const __grid_constant__ KParams<MAXR, MAXSEG> p) {
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ Ctl ctl;
-    run_ring<DT, MAXR>(p, smem, &ctl, blockIdx.x, gridDim.x);
+    if (p.dev_epoch == nullptr) {
+        run_ring<DT, MAXR>(p, smem, &ctl, blockIdx.x, gridDim.x, nullptr, 0);
+        return;
+    }
+    // chunks notify one another: the launch's epoch comes from device memory
+    epoch_enter(p.dev_epoch, &ctl);
+    __syncthreads();
+    const uint64_t epoch = ctl.epoch;
+    run_ring<DT, MAXR>(p, smem, &ctl, blockIdx.x, gridDim.x,
+                       p.flags + (epoch & 1ull) * p.flag_slots, epoch);
+    epoch_leave(p.dev_epoch, p.epoch_inc, gridDim.x);   // run_ring ended with a CTA barrier
 }
 
 template <int MAXR, int MAXSEG>
@@ -83,10 +94,11 @@ void fill_params(KParams<MAXR, MAXSEG> &p, const LaunchArgs &a) {
     for (size_t i = 0; i < (size_t)MAXSEG; ++i) p.segs[i] = i < nseg && !a.segs_dev ? pl.segs[i] : Seg{};
     p.segs_dev = a.segs_dev;
     p.flags = a.flags;
+    p.dev_epoch = reinterpret_cast<DevEpoch *>(a.dev_epoch);
+    p.epoch_inc = a.epoch_inc;
     p.err = a.err;
     p.nchunks = pl.nchunks;
     p.nunits = pl.nunits;
-    p.epoch = a.epoch;
     p.timeout_ns = a.timeout_ns;
     p.drop_notify = a.drop_notify;
     p.flag_slots = a.flag_slots;

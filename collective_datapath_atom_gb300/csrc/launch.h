@@ -20,9 +20,10 @@ struct LaunchArgs {
     void *const *dst = nullptr;
     int R = 0;
     int dtype = 0;
-    uint64_t epoch = 0;
-    unsigned long long *flags = nullptr;   // the parity set of this launch
+    unsigned long long *flags = nullptr;   // both parity sets, flag_slots each (composed)
     uint32_t flag_slots = kFlagSlots;
+    unsigned long long *dev_epoch = nullptr;   // {epoch, done} in device memory (composed)
+    uint64_t epoch_inc = 1;                    // odd
     unsigned long long *err = nullptr;
     int64_t timeout_ns = 0;
     int64_t drop_notify = -1;
@@ -74,12 +75,12 @@ constexpr uint64_t kPacketPayloadBytes = kPacketStagingBytes / 2;   // 8 payload
 struct PktLaunch {
     const void *const *src = nullptr;
     void *const *dst = nullptr;
-    unsigned char *staging = nullptr;   // this call's parity
+    unsigned char *staging = nullptr;   // both parities, kPacketStagingBytes each
+    unsigned long long *dev_epoch = nullptr;   // {epoch, done}: selects the parity, gives the flag
     unsigned long long *err = nullptr;
     uint64_t nbytes = 0;
     int64_t timeout_ns = 0;
     int64_t drop_unit = -1;
-    uint32_t flag = 0;
     int R = 0;
     int dtype = 0;
     int G = 0;                          // reducing CTAs; as many gather

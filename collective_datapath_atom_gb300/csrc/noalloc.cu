@@ -15,8 +15,10 @@
 //
 // The scratch array:
 //   g_noalloc_scratch holds 2 x kStaticFlagSlots u64 flags (one set per
-//   epoch parity) and one u64 error word: 128 KiB + 8 bytes, kept by every
-//   GPU that loads the library until the process exits.  The largest call
+//   epoch parity), one u64 error word and the device epoch (epoch and a
+//   completion count): 128 KiB + 32 bytes, kept by every GPU that loads the
+//   library until the process exits.  The epoch lives on the device, so a
+//   call captured into a CUDA graph gets a new epoch at every replay.  The largest call
 //   therefore has at most kStaticFlagSlots reduce chunks of 96 KiB / R bytes
 //   per source (rounded down to 16): n * element_size <= 8192 * (98304 / R)
 //   bytes per rank (96 MiB per rank at R = 8).  Larger calls return
@@ -58,19 +60,20 @@ constexpr int kConsumerWarps = 12;
 
 }  // namespace
 
-// flags parity 0 | flags parity 1 | error word
-static __device__ __align__(256) unsigned long long g_noalloc_scratch[2 * 8192 + 1];
+// flags parity 0 | flags parity 1 | error word | pad | device epoch {epoch, done}
+static __device__ __align__(256) unsigned long long g_noalloc_scratch[2 * 8192 + 4];
 
 namespace {
 
-static_assert(sizeof(g_noalloc_scratch) == (2 * kStaticFlagSlots + 1) * 8, "scratch layout");
+static_assert(sizeof(g_noalloc_scratch) == (2 * kStaticFlagSlots + 4) * 8, "scratch layout");
+constexpr size_t kErrWord = 2 * kStaticFlagSlots;
+constexpr size_t kEpochWords = 2 * kStaticFlagSlots + 2;   // 16-byte aligned
 
 struct DeviceState {
     bool ready = false;
     unsigned long long *scratch = nullptr;   // device address of g_noalloc_scratch
     int sms = 0;
     int max_smem = 0;
-    uint64_t epoch = 1;
 };
 
 std::mutex g_mu;
@@ -87,7 +90,10 @@ purlin_status setup_device(int dev, DeviceState &st) {
     if (configure_kernels(st.max_smem - 1024) != cudaSuccess) return PURLIN_ERR_CUDA;
     if (cudaMemset(p, 0, sizeof(g_noalloc_scratch)) != cudaSuccess) return PURLIN_ERR_CUDA;
     st.scratch = static_cast<unsigned long long *>(p);
-    st.epoch = 1;
+    static const unsigned long long kFirstEpoch = 1;   // flags start at 0, below any epoch
+    if (cudaMemcpy(st.scratch + kEpochWords, &kFirstEpoch, sizeof kFirstEpoch,
+                   cudaMemcpyHostToDevice) != cudaSuccess)
+        return PURLIN_ERR_CUDA;
     st.ready = true;
     return PURLIN_OK;
 }
@@ -128,7 +134,7 @@ extern "C" purlin_status purlin_all_reduce_noalloc(int R, const void *const src[
         if (st != PURLIN_OK) return st;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    unsigned long long *err = ds.scratch + 2 * kStaticFlagSlots;
+    unsigned long long *err = ds.scratch + kErrWord;
     if (cudaMemsetAsync(err, 0, sizeof(unsigned long long), s) != cudaSuccess)
         return PURLIN_ERR_CUDA;
 
@@ -155,9 +161,10 @@ extern "C" purlin_status purlin_all_reduce_noalloc(int R, const void *const src[
     a.dst = dst;
     a.R = R;
     a.dtype = dtype;
-    a.epoch = ds.epoch;
-    a.flags = ds.scratch + (ds.epoch & 1ull) * kStaticFlagSlots;
+    a.flags = ds.scratch;              // both parities; the device epoch selects one
     a.flag_slots = kStaticFlagSlots;   // one flag per chunk: no slot is reused within a call
+    a.dev_epoch = ds.scratch + kEpochWords;
+    a.epoch_inc = 1;                   // odd: the parity flips every call
     a.err = err;
     a.timeout_ns = kTimeoutNs;
     a.drop_notify = -1;
@@ -169,6 +176,5 @@ extern "C" purlin_status purlin_all_reduce_noalloc(int R, const void *const src[
     a.cooperative = pl.composed;
     a.stream = s;
     if (launch_throughput(a) != cudaSuccess) return PURLIN_ERR_CUDA;
-    ds.epoch += 1;   // odd increment: the parity flips every call
     return PURLIN_OK;
 }

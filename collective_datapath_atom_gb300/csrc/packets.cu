@@ -37,13 +37,13 @@ template <int MAXR>
 struct PktParams {
     const void *src[MAXR];
     void *dst[MAXR];
-    unsigned char *staging;   // this call's parity: 16 bytes per unit
+    unsigned char *staging;   // both parities, kPacketStagingBytes each: 16 bytes per unit
+    DevEpoch *dev_epoch;      // the launch's epoch: parity and flag
     unsigned long long *err;
     uint64_t nbytes;          // bytes per rank buffer
     uint64_t units;           // ceil(nbytes / 8)
     int64_t timeout_ns;
     int64_t drop_unit;        // fault injection: a unit whose packet is never stored, or -1
-    uint32_t flag;
     int32_t R;
     int32_t G;                // reducing CTAs (as many gather)
 };
@@ -106,25 +106,34 @@ __device__ __forceinline__ uint64_t reduce_unit(const PktParams<MAXR> &p, uint64
 template <int DT, int MAXR>
 __global__ void __launch_bounds__(kPktThreads) purlin_packet_ar_kernel(
     const __grid_constant__ PktParams<MAXR> p) {
+    // The epoch comes from device memory, so a launch replayed from a graph
+    // still uses a new flag and the other staging buffer.
+    __shared__ Ctl ctl;
+    epoch_enter(p.dev_epoch, &ctl);
+    __syncthreads();
+    const uint64_t epoch = ctl.epoch;
+    const uint32_t flag = (uint32_t)epoch;
+    unsigned char *const staging = p.staging + (epoch & 1ull) * kPacketStagingBytes;
+
     const bool reducer = (int)blockIdx.x < p.G;
     const uint64_t b = reducer ? blockIdx.x : blockIdx.x - (unsigned)p.G;
     const uint64_t stride = (uint64_t)p.G * blockDim.x;
     for (uint64_t u = b * blockDim.x + threadIdx.x; u < p.units; u += stride) {
         const uint64_t off = 8 * u;
         const uint32_t valid = (uint32_t)(p.nbytes - off < 8 ? p.nbytes - off : 8);
-        unsigned char *pk = p.staging + 16 * u;
+        unsigned char *pk = staging + 16 * u;
         if (reducer) {
             const uint64_t v = reduce_unit<DT>(p, off, valid);
-            if ((int64_t)u != p.drop_unit) atom::packet_store(pk, v, p.flag);
+            if ((int64_t)u != p.drop_unit) atom::packet_store(pk, v, flag);
             continue;
         }
         uint64_t v;
-        if (!atom::packet_load(pk, p.flag, &v)) {
-            if (error_set(p.err)) return;   // an earlier wait of this launch gave up
+        if (!atom::packet_load(pk, flag, &v)) {
+            if (error_set(p.err)) break;   // an earlier wait of this launch gave up
             const uint64_t t0 = atom::globaltimer_ns();
             uint32_t ns = 0;
             bool ok = false;
-            while (!(ok = atom::packet_load(pk, p.flag, &v))) {
+            while (!(ok = atom::packet_load(pk, flag, &v))) {
                 if ((int64_t)(atom::globaltimer_ns() - t0) > p.timeout_ns) {
                     record_error(p.err, PURLIN_ERR_TIMEOUT, kSitePacketWait, u);
                     break;
@@ -132,10 +141,12 @@ __global__ void __launch_bounds__(kPktThreads) purlin_packet_ar_kernel(
                 if (ns) __nanosleep(ns);
                 ns = ns < 256 ? ns + 32 : 256;
             }
-            if (!ok) return;
+            if (!ok) break;
         }
         for (int d = 0; d < p.R; ++d) store_unit<DT>(static_cast<char *>(p.dst[d]), off, valid, v);
     }
+    __syncthreads();
+    epoch_leave(p.dev_epoch, 1, gridDim.x);
 }
 
 template <int DT, int MAXR>
@@ -146,12 +157,12 @@ cudaError_t launch_pkt_t(const PktLaunch &a) {
         p.dst[r] = r < a.R ? a.dst[r] : nullptr;
     }
     p.staging = a.staging;
+    p.dev_epoch = reinterpret_cast<DevEpoch *>(a.dev_epoch);
     p.err = a.err;
     p.nbytes = a.nbytes;
     p.units = (a.nbytes + 7) / 8;
     p.timeout_ns = a.timeout_ns;
     p.drop_unit = a.drop_unit;
-    p.flag = a.flag;
     p.R = a.R;
     p.G = a.G;
     cudaLaunchAttribute attr[1];

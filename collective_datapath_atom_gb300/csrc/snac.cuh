@@ -38,9 +38,9 @@
 // error word and the CTA winds down (its own bulk copies are waited for).
 //
 // Parameter objects (class P) expose: src[] and dst[] (rank buffer bases),
-// segs / segs_dev (segment table), flags, err, nchunks, nunits, epoch,
-// timeout_ns, drop_notify, flag_slots, stages, slot_stride, nseg, R and
-// vector_copies.
+// segs / segs_dev (segment table), err, nchunks, nunits, timeout_ns,
+// drop_notify, flag_slots, stages, slot_stride, nseg, R and vector_copies.
+// The flag set and epoch of a launch are passed to run_ring separately.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -69,7 +69,7 @@ enum ErrSite : uint64_t {
 struct Ctl {
     int abort;
     int pad;
-    unsigned long long epoch;   // device API: this CTA's epoch for the call
+    unsigned long long epoch;   // this CTA's epoch for the launch (device epoch, device API)
 };
 
 // Bytes of the ring's workspace: S stages of slot_stride bytes, 4*S
@@ -325,11 +325,12 @@ __device__ __forceinline__ bool ring_wait(uint64_t *bar, uint32_t parity, volati
 // waits of the launch are skipped.  __syncwarp then orders every lane's
 // acquire before the bulk load lane 0 issues next.
 template <class P>
-__device__ void acquire_range(const P &p, uint64_t d0, uint64_t d1, int lane) {
+__device__ void acquire_range(const P &p, const unsigned long long *flags, uint64_t epoch,
+                              uint64_t d0, uint64_t d1, int lane) {
     for (uint64_t d = d0 + (uint64_t)lane; d < d1; d += 32) {
         if (error_set(p.err)) break;
-        const unsigned long long *f = p.flags + (d % p.flag_slots);
-        const unsigned long long want = p.epoch + d / p.flag_slots;
+        const unsigned long long *f = flags + (d % p.flag_slots);
+        const unsigned long long want = epoch + d / p.flag_slots;
         if (atom::flag_acquire(f) >= want) continue;
         const uint64_t t0 = atom::globaltimer_ns();
         uint32_t ns = 32;
@@ -349,14 +350,45 @@ __device__ void acquire_range(const P &p, uint64_t d0, uint64_t d1, int lane) {
 // SNAC notify: publish a completed chunk (its stores are complete and
 // ordered before this store by the caller).
 template <class P>
-__device__ __forceinline__ void notify_chunk(const P &p, uint64_t c) {
+__device__ __forceinline__ void notify_chunk(const P &p, unsigned long long *flags, uint64_t epoch,
+                                             uint64_t c) {
     if ((int64_t)c == p.drop_notify) return;   // host-side fault injection
-    atom::flag_release(p.flags + (c % p.flag_slots), p.epoch + c / p.flag_slots);
+    atom::flag_release(flags + (c % p.flag_slots), epoch + c / p.flag_slots);
 }
 
+// ------------------------------------------------------ device epoch --
+//
+// The epoch of a launch whose CTAs notify one another lives in device
+// memory, so that a launch replayed from a CUDA graph (its parameters frozen
+// at capture) still gets a new epoch: every CTA reads it on entry, and the
+// last CTA to finish advances it by the launch's odd increment.  Every CTA
+// increments `done` only after it has read the epoch, and the epoch moves
+// only once `done` reaches the grid size, so all CTAs of a launch read the
+// same value; the next launch on the stream reads the advanced one.
+struct DevEpoch {
+    unsigned long long epoch;
+    unsigned long long done;
+};
+
+// Thread 0 reads the epoch into ctl->epoch; the caller synchronises the CTA.
+__device__ __forceinline__ void epoch_enter(const DevEpoch *e, Ctl *ctl) {
+    if (threadIdx.x == 0) ctl->epoch = *reinterpret_cast<const volatile unsigned long long *>(&e->epoch);
+}
+
+// Thread 0, after the whole CTA is done with the launch's work.
+__device__ __forceinline__ void epoch_leave(DevEpoch *e, uint64_t inc, uint32_t ctas) {
+    if (threadIdx.x != 0) return;
+    if (atomicAdd(&e->done, 1ull) == (unsigned long long)ctas - 1ull) {
+        e->done = 0;
+        atomicAdd(&e->epoch, (unsigned long long)inc);
+    }
+}
+
+// flags/epoch: this launch's flag set (the parity the epoch selects) and its
+// epoch, for plans whose chunks notify or wait (else unused).
 template <int DT, int MAXR, class P>
 __device__ void run_ring(const P &p, unsigned char *smem, Ctl *ctl_p, uint32_t bidx,
-                         uint32_t nblk) {
+                         uint32_t nblk, unsigned long long *flags, uint64_t epoch) {
     using V = atom::Vec<DT>;
     Ctl &ctl = *ctl_p;
     // Generic-proxy writes made before this call (by this CTA, or by others
@@ -415,7 +447,7 @@ __device__ void run_ring(const P &p, unsigned char *smem, Ctl *ctl_p, uint32_t b
                 const uint64_t nred = (sg.bytes - sg.head - sg.tail + rc - 1) / rc;
                 const uint64_t d0 = g.ci * ratio;
                 const uint64_t d1 = d0 + ratio < nred ? d0 + ratio : nred;
-                acquire_range(p, sg.dep_chunk + d0, sg.dep_chunk + d1, lane);
+                acquire_range(p, flags, epoch, sg.dep_chunk + d0, sg.dep_chunk + d1, lane);
             }
             unsigned char *sp = ring + (size_t)slot * p.slot_stride;
             const int nsrc = sg.src_rank < 0 ? R : 1;
@@ -455,7 +487,7 @@ __device__ void run_ring(const P &p, unsigned char *smem, Ctl *ctl_p, uint32_t b
         auto publish = [&]() {
             if (lane == 0 && npend > 0) {
                 atom::fence_acq_rel_gpu();   // the consumer warps' stores, at GPU scope
-                for (int i = 0; i < npend; ++i) notify_chunk(p, pend[i]);
+                for (int i = 0; i < npend; ++i) notify_chunk(p, flags, epoch, pend[i]);
             }
             npend = 0;
         };

@@ -55,11 +55,9 @@ struct VcView {
     void *const *dst;
     const Seg *segs;
     const Seg *segs_dev;
-    unsigned long long *flags;
     unsigned long long *err;
     uint64_t nchunks;
     uint64_t nunits;
-    uint64_t epoch;
     int64_t timeout_ns;
     int64_t drop_notify;
     uint32_t flag_slots;
@@ -244,9 +242,9 @@ __global__ void __launch_bounds__(kVcThreadsMax, 1)
     }
     __syncthreads();
 
-    const VcView v{p.src,     p.dst,         nullptr,       segs,    nullptr, p.err,
-                   hdr->nchunks, hdr->nunits, 0,            p.timeout_ns, -1, 1u,
-                   S,         p.slot_stride, nseg,          R,       p.vector_copies};
+    const VcView v{p.src,        p.dst,         nullptr,      segs, p.err,
+                   hdr->nchunks, hdr->nunits,   p.timeout_ns, -1,   1u,
+                   S,            p.slot_stride, nseg,         R,    p.vector_copies};
     if (hdr->nchunks > 0xFFFFFFF0ull) {
         if (blockIdx.x == 0 && threadIdx.x == 0)
             record_error(p.err, PURLIN_ERR_INVALID_ARG, kSiteDeviceCounts, 1);
@@ -259,7 +257,7 @@ __global__ void __launch_bounds__(kVcThreadsMax, 1)
                              (uint64_t)gridDim.x * nt);
         return;
     }
-    run_ring<DT, MAXR>(v, smem, ctl, blockIdx.x, gridDim.x);
+    run_ring<DT, MAXR>(v, smem, ctl, blockIdx.x, gridDim.x, nullptr, 0);
 }
 
 template <int DT, int MAXR>

@@ -211,9 +211,11 @@ purlin_status purlin_all_to_all_v_device_counts(purlin_ctx *ctx, const void *con
  * their own pool and let no library take more.  Same contract and result
  * (bit for bit) as purlin_all_reduce with PURLIN_OPT_AR_MODE = composed,
  * without a context: R (1..31) rank buffers, n elements each, enqueued on
- * `stream`.  Its scratch (per-chunk flags and an error word, 128 KiB + 8
- * bytes) is a fixed device array inside the library, held by every GPU that
- * loads it until the process exits.  Limit: at most 8192 reduce chunks of
+ * `stream`.  Its scratch (per-chunk flags, an error word and the device
+ * epoch, 128 KiB + 32 bytes) is a fixed device array inside the library,
+ * held by every GPU that loads it until the process exits.  The epoch is
+ * kept on the device, so a call captured into a CUDA graph stays correct at
+ * every replay.  Limit: at most 8192 reduce chunks of
  * 96 KiB / R bytes per source (rounded down to a multiple of 16), i.e.
  * n * element size <= 8192 * (98304 / R) bytes per rank (96 MiB at R = 8);
  * larger calls and R > 31 return

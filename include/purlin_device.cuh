@@ -77,11 +77,9 @@ struct CollView {
     void *const *dst;
     const Seg *segs;       // no inline table
     const Seg *segs_dev;   // the descriptor's device table
-    unsigned long long *flags;
     unsigned long long *err;
     uint64_t nchunks;
     uint64_t nunits;
-    uint64_t epoch;
     int64_t timeout_ns;
     int64_t drop_notify;
     uint32_t flag_slots;
@@ -122,11 +120,9 @@ __device__ purlin_status collective_t(const purlin_device_coll &c, const SnacArg
                              c.dst,
                              nullptr,
                              static_cast<const Seg *>(c.segs),
-                             c.flags ? c.flags + (epoch & 1ull) * c.flag_slots : nullptr,
                              c.err,
                              c.nchunks,
                              c.nunits,
-                             epoch,
                              c.timeout_ns,
                              c.drop_notify,
                              c.flag_slots,
@@ -135,7 +131,8 @@ __device__ purlin_status collective_t(const purlin_device_coll &c, const SnacArg
                              c.nseg,
                              c.R,
                              c.vector_copies};
-    snac::run_ring<DT, MAXR>(v, ws, ctl, (uint32_t)a.bIdx, (uint32_t)a.blocks);
+    snac::run_ring<DT, MAXR>(v, ws, ctl, (uint32_t)a.bIdx, (uint32_t)a.blocks,
+                             c.flags ? c.flags + (epoch & 1ull) * c.flag_slots : nullptr, epoch);
     // (run_ring ends with a CTA barrier.)  One thread reads the error word
     // so that every thread returns the same status.
     if (threadIdx.x == 0) {
@@ -186,11 +183,9 @@ struct Atom {
         void *const *dst;
         const Seg *segs;
         const Seg *segs_dev;
-        unsigned long long *flags;
         unsigned long long *err;
         uint64_t nchunks;
         uint64_t nunits;
-        uint64_t epoch;
         int64_t timeout_ns;
         int64_t drop_notify;
         uint32_t flag_slots;
@@ -236,11 +231,9 @@ struct Atom {
                      reinterpret_cast<void *const *>(ws + kPtrs + 8),
                      nullptr,
                      reinterpret_cast<const Seg *>(ws + kSeg),
-                     nullptr,
                      reinterpret_cast<unsigned long long *>(ws + kErr),
                      nchunks,
                      nunits,
-                     0,
                      0,
                      -1,
                      1,
@@ -249,7 +242,8 @@ struct Atom {
                      1,
                      nsrc,
                      0};
-        snac::run_ring<DT, MAXR>(v, ws, reinterpret_cast<snac::Ctl *>(ws + kCtl), 0u, 1u);
+        snac::run_ring<DT, MAXR>(v, ws, reinterpret_cast<snac::Ctl *>(ws + kCtl), 0u, 1u, nullptr,
+                                 0);
         return *reinterpret_cast<volatile unsigned long long *>(ws + kErr) != 0ull
                    ? PURLIN_ERR_TIMEOUT
                    : PURLIN_OK;

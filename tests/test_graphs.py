@@ -1,0 +1,108 @@
+"""Calls captured into a CUDA graph stay correct at every replay.
+
+The modes whose CTAs notify one another (the composed AllReduce with chunk
+flags, the latency path's packets, the no-allocation AllReduce, and a
+device-side collective) take their epoch from device memory: a replayed
+launch has its parameters frozen at capture, yet must not take the flags or
+packets of an earlier replay for its own.  Each test captures a few calls,
+then replays the graph several times with new inputs copied in between, and
+checks every replay bit for bit against the CPU oracle.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from test_parity_gpu import gen_inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+R = 8
+
+
+@pytest.fixture(scope="module")
+def P():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import collective_datapath_atom_gb300 as mod
+
+    torch.cuda.set_device(0)
+    return mod
+
+
+def replay_and_check(P, stream, call, src, dst, n, replays=4, calls_per_graph=2):
+    """Capture `calls_per_graph` calls of `call`, then replay with fresh inputs."""
+    call()                                   # compile and cache the plan before capture
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(calls_per_graph):
+            call()
+    for k in range(replays):
+        ins = gen_inputs([n] * R, 1, seed=7000 + k)
+        with torch.cuda.stream(stream):
+            for s, x in zip(src, ins):
+                s.copy_(torch.from_numpy(x.view(np.int16)), non_blocking=False)
+            for d in dst:
+                d.zero_()
+        stream.synchronize()
+        g.replay()
+        stream.synchronize()
+        want = oracle.all_reduce(ins, 1)
+        for d in range(R):
+            got = dst[d].cpu().numpy().view(np.uint16)
+            assert np.array_equal(got, want[d]), f"replay {k}: rank {d} differs"
+
+
+def buffers(n):
+    src = [torch.empty(n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    dst = [torch.zeros(n, dtype=torch.int16, device="cuda") for _ in range(R)]
+    return src, dst
+
+
+@pytest.mark.parametrize("mode", [2, 3], ids=["chunk-flags", "packets"])
+def test_composed_allreduce_in_a_graph(P, mode):
+    stream = torch.cuda.Stream()
+    ctx = P.purlin_init(R, stream)
+    try:
+        P.purlin_set_option(ctx, P.PURLIN_OPT_AR_MODE, mode)
+        P.purlin_set_option(ctx, P.PURLIN_OPT_VARIANT, 2 if mode == 2 else 0)
+        n = (3 << 20) // 2 + 5 if mode == 2 else (1 << 20) // 2 - 3
+        src, dst = buffers(n)
+        replay_and_check(P, stream, lambda: P.purlin_all_reduce(ctx, src, dst, n, 1), src, dst, n)
+        assert P.purlin_last_launch(ctx)["variant"] == (3 if mode == 2 else 5)
+        assert P.purlin_check_status(ctx) == P.PURLIN_OK
+    finally:
+        ctx.close()
+
+
+def test_noalloc_allreduce_in_a_graph(P):
+    stream = torch.cuda.Stream()
+    n = (5 << 20) // 2 + 1
+    src, dst = buffers(n)
+    replay_and_check(P, stream,
+                     lambda: P.purlin_all_reduce_noalloc(R, src, dst, n, 1, stream=stream),
+                     src, dst, n, calls_per_graph=3)
+
+
+def test_device_collective_in_a_graph(P):
+    from collective_datapath_atom_gb300 import examples as X
+
+    stream = torch.cuda.Stream()
+    ctx = P.purlin_init(R, stream)
+    try:
+        P.purlin_set_option(ctx, P.PURLIN_OPT_AR_MODE, 2)
+        n = (2 << 20) // 2 + 7
+        src, dst = buffers(n)
+        blocks = torch.cuda.get_device_properties(0).multi_processor_count
+        d = P.purlin_device_prepare(ctx, P.PURLIN_COLL_ALL_REDUCE, src, dst, n=n, dtype=1,
+                                    blocks=blocks)
+        assert d.composed == 1
+        replay_and_check(P, stream, lambda: X.collective(d, stream=stream), src, dst, n)
+        assert P.purlin_device_check(d, stream) == P.PURLIN_OK
+        P.purlin_device_release(ctx, d)
+    finally:
+        ctx.close()
