@@ -108,7 +108,13 @@ struct CacheEntry {
     std::string key;
     Plan plan;
     Seg *segs_dev = nullptr;
+    bool pinned = false;   // used while a CUDA graph was captured: kept until finalize
 };
+
+bool capturing(cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    return cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone;
+}
 
 int64_t env_or(const char *name, int64_t dflt) {
     const char *v = std::getenv(name);
@@ -176,6 +182,9 @@ purlin_status get_plan(purlin_ctx *ctx, const CallDesc &c, int variant, int ar_m
     purlin_status st = compile_plan(c, variant, ar_mode, red_slot, copy_chunk, &e.plan);
     if (st != PURLIN_OK) return st;
     if (param_class(c.R, e.plan.segs.size()) != kClassSmall) {
+        // An upload cannot be captured into a graph: the first call of such a
+        // shape must come before capture.
+        if (capturing(ctx->stream)) return PURLIN_ERR_UNSUPPORTED;
         // More segments than the small parameter block holds: the table
         // lives in device memory (uploaded once per cached plan) and the
         // kernels stage it into shared memory with coalesced loads.  A large
@@ -192,10 +201,18 @@ purlin_status get_plan(purlin_ctx *ctx, const CallDesc &c, int variant, int ar_m
     }
     ctx->lru.push_front(std::move(e));
     ctx->index[key] = ctx->lru.begin();
-    while (ctx->lru.size() > kPlanCacheCap) {
-        drop_entry(ctx->lru.back());
-        ctx->index.erase(ctx->lru.back().key);
-        ctx->lru.pop_back();
+    // Evict the least recently used plans past the cap, but never one that a
+    // captured graph may still launch (its device table address is frozen in
+    // the graph).
+    auto it2 = ctx->lru.end();
+    size_t unpinned_over = ctx->lru.size() > kPlanCacheCap ? ctx->lru.size() - kPlanCacheCap : 0;
+    while (unpinned_over > 0 && it2 != ctx->lru.begin()) {
+        --it2;
+        if (it2->pinned) continue;
+        drop_entry(*it2);
+        ctx->index.erase(it2->key);
+        it2 = ctx->lru.erase(it2);
+        --unpinned_over;
     }
     *out = &*ctx->lru.begin();
     return PURLIN_OK;
@@ -346,6 +363,7 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
         if (st != PURLIN_OK) return st;
     }
     const Plan &pl = e->plan;
+    if (e->segs_dev != nullptr && !e->pinned && capturing(ctx->stream)) e->pinned = true;
 
     purlin_launch_info info = {};
     info.segments = (int64_t)pl.segs.size();

@@ -40,6 +40,16 @@
  *     a valid no-op.
  *   Device faults.  A bounded wait that expires inside a kernel records
  *     PURLIN_ERR_TIMEOUT in the context's error word; purlin_check reports it.
+ *   CUDA graphs.  Calls may be captured from the context's stream and the
+ *     graph replayed any number of times (launches whose CTAs notify one
+ *     another keep their epoch in device memory).  The first call of a call
+ *     shape (collective, sizes, counts, options) compiles its plan; when the
+ *     plan's segment table is too large for the kernel parameters
+ *     (AllToAll(V) and the composed AllReduce at R = 8, for example) it is
+ *     uploaded to device memory, which cannot happen during capture: make
+ *     that first call before capturing, or it returns
+ *     PURLIN_ERR_UNSUPPORTED.  Plans used during a capture are kept until
+ *     purlin_finalize; a graph must not be replayed after it.
  */
 #ifndef PURLIN_H
 #define PURLIN_H

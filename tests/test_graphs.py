@@ -106,3 +106,78 @@ def test_device_collective_in_a_graph(P):
         P.purlin_device_release(ctx, d)
     finally:
         ctx.close()
+
+
+def test_alltoallv_graph_survives_plan_cache_pressure(P):
+    """An AllToAllV plan (its segment table in device memory) used in a
+    captured graph stays valid while more than the cache's 64 other shapes
+    pass through it; replays after that are still correct."""
+    import workloads
+
+    stream = torch.cuda.Stream()
+    ctx = P.purlin_init(R, stream)
+    try:
+        part = workloads.zipf_partition(300001)
+        C = workloads.rotated_counts(part)
+        counts = C.reshape(-1).tolist()
+        T = int(C.sum(axis=1)[0])
+        src = [torch.empty(T, dtype=torch.int16, device="cuda") for _ in range(R)]
+        dst = [torch.zeros(int(C[:, d].sum()), dtype=torch.int16, device="cuda") for d in range(R)]
+        call = lambda: P.purlin_all_to_all_v(ctx, src, dst, counts, 1)   # noqa: E731
+        call()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            call()
+
+        def check(k):
+            ins = gen_inputs([T] * R, 1, seed=8000 + k)
+            with torch.cuda.stream(stream):
+                for s, x in zip(src, ins):
+                    s.copy_(torch.from_numpy(x.view(np.int16)))
+                for d in dst:
+                    d.zero_()
+            stream.synchronize()
+            g.replay()
+            stream.synchronize()
+            want = oracle.all_to_all_v(ins, C, 1)
+            for d in range(R):
+                assert np.array_equal(dst[d].cpu().numpy().view(np.uint16), want[d]), \
+                    f"replay {k}: rank {d}"
+
+        check(0)
+        # 70 other shapes through the 64-entry plan cache
+        small = [torch.empty(4096, dtype=torch.int16, device="cuda") for _ in range(2 * R)]
+        for k in range(70):
+            cs = [1 + (k + i) % 7 for i in range(R * R)]
+            need_in = max(sum(cs[s * R:(s + 1) * R]) for s in range(R))
+            need_out = max(sum(cs[s * R + d] for s in range(R)) for d in range(R))
+            assert need_in <= 4096 and need_out <= 4096
+            P.purlin_all_to_all_v(ctx, small[:R], small[R:], cs, 1)
+        P.purlin_check(ctx)
+        check(1)
+    finally:
+        ctx.close()
+
+
+def test_first_call_of_a_large_plan_during_capture_is_refused(P):
+    """A plan whose table must be uploaded cannot be compiled while the
+    stream is being captured: the call returns UNSUPPORTED instead of
+    recording an upload the graph could not replay."""
+    stream = torch.cuda.Stream()
+    ctx = P.purlin_init(R, stream)
+    try:
+        counts = [3] * (R * R)
+        src = [torch.empty(3 * R, dtype=torch.int16, device="cuda") for _ in range(R)]
+        dst = [torch.empty(3 * R, dtype=torch.int16, device="cuda") for _ in range(R)]
+        g = torch.cuda.CUDAGraph()
+        with pytest.raises(P.PurlinError) as e:
+            with torch.cuda.graph(g, stream=stream):
+                P.purlin_all_to_all_v(ctx, src, dst, counts, 1)
+        assert e.value.status == P.PURLIN_ERR_UNSUPPORTED
+        torch.cuda.synchronize()
+        # outside capture the same call works
+        P.purlin_all_to_all_v(ctx, src, dst, counts, 1)
+        P.purlin_check(ctx)
+    finally:
+        ctx.close()
