@@ -181,3 +181,48 @@ def test_first_call_of_a_large_plan_during_capture_is_refused(P):
         P.purlin_check(ctx)
     finally:
         ctx.close()
+
+
+def test_device_count_alltoallv_graph_with_new_counts_each_replay(P):
+    """MoE dispatch in a graph: the counts live in device memory and change
+    between replays (as a router on the GPU would write them); each replay
+    dispatches by the counts it finds, with no host involvement."""
+    import workloads
+
+    H = 64
+    tokens = 96
+    stream = torch.cuda.Stream()
+    ctx = P.purlin_init(R, stream)
+    try:
+        cap_out = R * tokens * H
+        src = [torch.empty(tokens * H, dtype=torch.int16, device="cuda") for _ in range(R)]
+        dst = [torch.zeros(cap_out, dtype=torch.int16, device="cuda") for _ in range(R)]
+        d_counts = torch.zeros(R * R, dtype=torch.int64, device="cuda")
+        call = lambda: P.purlin_all_to_all_v_device_counts(   # noqa: E731
+            ctx, src, dst, d_counts, tokens * H, cap_out, 1)
+        call()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            call()
+        for k in range(4):
+            C, _ = workloads.moe_dispatch(seed=20 + k, tokens=tokens, hidden=H, payload=False)
+            counts = (C * H).reshape(-1)
+            ins = gen_inputs([tokens * H] * R, 1, seed=9000 + k)
+            with torch.cuda.stream(stream):
+                d_counts.copy_(torch.from_numpy(counts))
+                for s, x in zip(src, ins):
+                    s.copy_(torch.from_numpy(x.view(np.int16)))
+                for d in dst:
+                    d.zero_()
+            stream.synchronize()
+            g.replay()
+            stream.synchronize()
+            want = oracle.all_to_all_v(ins, counts.reshape(R, R), 1)
+            for d in range(R):
+                got = dst[d][:want[d].size].cpu().numpy().view(np.uint16)
+                assert np.array_equal(got, want[d]), f"replay {k}: rank {d}"
+                assert int(dst[d][want[d].size:].abs().sum().item()) == 0
+        assert P.purlin_check_status(ctx) == P.PURLIN_OK
+    finally:
+        ctx.close()
