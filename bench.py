@@ -589,7 +589,8 @@ def sweep(args):
             r["row"] = "small"
             emit(r)
 
-    # ---- the pages' V-collective sweep (paper summary §C.4): Zipf(0.125)
+    # ---- the pages' V-collective sweep ("Purlin: Separating Orchestration from the Datapath of Collectives"
+    # §C.4): Zipf(0.125)
     # split of a total T per rank, 1 KiB .. 1 GiB, through the C ABI
     for coll in ("AGV", "RSV", "A2AV"):
         res = subprocess.run([exe, coll, "1024", str(1 << 30), "10", "10", "2", "42"],

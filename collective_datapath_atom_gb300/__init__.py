@@ -40,7 +40,8 @@ PURLIN_ERR_TIMEOUT = 7
  PURLIN_COLL_ALL_TO_ALL, PURLIN_COLL_ALL_GATHER_V, PURLIN_COLL_REDUCE_SCATTER_V,
  PURLIN_COLL_ALL_TO_ALL_V) = range(7)
 
-# The one legal (op, layout) pair of each collective (paper summary §3.1).
+# The one legal (op, layout) pair of each collective
+# ("Purlin: Separating Orchestration from the Datapath of Collectives" §3.1).
 LAYOUTS = {
     "all_reduce": (PURLIN_SUM, (PURLIN_SCATTERED, PURLIN_SCATTERED)),
     "reduce_scatter": (PURLIN_SUM, (PURLIN_SCATTERED, PURLIN_PACKED)),

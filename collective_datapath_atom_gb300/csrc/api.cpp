@@ -2,7 +2,8 @@
 //
 // Host side of one call: validate (no partial work on error), compile the
 // layout into a plan (cached by its key), pick the variant by message size
-// (codesign policy, paper summary §4.2; push/latency vs pull/throughput,
+// (codesign policy, "Purlin: Separating Orchestration from the Datapath of Collectives"
+// §4.2; push/latency vs pull/throughput,
 // §3.2), size the launch (CTAs, ring depth: in-flight capacity near the
 // bandwidth-delay product with few CTAs, §3.3), advance the epoch (§4.3)
 // and enqueue one kernel.  Nothing here synchronises with the device
@@ -35,7 +36,8 @@ constexpr int kCopyConsumerWarps = 4;
 constexpr int kReduceConsumerWarps = 8;
 constexpr int kShiftedCopyConsumerWarps = 6;
 
-// Policy per collective (codesign policy, paper summary §4.2), measured on
+// Policy per collective (codesign policy, "Purlin: Separating Orchestration from the Datapath of Collectives"
+// §4.2), measured on
 // GB300 over 256 B..64 MiB per rank and at the workloads' sizes.
 // Crossover: per-rank message bytes up to which the one-shot vector kernel
 // beats the staged ring (it keeps ~150k threads' loads in flight, so for

@@ -1,4 +1,4 @@
-// atom.cuh -- sm_103a datapath primitives ("Atom", paper summary §3.3).
+// atom.cuh -- sm_103a datapath primitives (the "Atom").
 //
 // "Purlin: Separating Orchestration from the Datapath of Collectives":
 //   §3.3  the Atom offers copy and reduce through a pipeline that stages
@@ -155,7 +155,8 @@ __device__ __forceinline__ unsigned long long flag_acquire(const unsigned long l
 
 // ------------------------------------------------------------- packets --
 //
-// The latency path's payload+notification packet (paper summary §3.2): 16
+// The latency path's payload+notification packet ("Purlin: Separating Orchestration from the Datapath of Collectives"
+// §3.2): 16
 // bytes holding 8 payload bytes and the call's 32-bit flag twice, as two
 // 8-byte lines {payload word, flag}.  The store is one v2.u64 access whose
 // two 64-bit elements are each single-copy atomic (aligned 64-bit accesses),

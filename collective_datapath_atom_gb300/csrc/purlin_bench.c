@@ -19,7 +19,8 @@
  *   algbw_gbs   totalBytes / graph time (or single time without graphs);
  *   eff_gbs     bytes every rank buffer reads plus writes / the same time.
  * The V collectives split the size with the Zipf(s = 0.125) partition of the
- * paper summary §C.4 (uniform at 1 and 2 KiB; AllToAllV rotates the
+ * "Purlin: Separating Orchestration from the Datapath of Collectives" §C.4
+ * (uniform at 1 and 2 KiB; AllToAllV rotates the
  * partition so every rank sends and receives the full size).
  * Inputs are seeded pseudo-random bf16 values; their values do not change
  * the work.

@@ -2,7 +2,7 @@
 // memory.
 //
 // "Purlin: Separating Orchestration from the Datapath of Collectives", §C.4
-// (the V variants) and the paper summary's note that the implementation
+// (the V variants) and the same page's §4 note that the implementation
 // takes prefix sums on the device; here the counts come from a kernel (an
 // MoE router, say) and never travel to the host.  One kernel does it all:
 // every CTA loads the counts, checks them against the capacities the caller

@@ -3,7 +3,7 @@
  *
  * What the library computes.  The seven non-rooted collectives of
  * "Purlin: Separating Orchestration from the Datapath of Collectives"
- * (paper summary, §2.1 collective contracts; §3.1 layouts) over R "rank
+ * (§2.1 collective contracts; §3.1 layouts) over R "rank
  * buffers" that all live in ONE GPU's memory: rank r's input is src[r] and
  * its output is dst[r].  Each call is a single kernel: a layout compiler turns
  * (input layout, output layout, copy-or-reduce op, counts) into a chunk
@@ -105,9 +105,10 @@ typedef enum {
  * "Host-side", reshaped for one process holding all R ranks).  Allocates the
  * device flag array (2 parities x 65536 u64, zeroed once here), the
  * latency path's packet staging (2 parities x 2 MiB, zeroed once here;
- * paper summary §4.1) and a device error word on the current CUDA device,
+ * "Purlin: Separating Orchestration from the Datapath of Collectives" §4.1) and a device
+ * error word on the current CUDA device,
  * and reads the device's SM count and shared-memory limit.  The epoch
- * (paper summary §4.3) starts at 1.
+ * ("Purlin: Separating Orchestration from the Datapath of Collectives" §4.3) starts at 1.
  * Errors: INVALID_ARG (R out of range, out == NULL), CUDA, OOM. */
 purlin_status purlin_init(int R, purlin_stream stream, purlin_ctx **out);
 
@@ -260,7 +261,8 @@ const char *purlin_status_string(purlin_status status);
 
 /* ---------------------------------------------------------------- policy */
 
-/* Codesign policy knobs (paper summary §4.2: crossover, chunk sizes, CTA
+/* Codesign policy knobs ("Purlin: Separating Orchestration from the Datapath of Collectives"
+ * §4.2: crossover, chunk sizes, CTA
  * allocation, pipeline depth, tuned per collective and GPU; applications
  * may override).  0 means "the built-in policy" for every knob.
  * purlin_init also reads PURLIN_VARIANT, PURLIN_CROSSOVER_BYTES,
@@ -354,7 +356,8 @@ purlin_status purlin_plan_inspect(purlin_collective coll, int R, const void *con
 /* A collective compiled for kernels that run it themselves (the "Purlin"
  * project README, "Device-side": a user kernel calls a collective, or an
  * Atom, from inside itself, so communication fuses with its other work;
- * paper summary §3: applications invoke the Atom directly).
+ * "Purlin: Separating Orchestration from the Datapath of Collectives" §3: applications
+ * invoke the Atom directly).
  *
  * purlin_device_prepare fills one of these for one call shape: the
  * collective, its R rank buffers, counts and dtype, and the number of CTAs

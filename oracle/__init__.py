@@ -9,7 +9,7 @@ The arithmetic lives in ``purlin_oracle.c`` (plain C99, nested per-rank
 loops, one binary32 addition per step); this module only builds that file
 with gcc and marshals numpy arrays into it.  Every function cites the
 passage of "Purlin: Separating Orchestration from the Datapath of
-Collectives" (paper summary, sections §2.1, §3.1, §3.3, §C.4) or of the
+Collectives" (§2.1, §3.1, §3.3, §C.4) or of the
 "Purlin" project README that it follows; see the C file's header.
 
 Arrays: each rank buffer is a 1-D numpy array.  fp32 data is ``np.float32``;

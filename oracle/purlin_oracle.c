@@ -11,7 +11,7 @@
  *
  * Sources (page title, then section):
  *   [P2] "Purlin: Separating Orchestration from the Datapath of Collectives"
- *        (paper summary): §2.1 collective contracts are fixed independently of
+ *        §2.1: collective contracts are fixed independently of
  *        the communication steps; variable-length variants let contributions
  *        or partitions differ in size.  §3.1 layouts: packed, scattered,
  *        transposed; AllReduce is ReduceScatter followed by AllGather.  §3.3

@@ -95,7 +95,8 @@ def test_device_collective_parity(P, X, coll, dtype, R):
 @pytest.mark.parametrize("dtype", [0, 1], ids=["f32", "bf16"])
 def test_device_composed_allreduce(P, X, dtype):
     """Composed AllReduce inside a user kernel: reducing CTAs publish
-    per-chunk flags, gathering CTAs acquire them (paper summary §3.2).  With
+    per-chunk flags, gathering CTAs acquire them ("Purlin: Separating Orchestration from the Datapath of Collectives"
+    §3.2).  With
     256-byte chunks the 16 MiB-per-rank case has more notifying chunks than
     flag slots, so chunk flags take two generations within a call."""
     R = 8

@@ -200,7 +200,8 @@ def test_parity(P, coll, dtype, variant, R):
 @pytest.mark.parametrize("R", [2, 3, 8])
 def test_allreduce_composed_mode(P, dtype, R):
     """SNAC across CTAs: reducing CTAs notify per-chunk flags, gathering CTAs
-    acquire them (paper summary §3.2 composed AllReduce)."""
+    acquire them ("Purlin: Separating Orchestration from the Datapath of Collectives"
+    §3.2, composed AllReduce)."""
     ctx = make_ctx(P, R)
     try:
         P.purlin_set_option(ctx, P.PURLIN_OPT_VARIANT, 2)
@@ -258,7 +259,8 @@ def test_allreduce_composed_flag_generations(P, ctx8):
 
 
 def test_repeated_calls_need_no_reset(P, ctx8):
-    """Epoch parity and monotonic flags (paper summary §4.3): many calls in a
+    """Epoch parity and monotonic flags ("Purlin: Separating Orchestration from the Datapath of Collectives"
+    §4.3): many calls in a
     row, no flag reset, each correct; the epoch advances by an odd amount."""
     P.purlin_set_option(ctx8, P.PURLIN_OPT_VARIANT, 2)
     P.purlin_set_option(ctx8, P.PURLIN_OPT_AR_MODE, 2)
@@ -408,7 +410,8 @@ def test_nan_and_signed_zero_copies_are_bitwise(P, ctx8):
 def test_v_collectives_zipf_partition(P, ctx8, total_bytes):
     """AllGatherV / ReduceScatterV / AllToAllV on the Zipf(s = 0.125) split of
     a total T over 8 ranks (uniform at 1 and 2 KiB; AllToAllV rotates the
-    split so every rank sends and receives T), paper summary §C.4."""
+    split so every rank sends and receives T), "Purlin: Separating Orchestration from the Datapath of Collectives"
+    §C.4."""
     T = total_bytes // 2
     part = workloads.zipf_partition(T)
     assert sum(part) == T

@@ -13,7 +13,8 @@ Recipe (every array is drawn rank-major, rank 0 first, from one
   source rank in order, ``multinomial(tokens, p)`` with Zipf destination
   weights ``p_d ~ (d+1)^-1.2``; the payload normals continue the same stream.
 
-The workloads are the ones the paper summary's §2.1 names (throughput-bound
+The workloads are the ones "Purlin: Separating Orchestration from the Datapath of Collectives"
+§2.1 names (throughput-bound
 prefill payloads and latency-bound decode messages) and the MoE dispatch
 pattern of Table 2, shaped as single-GPU rank buffers.
 """
@@ -115,7 +116,8 @@ def moe_dispatch(seed: int = 3, R: int = 8, tokens: int = MOE_TOKENS, hidden: in
 
 
 def zipf_partition(total: int, R: int = 8, s: float = 0.125) -> list[int]:
-    """The V-collective split of the paper summary §C.4: rank r's share of a
+    """The V-collective split of "Purlin: Separating Orchestration from the Datapath of Collectives"
+    §C.4: rank r's share of a
     total of `total` elements has weight (r+1)^-s; floor each share and give
     the remainder to rank 0, so the split preserves the total.  Totals of at
     most 2 KiB of bf16 (1024 elements) are split uniformly, as the section
