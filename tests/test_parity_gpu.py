@@ -512,3 +512,32 @@ def test_cfg_allreduce_sweep(P, ctx8, batch):
         # every output holds the same bits
         for d in range(1, 8):
             assert torch.equal(dst[d], dst[0])
+
+
+# --------------------------------------------------------------- wide R ----
+
+@pytest.mark.parametrize("coll", COLLS)
+@pytest.mark.parametrize("variant", [1, 2], ids=["latency", "throughput"])
+@pytest.mark.parametrize("R", [16, 64])
+def test_parity_wide_R(P, coll, variant, R):
+    """More than 8 ranks: the rank pointers need the large parameter block and
+    the segment tables live in device memory (AllToAll(V) at R = 64 has 4096
+    segments, read from global memory rather than staged)."""
+    ctx = make_ctx(P, R)
+    try:
+        P.purlin_set_option(ctx, P.PURLIN_OPT_VARIANT, variant)
+        rng = np.random.default_rng(R + variant)
+        if coll in ("all_reduce", "all_gather"):
+            cases = [(37, None), (4099, None)]
+        elif coll in ("reduce_scatter", "all_to_all"):
+            cases = [(R * 3, None), (R * 517, None)]
+        elif coll in ("all_gather_v", "reduce_scatter_v"):
+            cases = [(0, [int(x) for x in rng.integers(0, 300, size=R)])]
+        else:
+            cases = [(0, [int(x) for x in rng.integers(0, 40, size=R * R)])]
+        for k, (n, counts) in enumerate(cases):
+            ins = gen_inputs(in_lengths(coll, R, n, counts), 1, seed=4000 + 10 * k + R)
+            got, _ = run(P, ctx, coll, ins, out_sizes(coll, R, n, counts, 2), 1, n, counts)
+            assert_same(got, oracle_of(coll, ins, 1, counts), f"{coll} R={R} v={variant} n={n}")
+    finally:
+        ctx.close()
