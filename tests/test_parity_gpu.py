@@ -541,3 +541,20 @@ def test_parity_wide_R(P, coll, variant, R):
             assert_same(got, oracle_of(coll, ins, 1, counts), f"{coll} R={R} v={variant} n={n}")
     finally:
         ctx.close()
+
+
+@pytest.mark.parametrize("R", [16, 31, 64])
+def test_composed_allreduce_wide_R(P, R):
+    """Composed AllReduce (2R + 1 segments, notifying and waiting chunks)
+    with more than 8 ranks, against the oracle."""
+    ctx = make_ctx(P, R)
+    try:
+        P.purlin_set_option(ctx, P.PURLIN_OPT_VARIANT, 2)
+        P.purlin_set_option(ctx, P.PURLIN_OPT_AR_MODE, 2)
+        for k, n in enumerate((R * 16 * 3 + 5, 70001)):
+            ins = gen_inputs([n] * R, 1, seed=5000 + k + R)
+            got, _ = run(P, ctx, "all_reduce", ins, [n * 2] * R, 1, n)
+            assert_same(got, oracle.all_reduce(ins, 1), f"composed R={R} n={n}")
+            assert P.purlin_last_launch(ctx)["variant"] == 3
+    finally:
+        ctx.close()

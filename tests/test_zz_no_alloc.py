@@ -56,7 +56,7 @@ def _call_noalloc(P, R, src, dst, n, dtype, stream):
 
 
 @pytest.mark.parametrize("dtype", [0, 1], ids=["f32", "bf16"])
-@pytest.mark.parametrize("R,n", [(8, 1 << 20), (8, 100003), (3, 4096 + 7), (2, 40)])
+@pytest.mark.parametrize("R,n", [(8, 1 << 20), (8, 100003), (3, 4096 + 7), (2, 40), (31, 31 * 4099)])
 def test_noalloc_matches_context_allreduce_twice(P, dtype, R, n):
     stream = torch.cuda.current_stream()
     ctx = P.purlin_init(R, stream)
