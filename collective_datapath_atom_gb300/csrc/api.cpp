@@ -2,11 +2,13 @@
 //
 // Host side of one call: validate (no partial work on error), compile the
 // layout into a plan (cached by its key), pick the variant by message size
-// (codesign policy, "Purlin: Separating Orchestration from the Datapath of Collectives"
-// §4.2; push/latency vs pull/throughput,
-// §3.2), size the launch (CTAs, ring depth: in-flight capacity near the
-// bandwidth-delay product with few CTAs, §3.3), advance the epoch (§4.3)
-// and enqueue one kernel.  Nothing here synchronises with the device
+// (codesign policy, "Purlin: Separating Orchestration from the Datapath of
+// Collectives" §4.2; push/latency vs pull/throughput, §3.2), size the
+// launch (CTAs, ring depth: in-flight capacity near the bandwidth-delay
+// product with few CTAs, §3.3) and enqueue one kernel.  Notifying launches
+// advance the epoch (§4.3) themselves, in device memory.  The device-side
+// API's host calls are in device_api.cpp, the device-count V collectives'
+// in vcounts_api.cpp; what they share with this file is in host.h.  Nothing here synchronises with the device
 // except purlin_check, purlin_finalize and purlin_set_stream.
 #include <cuda_runtime.h>
 
@@ -18,47 +20,17 @@
 #include <string>
 #include <unordered_map>
 
+#include "host.h"
 #include "launch.h"
 #include "plan.h"
 
 using namespace purlin;
+using namespace purlin::host;
 
-namespace {
+// ---- shared with the other host translation units (host.h)
 
-constexpr int kNumOptions = 12;
-constexpr size_t kPlanCacheCap = 64;
-
-// Built-in policy.
-constexpr int64_t kInspectChunkBytes = 32 * 1024;        // plan_inspect default chunk
-constexpr int64_t kDefaultTimeoutNs = 100 * 1000 * 1000; // 100 ms
-constexpr int kLatBlock = 256;
-constexpr int kCopyConsumerWarps = 4;
-constexpr int kReduceConsumerWarps = 8;
-constexpr int kShiftedCopyConsumerWarps = 6;
-
-// Policy per collective (codesign policy, "Purlin: Separating Orchestration from the Datapath of Collectives"
-// §4.2), measured on
-// GB300 over 256 B..64 MiB per rank and at the workloads' sizes.
-// Crossover: per-rank message bytes up to which the one-shot vector kernel
-// beats the staged ring (it keeps ~150k threads' loads in flight, so for
-// reductions it stays competitive up to several MiB).
-// Ring shape:
-//   ReduceScatter(V)  one destination per reduced chunk: large per-source
-//                     chunks (96 KiB per stage), 2 stages;
-//   AllReduce         R stores per reduced vector: 32 KiB per stage, 3 stages;
-//   AllGather(V)      one staged tile written to R destinations: 16 KiB
-//                     chunks, 4 stages, and the 8 consumer warps store the
-//                     tile with 128-bit stores (0.956 of the copy peak versus
-//                     0.92 with bulk stores from one warp);
-//   AllToAll(V)       one load, one store per chunk: 16 KiB chunks, 3 stages,
-//                     bulk stores (0.98).
-struct Policy {
-    uint32_t chunk;         // bytes per source per chunk
-    uint32_t stages;
-    uint64_t crossover;     // latency kernel at or below this many bytes per rank
-    bool vector_copies;     // aligned copies stored by the consumer warps
-    int consumer_warps;     // 0: by plan (8 with reductions or shifted copies, else 4)
-};
+namespace purlin {
+namespace host {
 
 Policy policy_for(purlin_collective coll, int R) {
     auto clamp16 = [](uint64_t v, uint64_t lo, uint64_t hi) {
@@ -90,14 +62,6 @@ Policy composed_all_reduce_policy(int R) {
     return {chunk, 2, 8ull << 20, true, 12};
 }
 
-// Device memory behind one purlin_device_coll.
-struct DeviceCollMem {
-    Seg *segs = nullptr;
-    unsigned long long *flags = nullptr;
-    unsigned long long *epochs = nullptr;
-    unsigned long long *err = nullptr;
-};
-
 void free_device_coll(DeviceCollMem &m) {
     if (m.segs) cudaFree(m.segs);
     if (m.flags) cudaFree(m.flags);
@@ -106,46 +70,92 @@ void free_device_coll(DeviceCollMem &m) {
     m = DeviceCollMem{};
 }
 
-struct CacheEntry {
-    std::string key;
-    Plan plan;
-    Seg *segs_dev = nullptr;
-    bool pinned = false;   // used while a CUDA graph was captured: kept until finalize
-};
-
 bool capturing(cudaStream_t s) {
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     return cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone;
 }
+
+CallDesc make_desc(purlin_collective coll, int R, size_t n, const size_t *counts, int dtype,
+                   int op, purlin_layout layout) {
+    CallDesc c;
+    c.coll = coll;
+    c.R = R;
+    c.dtype = dtype;
+    c.n = n;
+    c.counts = counts;
+    c.op = op;
+    c.layout = layout;
+    return c;
+}
+
+purlin_status ring_shape(const purlin_ctx *ctx, const CallDesc &c, const Policy &shape,
+                         const Plan &pl, uint32_t limit, RingShape *out) {
+    RingShape r;
+    r.slot_stride = (pl.slot_bytes + 127u) & ~127u;
+    // Point-to-point copies at other 16-byte phases (ragged AllToAllV) go
+    // through the consumer warps: 6 warps and a deeper ring keep two CTAs
+    // per SM (measured +35% over 8 warps).
+    const bool shifted_p2p = pl.has_shifted_copies && !shape.vector_copies &&
+                             (c.coll == PURLIN_COLL_ALL_TO_ALL ||
+                              c.coll == PURLIN_COLL_ALL_TO_ALL_V);
+    uint32_t stages = (uint32_t)(ctx->opt[PURLIN_OPT_STAGES] > 0 ? ctx->opt[PURLIN_OPT_STAGES]
+                                 : shifted_p2p ? 4u : shape.stages);
+    stages = std::min<uint32_t>(32, std::max<uint32_t>(2, stages));
+    while (stages > 2 && throughput_smem(stages, r.slot_stride) > limit) --stages;
+    r.stages = stages;
+    r.smem = throughput_smem(stages, r.slot_stride);
+    if (r.smem > limit) return PURLIN_ERR_UNSUPPORTED;
+    r.vector_copies = ctx->opt[PURLIN_OPT_COPY_STORES] == 0 ? shape.vector_copies
+                                                            : ctx->opt[PURLIN_OPT_COPY_STORES] == 2;
+    r.consumer_warps = ctx->opt[PURLIN_OPT_CONSUMER_WARPS] > 0
+                           ? (int)ctx->opt[PURLIN_OPT_CONSUMER_WARPS]
+                       : shape.consumer_warps > 0 ? shape.consumer_warps
+                       : shifted_p2p ? kShiftedCopyConsumerWarps
+                       : pl.has_reduce || pl.has_shifted_copies ? kReduceConsumerWarps
+                                                                : kCopyConsumerWarps;
+    *out = r;
+    return PURLIN_OK;
+}
+
+// Per-parity flag slots for a grid of `grid` CTAs (a multiple of the grid,
+// so a slot is always reused by the CTA that owns its chunks) and the odd
+// epoch increment that keeps every generation of a call distinct.
+void flag_geometry(uint64_t notify_chunks, int64_t grid, uint32_t *slots, uint64_t *epoch_inc) {
+    *slots = (kFlagSlots / (uint32_t)grid) * (uint32_t)grid;
+    uint64_t gens = (notify_chunks + *slots - 1) / *slots;
+    if (gens == 0) gens = 1;
+    *epoch_inc = gens | 1ull;   // odd: the parity flips every call
+}
+
+// AllReduce mode for the ring: the packet mode (3) runs the ring's composed
+// mode where packets do not apply.
+int ring_ar_mode(const purlin_ctx *ctx) {
+    const int m = (int)ctx->opt[PURLIN_OPT_AR_MODE];
+    return m == 3 ? 2 : m;
+}
+
+Policy call_policy(const purlin_ctx *ctx, const CallDesc &c) {
+    return c.coll == PURLIN_COLL_ALL_REDUCE && ring_ar_mode(ctx) == 2
+               ? composed_all_reduce_policy(c.R)
+               : policy_for(c.coll, c.R);
+}
+
+}  // namespace host
+}  // namespace purlin
+
+namespace {
+
+constexpr size_t kPlanCacheCap = 64;
+
+// Built-in policy.
+constexpr int64_t kInspectChunkBytes = 32 * 1024;        // plan_inspect default chunk
+constexpr int kLatBlock = 256;
 
 int64_t env_or(const char *name, int64_t dflt) {
     const char *v = std::getenv(name);
     if (!v || !*v) return dflt;
     return std::strtoll(v, nullptr, 0);
 }
-
-}  // namespace
-
-struct purlin_ctx {
-    int R = 0;
-    cudaStream_t stream = nullptr;
-    int device = 0;
-    int sms = 0;
-    int max_smem = 0;
-    unsigned long long *flags = nullptr;   // 2 x kFlagSlots
-    unsigned char *packets = nullptr;      // 2 x kPacketStagingBytes (latency-path staging)
-    unsigned long long *err = nullptr;     // 4 words: error word, pad, device epoch {epoch, done}
-    unsigned long long *dev_epoch = nullptr;   // err + 2
-    uint64_t epoch = 1;   // host count of the increments calls applied (reported in
-                          // purlin_launch_info); the device epoch is the one kernels use
-    int64_t opt[kNumOptions] = {};
-    purlin_launch_info last = {};
-    std::list<CacheEntry> lru;
-    std::unordered_map<std::string, std::list<CacheEntry>::iterator> index;
-    std::list<DeviceCollMem> device_colls;   // memory of purlin_device_prepare descriptors
-};
-
-namespace {
 
 void append(std::string &k, const void *p, size_t n) { k.append(static_cast<const char *>(p), n); }
 
@@ -226,68 +236,6 @@ uint64_t message_bytes(const CallDesc &c) {
     uint64_t m = 0;
     for (int r = 0; r < c.R; ++r) m = std::max(m, in_b[r]);
     return m;
-}
-
-// Ring shape of a throughput launch: stages (reduced until the shared
-// memory fits `limit`), stage stride, consumer warps and copy stores.
-struct RingShape {
-    uint32_t stages = 0;
-    uint32_t slot_stride = 0;
-    uint32_t smem = 0;
-    int consumer_warps = 0;
-    bool vector_copies = false;
-};
-
-purlin_status ring_shape(const purlin_ctx *ctx, const CallDesc &c, const Policy &shape,
-                         const Plan &pl, uint32_t limit, RingShape *out) {
-    RingShape r;
-    r.slot_stride = (pl.slot_bytes + 127u) & ~127u;
-    // Point-to-point copies at other 16-byte phases (ragged AllToAllV) go
-    // through the consumer warps: 6 warps and a deeper ring keep two CTAs
-    // per SM (measured +35% over 8 warps).
-    const bool shifted_p2p = pl.has_shifted_copies && !shape.vector_copies &&
-                             (c.coll == PURLIN_COLL_ALL_TO_ALL ||
-                              c.coll == PURLIN_COLL_ALL_TO_ALL_V);
-    uint32_t stages = (uint32_t)(ctx->opt[PURLIN_OPT_STAGES] > 0 ? ctx->opt[PURLIN_OPT_STAGES]
-                                 : shifted_p2p ? 4u : shape.stages);
-    stages = std::min<uint32_t>(32, std::max<uint32_t>(2, stages));
-    while (stages > 2 && throughput_smem(stages, r.slot_stride) > limit) --stages;
-    r.stages = stages;
-    r.smem = throughput_smem(stages, r.slot_stride);
-    if (r.smem > limit) return PURLIN_ERR_UNSUPPORTED;
-    r.vector_copies = ctx->opt[PURLIN_OPT_COPY_STORES] == 0 ? shape.vector_copies
-                                                            : ctx->opt[PURLIN_OPT_COPY_STORES] == 2;
-    r.consumer_warps = ctx->opt[PURLIN_OPT_CONSUMER_WARPS] > 0
-                           ? (int)ctx->opt[PURLIN_OPT_CONSUMER_WARPS]
-                       : shape.consumer_warps > 0 ? shape.consumer_warps
-                       : shifted_p2p ? kShiftedCopyConsumerWarps
-                       : pl.has_reduce || pl.has_shifted_copies ? kReduceConsumerWarps
-                                                                : kCopyConsumerWarps;
-    *out = r;
-    return PURLIN_OK;
-}
-
-// Per-parity flag slots for a grid of `grid` CTAs (a multiple of the grid,
-// so a slot is always reused by the CTA that owns its chunks) and the odd
-// epoch increment that keeps every generation of a call distinct.
-void flag_geometry(uint64_t notify_chunks, int64_t grid, uint32_t *slots, uint64_t *epoch_inc) {
-    *slots = (kFlagSlots / (uint32_t)grid) * (uint32_t)grid;
-    uint64_t gens = (notify_chunks + *slots - 1) / *slots;
-    if (gens == 0) gens = 1;
-    *epoch_inc = gens | 1ull;   // odd: the parity flips every call
-}
-
-// AllReduce mode for the ring: the packet mode (3) runs the ring's composed
-// mode where packets do not apply.
-int ring_ar_mode(const purlin_ctx *ctx) {
-    const int m = (int)ctx->opt[PURLIN_OPT_AR_MODE];
-    return m == 3 ? 2 : m;
-}
-
-Policy call_policy(const purlin_ctx *ctx, const CallDesc &c) {
-    return c.coll == PURLIN_COLL_ALL_REDUCE && ring_ar_mode(ctx) == 2
-               ? composed_all_reduce_policy(c.R)
-               : policy_for(c.coll, c.R);
 }
 
 purlin_status run_packets(purlin_ctx *ctx, const CallDesc &c, const void *const src[],
@@ -451,115 +399,6 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
     return PURLIN_OK;
 }
 
-// A V collective whose counts are in device memory (vcounts.cu): the host
-// checks what it can (shape, pointers, the declared capacities' overlaps)
-// and sizes the ring for the worst case of any counts; the kernel derives
-// the displacements and checks the counts against the capacities.
-purlin_status run_vcounts(purlin_ctx *ctx, purlin_collective coll, const void *const src[],
-                          void *const dst[], const size_t *d_counts, size_t in_cap,
-                          size_t out_cap, int dtype, int op, purlin_layout layout) {
-    if (ctx == nullptr) return PURLIN_ERR_INVALID_ARG;
-    CallDesc c;
-    c.coll = coll;
-    c.R = ctx->R;
-    c.dtype = dtype;
-    c.n = 0;
-    c.counts = nullptr;
-    c.op = op;
-    c.layout = layout;
-    purlin_status st = validate_shape(c, src, dst);
-    if (st != PURLIN_OK) return st;
-    if (c.R > kVcMaxRanks) return PURLIN_ERR_UNSUPPORTED;
-    if (d_counts == nullptr || ((uintptr_t)d_counts & 7u) != 0) return PURLIN_ERR_INVALID_ARG;
-    const uint64_t es = (uint64_t)elem_bytes(dtype);
-    if (in_cap > (1ull << 44) || out_cap > (1ull << 44)) return PURLIN_ERR_INVALID_ARG;
-    std::vector<uint64_t> in_b((size_t)c.R, in_cap * es), out_b((size_t)c.R, out_cap * es);
-    st = validate_extents(c, src, dst, in_b, out_b);
-    if (st != PURLIN_OK) return st;
-
-    const Policy shape = policy_for(coll, c.R);
-    const int64_t chunk_opt = ctx->opt[PURLIN_OPT_CHUNK_BYTES];
-    const uint32_t chunk = (uint32_t)(chunk_opt > 0 ? chunk_opt : shape.chunk) & ~15u;
-    const bool reduce = coll == PURLIN_COLL_REDUCE_SCATTER_V;
-    // Any count may put a source at another 16-byte phase: room for the hull.
-    const uint32_t slot = reduce ? (chunk + 16u) * (uint32_t)c.R : chunk + 16u;
-    const uint32_t slot_stride = (slot + 127u) & ~127u;
-    // AllToAllV: 3 stages and 6 consumer warps (two CTAs per SM) measured
-    // best for both 16-byte aligned counts (the MoE dispatch: equal to the
-    // host-count call) and ragged ones (Zipf V split: 4% faster than it).
-    uint32_t stages = (uint32_t)(ctx->opt[PURLIN_OPT_STAGES] > 0 ? ctx->opt[PURLIN_OPT_STAGES]
-                                                                 : shape.stages);
-    stages = std::min<uint32_t>(32, std::max<uint32_t>(2, stages));
-    const uint32_t limit = (uint32_t)ctx->max_smem - 1024;
-    while (stages > 2 && vcounts_smem(coll, c.R, stages, slot_stride) > limit) --stages;
-    const uint32_t smem = vcounts_smem(coll, c.R, stages, slot_stride);
-    if (smem > limit) return PURLIN_ERR_UNSUPPORTED;
-    const int cw = ctx->opt[PURLIN_OPT_CONSUMER_WARPS] > 0 ? (int)ctx->opt[PURLIN_OPT_CONSUMER_WARPS]
-                   : shape.consumer_warps > 0 ? shape.consumer_warps
-                   : coll == PURLIN_COLL_ALL_TO_ALL_V ? kShiftedCopyConsumerWarps
-                                                      : kReduceConsumerWarps;
-    const int block = 32 * (2 + cw);
-    int per_sm = 0;
-    if (vcounts_occupancy(dtype, c.R, block, smem, &per_sm) != cudaSuccess || per_sm < 1)
-        return PURLIN_ERR_UNSUPPORTED;
-
-    VcLaunch a;
-    a.src = src;
-    a.dst = dst;
-    a.counts = reinterpret_cast<const unsigned long long *>(d_counts);
-    a.err = ctx->err;
-    a.in_cap = in_cap;
-    a.out_cap = out_cap;
-    const int64_t variant = ctx->opt[PURLIN_OPT_VARIANT];
-    a.crossover = variant == kVariantLatency      ? ~0ull
-                  : variant == kVariantThroughput ? 0ull
-                  : ctx->opt[PURLIN_OPT_CROSSOVER_BYTES] > 0
-                      ? (uint64_t)ctx->opt[PURLIN_OPT_CROSSOVER_BYTES]
-                      : shape.crossover;
-    a.timeout_ns = ctx->opt[PURLIN_OPT_SPIN_TIMEOUT_NS] > 0 ? ctx->opt[PURLIN_OPT_SPIN_TIMEOUT_NS]
-                                                            : kDefaultTimeoutNs;
-    a.red_chunk = chunk;
-    a.copy_chunk = chunk;
-    a.stages = stages;
-    a.slot_stride = slot_stride;
-    a.R = c.R;
-    a.coll = coll;
-    a.dtype = dtype;
-    a.vector_copies = ctx->opt[PURLIN_OPT_COPY_STORES] == 0 ? shape.vector_copies
-                                                            : ctx->opt[PURLIN_OPT_COPY_STORES] == 2;
-    int64_t grid = (int64_t)ctx->sms * per_sm;
-    if (ctx->opt[PURLIN_OPT_CTAS] > 0) grid = std::min<int64_t>(grid, ctx->opt[PURLIN_OPT_CTAS]);
-    a.grid = (int)grid;
-    a.block = block;
-    a.smem = smem;
-    a.stream = ctx->stream;
-    if (launch_vcounts(a) != cudaSuccess) return PURLIN_ERR_CUDA;
-    purlin_launch_info info = {};
-    info.variant = 4;   // decided on the device from the counts
-    info.grid = a.grid;
-    info.block = a.block;
-    info.stages = (int32_t)stages;
-    info.chunk_bytes = chunk;
-    info.segments = coll == PURLIN_COLL_ALL_TO_ALL_V ? (int64_t)c.R * c.R : c.R;
-    info.smem_bytes = smem;
-    info.epoch = info.epoch_next = ctx->epoch;
-    ctx->last = info;
-    return PURLIN_OK;
-}
-
-CallDesc make_desc(purlin_collective coll, int R, size_t n, const size_t *counts, int dtype,
-                   int op, purlin_layout layout) {
-    CallDesc c;
-    c.coll = coll;
-    c.R = R;
-    c.dtype = dtype;
-    c.n = n;
-    c.counts = counts;
-    c.op = op;
-    c.layout = layout;
-    return c;
-}
-
 }  // namespace
 
 extern "C" {
@@ -692,33 +531,6 @@ purlin_status purlin_all_to_all_v(purlin_ctx *ctx, const void *const src[], void
                src, dst);
 }
 
-purlin_status purlin_all_gather_v_device_counts(purlin_ctx *ctx, const void *const src[],
-                                                void *const dst[], const size_t counts[],
-                                                size_t in_capacity, size_t out_capacity,
-                                                purlin_dtype dtype, purlin_op op,
-                                                purlin_layout layout) {
-    return run_vcounts(ctx, PURLIN_COLL_ALL_GATHER_V, src, dst, counts, in_capacity,
-                       out_capacity, dtype, op, layout);
-}
-
-purlin_status purlin_reduce_scatter_v_device_counts(purlin_ctx *ctx, const void *const src[],
-                                                    void *const dst[], const size_t counts[],
-                                                    size_t in_capacity, size_t out_capacity,
-                                                    purlin_dtype dtype, purlin_op op,
-                                                    purlin_layout layout) {
-    return run_vcounts(ctx, PURLIN_COLL_REDUCE_SCATTER_V, src, dst, counts, in_capacity,
-                       out_capacity, dtype, op, layout);
-}
-
-purlin_status purlin_all_to_all_v_device_counts(purlin_ctx *ctx, const void *const src[],
-                                                void *const dst[], const size_t counts[],
-                                                size_t in_capacity, size_t out_capacity,
-                                                purlin_dtype dtype, purlin_op op,
-                                                purlin_layout layout) {
-    return run_vcounts(ctx, PURLIN_COLL_ALL_TO_ALL_V, src, dst, counts, in_capacity,
-                       out_capacity, dtype, op, layout);
-}
-
 purlin_status purlin_empty_launch(purlin_stream stream) {
     return launch_empty(static_cast<cudaStream_t>(stream)) == cudaSuccess ? PURLIN_OK
                                                                           : PURLIN_ERR_CUDA;
@@ -838,134 +650,5 @@ purlin_status purlin_plan_inspect(purlin_collective coll, int R, const void *con
     }
     return PURLIN_OK;
 }
-
-purlin_status purlin_device_prepare(purlin_ctx *ctx, purlin_collective coll,
-                                    const void *const src[], void *const dst[], size_t n,
-                                    const size_t counts[], purlin_dtype dtype, purlin_op op,
-                                    purlin_layout layout, int blocks,
-                                    uint32_t max_workspace_bytes, purlin_device_coll *out) {
-    if (ctx == nullptr || out == nullptr) return PURLIN_ERR_INVALID_ARG;
-    if ((int)coll < 0 || (int)coll > (int)PURLIN_COLL_ALL_TO_ALL_V) return PURLIN_ERR_INVALID_ARG;
-    if (blocks < 1 || blocks > 65535) return PURLIN_ERR_INVALID_ARG;
-    const bool is_v = coll == PURLIN_COLL_ALL_GATHER_V || coll == PURLIN_COLL_REDUCE_SCATTER_V ||
-                      coll == PURLIN_COLL_ALL_TO_ALL_V;
-    const CallDesc c = make_desc(coll, ctx->R, is_v ? 0 : n, is_v ? counts : nullptr, dtype, op,
-                                 layout);
-    purlin_status st = validate_call(c, src, dst);
-    if (st != PURLIN_OK) return st;
-
-    // The launch's CTA budget for the workspace: the caller's cap, else the
-    // device maximum less room for the kernel's own static shared memory.
-    const uint32_t dev_limit = (uint32_t)ctx->max_smem - 4096u;
-    const uint32_t limit = max_workspace_bytes ? std::min(max_workspace_bytes, dev_limit) : dev_limit;
-    const uint32_t ctl_bytes = 128;   // snac::Ctl, padded to the workspace alignment
-    if (limit <= ctl_bytes) return PURLIN_ERR_UNSUPPORTED;
-
-    const Policy shape = call_policy(ctx, c);
-    const int64_t chunk_opt = ctx->opt[PURLIN_OPT_CHUNK_BYTES];
-    uint32_t chunk = (uint32_t)(chunk_opt > 0 ? chunk_opt : shape.chunk);
-    Plan pl;
-    RingShape rs;
-    for (;;) {   // halve the chunk until the ring fits the cap
-        st = compile_plan(c, kVariantThroughput, ring_ar_mode(ctx), chunk * (uint32_t)c.R, chunk,
-                          &pl);
-        if (st != PURLIN_OK) return st;
-        st = ring_shape(ctx, c, shape, pl, limit - ctl_bytes, &rs);
-        if (st == PURLIN_OK) break;
-        if (st != PURLIN_ERR_UNSUPPORTED || chunk <= 256) return st;
-        chunk = std::max<uint32_t>(256, (chunk / 2) & ~15u);
-    }
-    if (pl.composed && pl.notify_chunks > (uint64_t)kFlagSlots * 0xFFFFull)
-        return PURLIN_ERR_INVALID_ARG;
-
-    purlin_device_coll d;
-    std::memset(&d, 0, sizeof d);
-    for (int r = 0; r < c.R; ++r) {
-        d.src[r] = src[r];
-        d.dst[r] = dst[r];
-    }
-    d.nchunks = pl.nchunks;
-    d.nunits = pl.nunits;
-    d.epoch_inc = 1;
-    d.timeout_ns = ctx->opt[PURLIN_OPT_SPIN_TIMEOUT_NS] > 0 ? ctx->opt[PURLIN_OPT_SPIN_TIMEOUT_NS]
-                                                            : kDefaultTimeoutNs;
-    d.drop_notify = ctx->opt[PURLIN_OPT_DROP_NOTIFY];
-    d.flag_slots = 1;
-    d.stages = rs.stages;
-    d.slot_stride = rs.slot_stride;
-    d.workspace_bytes = rs.smem + ctl_bytes;
-    d.nseg = (int32_t)pl.segs.size();
-    d.R = c.R;
-    d.dtype = dtype;
-    d.vector_copies = rs.vector_copies ? 1 : 0;
-    d.blocks = blocks;
-    d.threads = 32 * (2 + rs.consumer_warps);
-    d.composed = pl.composed ? 1 : 0;
-    d.coll = coll;
-
-    DeviceCollMem m;
-    auto fail = [&](purlin_status s) {
-        free_device_coll(m);
-        return s;
-    };
-    const size_t seg_bytes = std::max<size_t>(1, pl.segs.size()) * sizeof(Seg);
-    if (cudaMalloc(&m.segs, seg_bytes) != cudaSuccess ||
-        cudaMalloc(&m.epochs, (size_t)blocks * sizeof(unsigned long long)) != cudaSuccess ||
-        cudaMalloc(&m.err, sizeof(unsigned long long)) != cudaSuccess)
-        return fail(PURLIN_ERR_OOM);
-    if (pl.composed) {
-        flag_geometry(pl.notify_chunks, blocks, &d.flag_slots, &d.epoch_inc);
-        if (cudaMalloc(&m.flags, 2 * (size_t)d.flag_slots * sizeof(unsigned long long)) !=
-            cudaSuccess)
-            return fail(PURLIN_ERR_OOM);
-        if (cudaMemset(m.flags, 0, 2 * (size_t)d.flag_slots * sizeof(unsigned long long)) !=
-            cudaSuccess)
-            return fail(PURLIN_ERR_CUDA);
-    }
-    // Every CTA starts at epoch 1: flags start at 0, below any epoch.
-    std::vector<unsigned long long> ep((size_t)blocks, 1ull);
-    if ((!pl.segs.empty() &&
-         cudaMemcpy(m.segs, pl.segs.data(), pl.segs.size() * sizeof(Seg),
-                    cudaMemcpyHostToDevice) != cudaSuccess) ||
-        cudaMemcpy(m.epochs, ep.data(), ep.size() * sizeof(unsigned long long),
-                   cudaMemcpyHostToDevice) != cudaSuccess ||
-        cudaMemset(m.err, 0, sizeof(unsigned long long)) != cudaSuccess)
-        return fail(PURLIN_ERR_CUDA);
-    d.segs = m.segs;
-    d.flags = m.flags;
-    d.epochs = m.epochs;
-    d.err = m.err;
-    ctx->device_colls.push_back(m);
-    d.owner = &ctx->device_colls.back();
-    *out = d;
-    return PURLIN_OK;
-}
-
-purlin_status purlin_device_check(const purlin_device_coll *coll, purlin_stream stream) {
-    if (coll == nullptr || coll->err == nullptr) return PURLIN_ERR_INVALID_ARG;
-    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return PURLIN_ERR_CUDA;
-    unsigned long long word = 0;
-    if (cudaMemcpy(&word, coll->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
-        return PURLIN_ERR_CUDA;
-    if (word == 0) return PURLIN_OK;
-    if (cudaMemset(coll->err, 0, sizeof word) != cudaSuccess) return PURLIN_ERR_CUDA;
-    return static_cast<purlin_status>(word & 0xFF);
-}
-
-purlin_status purlin_device_release(purlin_ctx *ctx, purlin_device_coll *coll) {
-    if (ctx == nullptr || coll == nullptr) return PURLIN_ERR_INVALID_ARG;
-    if (coll->owner == nullptr) return PURLIN_OK;
-    for (auto it = ctx->device_colls.begin(); it != ctx->device_colls.end(); ++it) {
-        if (&*it != coll->owner) continue;
-        free_device_coll(*it);
-        ctx->device_colls.erase(it);
-        std::memset(coll, 0, sizeof *coll);
-        return PURLIN_OK;
-    }
-    return PURLIN_ERR_INVALID_ARG;
-}
-
-size_t purlin_device_coll_size(void) { return sizeof(purlin_device_coll); }
 
 }  // extern "C"

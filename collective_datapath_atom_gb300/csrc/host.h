@@ -1,0 +1,119 @@
+// host.h -- what the host-side translation units of the C ABI share: the
+// context, the plan cache entry, the codesign policy and the ring shaping.
+// Internal to the library (not part of include/).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <list>
+#include <string>
+#include <unordered_map>
+
+#include "launch.h"
+#include "plan.h"
+
+namespace purlin {
+namespace host {
+
+constexpr int kNumOptions = 12;
+constexpr int64_t kDefaultTimeoutNs = 100 * 1000 * 1000;   // 100 ms
+constexpr int kCopyConsumerWarps = 4;
+constexpr int kReduceConsumerWarps = 8;
+constexpr int kShiftedCopyConsumerWarps = 6;
+
+// Policy per collective (codesign policy, "Purlin: Separating Orchestration
+// from the Datapath of Collectives" §4.2), measured on GB300 over 256 B..64
+// MiB per rank and at the workloads' sizes.
+// Crossover: per-rank message bytes up to which the one-shot vector kernel
+// beats the staged ring (it keeps ~150k threads' loads in flight, so for
+// reductions it stays competitive up to several MiB).
+// Ring shape:
+//   ReduceScatter(V)  one destination per reduced chunk: large per-source
+//                     chunks (96 KiB per stage), 2 stages;
+//   AllReduce         R stores per reduced vector: 32 KiB per stage, 3 stages;
+//   AllGather(V)      one staged tile written to R destinations: 16 KiB
+//                     chunks, 4 stages, and the 8 consumer warps store the
+//                     tile with 128-bit stores (0.956 of the copy peak versus
+//                     0.92 with bulk stores from one warp);
+//   AllToAll(V)       one load, one store per chunk: 16 KiB chunks, 3 stages,
+//                     bulk stores (0.98).
+struct Policy {
+    uint32_t chunk;         // bytes per source per chunk
+    uint32_t stages;
+    uint64_t crossover;     // latency kernel at or below this many bytes per rank
+    bool vector_copies;     // aligned copies stored by the consumer warps
+    int consumer_warps;     // 0: by plan (8 with reductions or shifted copies, else 4)
+};
+
+Policy policy_for(purlin_collective coll, int R);
+
+// Composed AllReduce's ring shape (see api.cpp).
+Policy composed_all_reduce_policy(int R);
+
+// Device memory behind one purlin_device_coll.
+struct DeviceCollMem {
+    Seg *segs = nullptr;
+    unsigned long long *flags = nullptr;
+    unsigned long long *epochs = nullptr;
+    unsigned long long *err = nullptr;
+};
+
+void free_device_coll(DeviceCollMem &m);
+
+struct CacheEntry {
+    std::string key;
+    Plan plan;
+    Seg *segs_dev = nullptr;
+    bool pinned = false;   // used while a CUDA graph was captured: kept until finalize
+};
+
+// True while a CUDA graph is being captured from stream s.
+bool capturing(cudaStream_t s);
+
+CallDesc make_desc(purlin_collective coll, int R, size_t n, const size_t *counts, int dtype,
+                   int op, purlin_layout layout);
+
+// Ring shape of a throughput launch: stages (reduced until the shared
+// memory fits `limit`), stage stride, consumer warps and copy stores.
+struct RingShape {
+    uint32_t stages = 0;
+    uint32_t slot_stride = 0;
+    uint32_t smem = 0;
+    int consumer_warps = 0;
+    bool vector_copies = false;
+};
+
+}  // namespace host
+}  // namespace purlin
+
+struct purlin_ctx {
+    int R = 0;
+    cudaStream_t stream = nullptr;
+    int device = 0;
+    int sms = 0;
+    int max_smem = 0;
+    unsigned long long *flags = nullptr;   // 2 x kFlagSlots
+    unsigned char *packets = nullptr;      // 2 x kPacketStagingBytes (latency-path staging)
+    unsigned long long *err = nullptr;     // 4 words: error word, pad, device epoch {epoch, done}
+    unsigned long long *dev_epoch = nullptr;   // err + 2
+    uint64_t epoch = 1;   // host count of the increments calls applied (reported in
+                          // purlin_launch_info); the device epoch is the one kernels use
+    int64_t opt[purlin::host::kNumOptions] = {};
+    purlin_launch_info last = {};
+    std::list<purlin::host::CacheEntry> lru;
+    std::unordered_map<std::string, std::list<purlin::host::CacheEntry>::iterator> index;
+    std::list<purlin::host::DeviceCollMem> device_colls;   // memory of purlin_device_prepare descriptors
+};
+
+namespace purlin {
+namespace host {
+
+purlin_status ring_shape(const purlin_ctx *ctx, const CallDesc &c, const Policy &shape,
+                         const Plan &pl, uint32_t limit, RingShape *out);
+void flag_geometry(uint64_t notify_chunks, int64_t grid, uint32_t *slots, uint64_t *epoch_inc);
+int ring_ar_mode(const purlin_ctx *ctx);
+Policy call_policy(const purlin_ctx *ctx, const CallDesc &c);
+
+}  // namespace host
+}  // namespace purlin
