@@ -6,9 +6,14 @@ A step is one collective call over inputs already resident in HBM.
 
 Metric: effective HBM GB/s = (bytes every rank buffer must read + bytes every
 rank buffer must write) / device time.  Timing: W warm-up steps, then K
-steps, each bracketed by CUDA events on the library's stream, with an L2
-flush (a 512 MiB write) between steps outside the events; barrier +
-synchronize around the whole timed loop; max over ranks.
+steps on the library's stream, timed with CUDA events.  When the step's
+inputs are larger than the L2 the device reports (the ReduceScatter and
+AllToAllV workloads), the K steps run back to back between one pair of
+events, since no input can survive in L2 from one step to the next;
+otherwise (the default AllGather: 128 MiB of inputs) every step has its own
+events and an L2 flush (a 512 MiB write) comes before it, outside the events
+(``--flush`` forces this mode).  Barrier + synchronize around the whole timed
+loop; max over ranks.
 
 Extra keys: ``roofline`` (the throughput kernel against the measured HBM
 copy bandwidth), ``cpu_baseline`` (the CPU oracle on a bounded sample),
@@ -343,8 +348,23 @@ def whole_job_gbs(bytes_per_step_per_rank: int, steps: int, world: int, slowest_
 
 # ------------------------------------------------------------ GPU arm ----
 
-def time_steps(torch, stream, run, src, dst, steps, flush_buf, events_out):
-    """Per-step CUDA events on `stream`, L2 flushed between steps."""
+def time_steps(torch, stream, run, src, dst, steps, flush_buf, events_out, back_to_back=False):
+    """Per-step device time in ms.  back_to_back (inputs larger than L2): the
+    steps run one after another between one pair of CUDA events on `stream`
+    and each gets the average; otherwise every step has its own events and
+    the L2 is flushed (a 512 MiB write) before it, outside the events."""
+    if back_to_back:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                run(src, dst)
+            e1.record(stream)
+        stream.synchronize()
+        ms = [e0.elapsed_time(e1) / steps] * steps
+        events_out.extend(ms)
+        return ms
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     with torch.cuda.stream(stream):
@@ -410,7 +430,14 @@ def run_gpu(args, rank, world, local_rank):
         dist.barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    ms = time_steps(torch, stream, run, src, dst, args.steps, flush_buf, [])
+    # Inputs larger than the L2 cannot carry over from one step to the next
+    # (each step also writes its outputs through L2), so such workloads run
+    # back to back; smaller ones get the L2 flushed before every step.
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0) or 0)
+    back_to_back = (not args.flush) and l2_bytes > 0 and in_bytes > l2_bytes
+    l2_note = (f"not flushed: inputs ({in_bytes} B) larger than L2 ({l2_bytes} B), steps back to back"
+               if back_to_back else f"flushed between steps (512 MiB write; L2 {l2_bytes} B)")
+    ms = time_steps(torch, stream, run, src, dst, args.steps, flush_buf, [], back_to_back)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -487,7 +514,7 @@ def run_gpu(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == 1 else "f32",
         "data": "synthetic",
         "config": {"workload": w.name, "R": w.R, "elements_per_rank": w.n,
-                   "algorithmic_bytes_per_step": algo_bytes, "l2": "flushed between steps",
+                   "algorithmic_bytes_per_step": algo_bytes, "l2": l2_note,
                    "variant": info["variant"], "grid": info["grid"], "block": info["block"],
                    "stages": info["stages"], "chunk_bytes": info["chunk_bytes"],
                    "parallelism": f"replicas x{world}",
@@ -760,6 +787,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--flush", action="store_true",
+                    help="flush L2 before every timed step even when the inputs exceed it")
     ap.add_argument("--device-counts", action="store_true",
                     help="AllToAllV workload: counts in device memory (the device-count call)")
     ap.add_argument("--elements", type=int, default=0,
