@@ -36,19 +36,22 @@ Policy policy_for(purlin_collective coll, int R) {
     auto clamp16 = [](uint64_t v, uint64_t lo, uint64_t hi) {
         return (uint32_t)(std::min(hi, std::max(lo, v)) & ~uint64_t(15));
     };
+    // Crossovers: the largest per-rank input the vector kernel wins at,
+    // measured with each variant forced (single launches, 4 KiB..32 MiB).
     switch (coll) {
         case PURLIN_COLL_REDUCE_SCATTER:
-        case PURLIN_COLL_REDUCE_SCATTER_V:
-            return {clamp16(98304 / (uint64_t)R, 1024, 16384), 2, 8ull << 20, false, 0};
+            return {clamp16(98304 / (uint64_t)R, 1024, 16384), 2, 32ull << 20, false, 0, 1};
+        case PURLIN_COLL_REDUCE_SCATTER_V:   // ragged blocks: the ring from 16 MiB
+            return {clamp16(98304 / (uint64_t)R, 1024, 16384), 2, 8ull << 20, false, 0, 1};
         case PURLIN_COLL_ALL_REDUCE:
             // (composed mode: the gather chunks are stored by the consumer warps)
-            return {clamp16(32768 / (uint64_t)R, 512, 8192), 3, 8ull << 20, true, 0};
+            return {clamp16(32768 / (uint64_t)R, 512, 8192), 3, 32ull << 20, true, 0, 1};
         case PURLIN_COLL_ALL_GATHER:
-            return {16384, 4, 128ull << 10, true, 8};
+            return {16384, 4, 1ull << 20, true, 8, 1};
         case PURLIN_COLL_ALL_GATHER_V:
-            return {16384, 4, 1ull << 20, true, 8};
-        default:
-            return {16384, 3, 128ull << 10, false, 0};
+            return {16384, 4, 2ull << 20, true, 8, 1};
+        default:   // AllToAll(V): two CTAs per SM
+            return {16384, 3, 256ull << 10, false, 0, 2};
     }
 }
 
@@ -59,7 +62,7 @@ Policy policy_for(purlin_collective coll, int R) {
 // against 4.07 TB/s with the fused AllReduce's 4 KiB x 3-stage ring.
 Policy composed_all_reduce_policy(int R) {
     const uint32_t chunk = (uint32_t)std::max<uint64_t>(512, (98304 / (uint64_t)R) & ~uint64_t(15));
-    return {chunk, 2, 8ull << 20, true, 12};
+    return {chunk, 2, 8ull << 20, true, 12, 1};
 }
 
 void free_device_coll(DeviceCollMem &m) {
@@ -366,7 +369,7 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
         if (throughput_occupancy(c.dtype, pclass, block, smem, &per_sm) != cudaSuccess ||
             per_sm < 1)
             return PURLIN_ERR_UNSUPPORTED;
-        int64_t grid = (int64_t)ctx->sms * per_sm;
+        int64_t grid = (int64_t)ctx->sms * std::min(per_sm, std::max(1, shape.ctas_per_sm));
         if (ctx->opt[PURLIN_OPT_CTAS] > 0) grid = std::min<int64_t>(grid, ctx->opt[PURLIN_OPT_CTAS]);
         int64_t work = (int64_t)std::max<uint64_t>(pl.nchunks, (pl.nunits + 255) / 256);
         grid = std::max<int64_t>(1, std::min<int64_t>(grid, work));

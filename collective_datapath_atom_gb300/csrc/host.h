@@ -26,8 +26,10 @@ constexpr int kShiftedCopyConsumerWarps = 6;
 // from the Datapath of Collectives" §4.2), measured on GB300 over 256 B..64
 // MiB per rank and at the workloads' sizes.
 // Crossover: per-rank message bytes up to which the one-shot vector kernel
-// beats the staged ring (it keeps ~150k threads' loads in flight, so for
-// reductions it stays competitive up to several MiB).
+// beats the staged ring.  At 64 registers it runs four CTAs of 256 threads
+// per SM, which keeps enough loads in flight that for reductions it wins up
+// to tens of MiB: AllReduce and ReduceScatter 32 MiB, ReduceScatterV 8 MiB,
+// AllGather 1 MiB, AllGatherV 2 MiB, AllToAll(V) 256 KiB.
 // Ring shape:
 //   ReduceScatter(V)  one destination per reduced chunk: large per-source
 //                     chunks (96 KiB per stage), 2 stages;
@@ -44,6 +46,8 @@ struct Policy {
     uint64_t crossover;     // latency kernel at or below this many bytes per rank
     bool vector_copies;     // aligned copies stored by the consumer warps
     int consumer_warps;     // 0: by plan (8 with reductions or shifted copies, else 4)
+    int ctas_per_sm;        // the ring's CTAs per SM the shape was tuned at (the
+                            // occupancy limit when lower)
 };
 
 Policy policy_for(purlin_collective coll, int R);

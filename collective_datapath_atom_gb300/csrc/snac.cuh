@@ -134,8 +134,12 @@ __device__ __forceinline__ bool error_set(const unsigned long long *err) {
 // ------------------------------------------------------------ vector unit --
 
 // One 16-byte destination window of a segment: copy or reduce it to every
-// destination.  A full window whose source is 16-byte aligned uses 128-bit
-// accesses; anything else goes element by element.
+// destination.  The window's source bytes (all 16, or the 1..15 of a partial
+// head or tail window) are fetched with at most two aligned 128-bit loads
+// per source, each holding at least one of those bytes (so no load leaves
+// the source buffer's 16-byte granules), and shifted into place; sums use
+// the vector code on all 16 bytes, and a partial window stores only its own
+// elements.
 template <int DT, int MAXR, class P>
 __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
     using V = atom::Vec<DT>;
@@ -156,110 +160,82 @@ __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
         hi = (b < e ? b : e) - sg.dst_off;
     }
     const int R = p.R;
-    // A full destination window is written with one 128-bit store.  Its 16
-    // source bytes are one aligned vector (same phase), or two aligned
-    // vectors shifted into place when both lie inside the segment's source
-    // range (so no byte outside the segment is read); else element by element.
-    const bool full = hi - lo == 16;
+    const uint32_t nb = (uint32_t)(hi - lo);   // 1..16 bytes of this window
     const uint64_t sx = sg.src_off + lo;
     const uint32_t sh = (uint32_t)(sx & 15u);
-    const uint64_t sxa = sx - sh;
-    const bool vec = full && sh == 0;
-    const bool shifted = full && sh != 0 && sxa >= sg.src_off && sxa + 32 <= sg.src_off + sg.bytes;
+    const bool two = sh + nb > 16u;            // the bytes straddle two aligned vectors
     const uint64_t doff = sg.dst_off + lo;
 
-    if (sg.src_rank >= 0) {   // copy, bitwise
-        const char *s = static_cast<const char *>(sg.src_is_dst ? p.dst[sg.src_rank]
-                                                                : p.src[sg.src_rank]) +
-                        sg.src_off + lo;
-        // Read the window once (16 bytes, as a vector or element by element),
-        // then write it to every destination.
-        constexpr int NE = 16 / ES;
-        const int ne = (int)((hi - lo) / ES);
-        uint4 v = make_uint4(0, 0, 0, 0);
-        uint32_t e[NE];
-        if (vec) {
-            v = atom::ld_v4(s);
-        } else if (shifted) {
-            const char *a = s - sh;
-            v = atom::shift_pair(atom::ld_v4_l1(a), atom::ld_v4_l1(a + 16), sh);
-        } else {
-#pragma unroll
-            for (int j = 0; j < NE; ++j)
-                e[j] = j < ne ? (ES == 4 ? *reinterpret_cast<const uint32_t *>(s + j * ES)
-                                         : *reinterpret_cast<const uint16_t *>(s + j * ES))
-                              : 0u;
+    // The window's source bytes in the buffer that starts at `base` (the rank
+    // buffer itself: sx is the window's offset in it), in the low bytes of a
+    // vector.
+    auto fetch = [&](const char *base) -> uint4 {
+        const char *a = base + (sx - sh);
+        if (sh == 0) return atom::ld_v4(a);
+        const uint4 v0 = atom::ld_v4_l1(a);
+        return atom::shift_pair(v0, two ? atom::ld_v4_l1(a + 16) : v0, sh);
+    };
+    // Store the window's nb bytes of v at d: one 128-bit store when full.
+    auto put = [&](char *d, const uint4 &v) {
+        if (nb == 16u) {
+            atom::st_v4(d, v);
+            return;
         }
-        auto put = [&](char *d) {
-            if (d == s) return;   // in-place AllGather: the block is already there
-            if (vec || shifted) {
-                atom::st_v4(d, v);
-            } else {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                for (int j = 0; j < NE; ++j) {
-                    if (j >= ne) break;
-                    if (ES == 4) *reinterpret_cast<uint32_t *>(d + j * ES) = e[j];
-                    else *reinterpret_cast<uint16_t *>(d + j * ES) = (uint16_t)e[j];
-                }
-            }
-        };
+        for (int j = 0; j < 16 / ES; ++j) {
+            if ((uint32_t)(j * ES) >= nb) break;
+            const uint32_t word = w[(j * ES) >> 2];
+            if (ES == 4) *reinterpret_cast<uint32_t *>(d + j * ES) = word;
+            else *reinterpret_cast<uint16_t *>(d + j * ES) = (uint16_t)(word >> (8 * ((j * ES) & 3)));
+        }
+    };
+
+    if (sg.src_rank >= 0) {   // copy, bitwise
+        const char *sbase = static_cast<const char *>(sg.src_is_dst ? p.dst[sg.src_rank]
+                                                                    : p.src[sg.src_rank]);
+        const uint4 v = fetch(sbase);
+        const char *self = sbase + sx;   // in-place AllGather: the block is already there
         if (sg.dst_rank >= 0) {
-            put(static_cast<char *>(p.dst[sg.dst_rank]) + doff);
+            char *d = static_cast<char *>(p.dst[sg.dst_rank]) + doff;
+            if (d != self) put(d, v);
         } else {
-            for (int d = 0; d < R; ++d)
-                if (d != sg.skip_rank) put(static_cast<char *>(p.dst[d]) + doff);
+            for (int r = 0; r < R; ++r) {
+                if (r == sg.skip_rank) continue;
+                char *d = static_cast<char *>(p.dst[r]) + doff;
+                if (d != self) put(d, v);
+            }
         }
         return;
     }
 
-    // reduce (SCORE): rank order 0..R-1, binary32, one rounding at the end
-    const uint64_t soff = sg.src_off + lo;
-    if (vec || shifted) {
-        // source j's 16 bytes: one aligned vector, or two shifted into place
-        auto load = [&](int j) -> uint4 {
-            const char *b = static_cast<const char *>(p.src[j]) + soff;
-            if (vec) return atom::ld_v4(b);
-            return atom::shift_pair(atom::ld_v4_l1(b - sh), atom::ld_v4_l1(b - sh + 16), sh);
-        };
-        float acc[V::VE];
-        uint4 v[8];
+    // reduce (SCORE): rank order 0..R-1, binary32, one rounding at the end.
+    // Bytes past a partial window's end are summed too and never stored.
+    float acc[V::VE];
+    uint4 v[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (j < R) v[j] = load(j);
-        V::init(acc, v[0]);
+    for (int j = 0; j < 8; ++j)
+        if (j < R) v[j] = fetch(static_cast<const char *>(p.src[j]));
+    V::init(acc, v[0]);
 #pragma unroll
-        for (int j = 1; j < 8; ++j)
-            if (j < R) V::add(acc, v[j]);
-        if (MAXR > 8) {
-            for (int s0 = 8; s0 < R; s0 += 8) {
+    for (int j = 1; j < 8; ++j)
+        if (j < R) V::add(acc, v[j]);
+    if (MAXR > 8) {
+        for (int s0 = 8; s0 < R; s0 += 8) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (s0 + j < R) v[j] = load(s0 + j);
+            for (int j = 0; j < 8; ++j)
+                if (s0 + j < R) v[j] = fetch(static_cast<const char *>(p.src[s0 + j]));
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (s0 + j < R) V::add(acc, v[j]);
-            }
+            for (int j = 0; j < 8; ++j)
+                if (s0 + j < R) V::add(acc, v[j]);
         }
-        const uint4 out = V::pack(acc);
-        if (sg.dst_rank >= 0) {
-            atom::st_v4(static_cast<char *>(p.dst[sg.dst_rank]) + doff, out);
-        } else {
-            for (int d = 0; d < R; ++d)
-                if (d != sg.skip_rank) atom::st_v4(static_cast<char *>(p.dst[d]) + doff, out);
-        }
-        return;
     }
-    for (uint64_t j = 0; j < hi - lo; j += ES) {
-        float acc = atom::load_elem<DT>(static_cast<const char *>(p.src[0]) + soff + j);
-        for (int s = 1; s < R; ++s)
-            acc = __fadd_rn(acc, atom::load_elem<DT>(static_cast<const char *>(p.src[s]) + soff + j));
-        if (sg.dst_rank >= 0) {
-            atom::store_elem<DT>(static_cast<char *>(p.dst[sg.dst_rank]) + doff + j, acc);
-        } else {
-            for (int d = 0; d < R; ++d)
-                if (d != sg.skip_rank)
-                    atom::store_elem<DT>(static_cast<char *>(p.dst[d]) + doff + j, acc);
-        }
+    const uint4 out = V::pack(acc);
+    if (sg.dst_rank >= 0) {
+        put(static_cast<char *>(p.dst[sg.dst_rank]) + doff, out);
+    } else {
+        for (int r = 0; r < R; ++r)
+            if (r != sg.skip_rank) put(static_cast<char *>(p.dst[r]) + doff, out);
     }
 }
 
