@@ -45,7 +45,7 @@ Policy policy_for(purlin_collective coll, int R) {
             return {clamp16(98304 / (uint64_t)R, 1024, 16384), 2, 8ull << 20, false, 0, 1};
         case PURLIN_COLL_ALL_REDUCE:
             // (composed mode: the gather chunks are stored by the consumer warps)
-            return {clamp16(32768 / (uint64_t)R, 512, 8192), 3, 32ull << 20, true, 0, 1};
+            return {clamp16(32768 / (uint64_t)R, 512, 8192), 3, 16ull << 20, true, 0, 1};
         case PURLIN_COLL_ALL_GATHER:
             return {16384, 4, 1ull << 20, true, 8, 1};
         case PURLIN_COLL_ALL_GATHER_V:
