@@ -28,9 +28,10 @@ constexpr int kShiftedCopyConsumerWarps = 6;
 // Crossover: per-rank message bytes up to which the one-shot vector kernel
 // beats the staged ring.  At 64 registers it runs four CTAs of 256 threads
 // per SM, which keeps enough loads in flight that for reductions it wins up
-// to tens of MiB: ReduceScatter 32 MiB, AllReduce 16 MiB (at 32 MiB the two
-// variants trade places from box to box), ReduceScatterV 8 MiB, AllGather
-// 1 MiB, AllGatherV 2 MiB, AllToAll(V) 256 KiB.
+// to tens of MiB: ReduceScatterV 64 MiB (ragged blocks: the ring shifts its
+// sources, the vector path reads them aligned), ReduceScatter 32 MiB,
+// AllReduce 16 MiB (at 32 MiB the two variants trade places from box to
+// box), AllGather 1 MiB, AllGatherV 2 MiB, AllToAll(V) 256 KiB.
 // Ring shape:
 //   ReduceScatter(V)  one destination per reduced chunk: large per-source
 //                     chunks (96 KiB per stage), 2 stages;

@@ -49,10 +49,10 @@ struct KParams {
 
 // ---------------------------------------------------------- latency kernel --
 
-// ---------------------------------------------------------- latency kernel --
-
+// Four CTAs of 256 threads per SM (the host's grid cap) leave 64 registers
+// a thread; the instantiations for more than 8 ranks take two.
 template <int DT, int MAXR, int MAXSEG>
-__global__ void __launch_bounds__(256, 2) purlin_latency_kernel(
+__global__ void __launch_bounds__(256, MAXR > 8 ? 2 : 4) purlin_latency_kernel(
     const __grid_constant__ KParams<MAXR, MAXSEG> p) {
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
     const uint64_t u0 = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(256, 2) purlin_latency_kernel(
     // for a 2 KiB AllGather).  Short segments would make a warp read many
     // addresses, so those tables are staged in shared memory.
     if (MAXSEG > 1 && (p.nseg == 1 || p.nunits >= 16ull * (uint64_t)p.nseg)) {
-        units_loop<DT, MAXR>(p, p.segs, u0, stride);
+        units_loop<DT, MAXR, false>(p, p.segs, u0, stride);
         return;
     }
     // an inline table of MAXSEG segments, or up to kSmemSegs of a device table
@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(256, 2) purlin_latency_kernel(
     __shared__ Seg s_segs[kStage];
     const Seg *segs = stage_segs(p, s_segs, kStage);
     __syncthreads();
-    units_loop<DT, MAXR>(p, segs, u0, stride);
+    units_loop<DT, MAXR, false>(p, segs, u0, stride);
 }
 
 // ------------------------------------------------------- throughput kernel --

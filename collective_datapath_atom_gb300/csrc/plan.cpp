@@ -362,7 +362,7 @@ purlin_status compile_plan(const CallDesc &c, int variant, int ar_mode, uint32_t
                 p.notify_chunks += nch;
             }
         } else {
-            unit += units_in(r.dst_off, 0, r.bytes);
+            unit += units_in(unit_grid(r.src_off, r.dst_off, reduce), 0, r.bytes);
         }
         p.segs.push_back(s);
     }

@@ -90,12 +90,21 @@ PURLIN_HD inline Cut cut_transfer(uint64_t src_off, uint64_t dst_off, uint64_t b
     return c;
 }
 
-// Vector units covering the destination bytes [dst_off + a, dst_off + b):
-// one unit per 16-byte window of the destination address space.
-PURLIN_HD inline uint64_t units_in(uint64_t dst_off, uint64_t a, uint64_t b) {
+// The offset whose 16-byte grid a segment's vector units follow.  A reduce
+// reads every source at the same offset: on the sources' grid each source
+// is one aligned 128-bit load and only the single sum is stored at another
+// phase.  A copy reads one source: on the destination's grid that source is
+// fetched (and shifted) once and every destination store is aligned.
+PURLIN_HD inline uint64_t unit_grid(uint64_t src_off, uint64_t dst_off, bool reduce) {
+    return reduce ? src_off : dst_off;
+}
+
+// Vector units covering the bytes [grid + a, grid + b) of a segment whose
+// units follow the 16-byte grid of offset `grid`: one unit per window.
+PURLIN_HD inline uint64_t units_in(uint64_t grid, uint64_t a, uint64_t b) {
     if (b <= a) return 0;
-    const uint64_t first = (dst_off + a) / 16;
-    const uint64_t last = (dst_off + b + 15) / 16;
+    const uint64_t first = (grid + a) / 16;
+    const uint64_t last = (grid + b + 15) / 16;
     return last - first;
 }
 

@@ -133,19 +133,61 @@ __device__ __forceinline__ bool error_set(const unsigned long long *err) {
 
 // ------------------------------------------------------------ vector unit --
 
-// One 16-byte destination window of a segment: copy or reduce it to every
-// destination.  The window's source bytes (all 16, or the 1..15 of a partial
-// head or tail window) are fetched with at most two aligned 128-bit loads
-// per source, each holding at least one of those bytes (so no load leaves
-// the source buffer's 16-byte granules), and shifted into place; sums use
-// the vector code on all 16 bytes, and a partial window stores only its own
-// elements.
-template <int DT, int MAXR, class P>
+// Store bytes [b0, b0 + nb) of v at d (b0 + nb <= 16; d aligned to the
+// element size) as 32-bit words, with a 16-bit piece at either end where d
+// or the length is only 2-byte aligned.
+template <int ES>
+__device__ __forceinline__ void put_span_words(char *d, uint4 v, uint32_t b0, uint32_t nb) {
+    if (b0 != 0) v = atom::shift_pair(v, v, b0);   // the span's first byte to byte 0
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    auto pick = [&](uint32_t i) { return i == 0 ? w[0] : i == 1 ? w[1] : i == 2 ? w[2] : w[3]; };
+    if (ES == 4 || ((uintptr_t)d & 2u) == 0) {
+#pragma unroll
+        for (uint32_t i = 0; i < 4; ++i)
+            if (4 * i + 4 <= nb) *reinterpret_cast<uint32_t *>(d + 4 * i) = w[i];
+        if (ES == 2 && (nb & 2u))
+            *reinterpret_cast<uint16_t *>(d + (nb & ~3u)) = (uint16_t)pick(nb >> 2);
+    } else {   // d is 2 mod 4: a half word, whole words across x's words, a half word
+        *reinterpret_cast<uint16_t *>(d) = (uint16_t)w[0];
+#pragma unroll
+        for (uint32_t i = 0; i < 3; ++i)
+            if (4 * i + 6 <= nb)
+                *reinterpret_cast<uint32_t *>(d + 2 + 4 * i) = __funnelshift_r(w[i], w[i + 1], 16);
+        const uint32_t words = (nb - 2) >> 2;
+        if ((nb - 2) & 2u)
+            *reinterpret_cast<uint16_t *>(d + 2 + 4 * words) = (uint16_t)(pick(words) >> 16);
+    }
+}
+
+// Store bytes [b0, b0 + nb) of v at d: one 128-bit store for a whole aligned
+// window, else put_span_words.
+template <int ES>
+__device__ __forceinline__ void put_span(char *d, uint4 v, uint32_t b0, uint32_t nb) {
+    if (b0 == 0 && nb == 16u && ((uintptr_t)d & 15u) == 0) atom::st_v4(d, v);
+    else put_span_words<ES>(d, v, b0, nb);
+}
+
+// One 16-byte window of a segment: copy or reduce it to every destination.
+//
+// A reduce reads every source at the same offset, so its windows follow the
+// sources' 16-byte grid (unit_grid): each source takes one aligned 128-bit
+// load, all R in flight together, and the sum's window is stored at the
+// destination's phase (put_span).  A copy's windows follow the destination's
+// grid: its one source is fetched with at most two aligned 128-bit loads,
+// each holding at least one of the window's bytes (no load leaves the
+// source buffer's 16-byte granules), and shifted into place, so that the
+// stores to the R destinations are aligned.  A ring segment's vector units
+// are the destination bytes outside its aligned body (head and tail); a
+// reduce meets a shifted source only there and fetches it the copy's way
+// (RING: the caller is the ring, whose segments may have a body; the
+// one-shot kernels' never do).
+template <int DT, int MAXR, bool RING, class P>
 __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
     using V = atom::Vec<DT>;
     constexpr int ES = DT == PURLIN_F32 ? 4 : 2;
+    const bool reduce = sg.src_rank < 0;
     uint64_t lo, hi;
-    if (sg.tma) {
+    if (RING && sg.tma) {
         if (k == 0 && sg.head) {
             lo = 0;
             hi = sg.head;
@@ -154,10 +196,11 @@ __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
             hi = sg.bytes;
         }
     } else {
-        const uint64_t a = (sg.dst_off / 16 + k) * 16;
-        lo = (a > sg.dst_off ? a : sg.dst_off) - sg.dst_off;
-        const uint64_t b = a + 16, e = sg.dst_off + sg.bytes;
-        hi = (b < e ? b : e) - sg.dst_off;
+        const uint64_t g = unit_grid(sg.src_off, sg.dst_off, reduce);
+        const uint64_t a = (g / 16 + k) * 16;
+        lo = (a > g ? a : g) - g;
+        const uint64_t b = a + 16, e = g + sg.bytes;
+        hi = (b < e ? b : e) - g;
     }
     const int R = p.R;
     const uint32_t nb = (uint32_t)(hi - lo);   // 1..16 bytes of this window
@@ -175,7 +218,9 @@ __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
         const uint4 v0 = atom::ld_v4_l1(a);
         return atom::shift_pair(v0, two ? atom::ld_v4_l1(a + 16) : v0, sh);
     };
-    // Store the window's nb bytes of v at d: one 128-bit store when full.
+
+    // A copy's store: its window lies on the destination's grid, so a whole
+    // window is one aligned 128-bit store and a partial one element stores.
     auto put = [&](char *d, const uint4 &v) {
         if (nb == 16u) {
             atom::st_v4(d, v);
@@ -191,7 +236,7 @@ __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
         }
     };
 
-    if (sg.src_rank >= 0) {   // copy, bitwise
+    if (!reduce) {   // copy, bitwise
         const char *sbase = static_cast<const char *>(sg.src_is_dst ? p.dst[sg.src_rank]
                                                                     : p.src[sg.src_rank]);
         const uint4 v = fetch(sbase);
@@ -210,12 +255,19 @@ __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
     }
 
     // reduce (SCORE): rank order 0..R-1, binary32, one rounding at the end.
-    // Bytes past a partial window's end are summed too and never stored.
+    // Bytes of a vector outside the window are summed too and never stored.
+    // A group's loads all issue before any of its values is used.
+    const bool aligned = !RING || !sg.tma || sh == 0;   // one aligned vector per source
+    const uint32_t b0 = aligned ? sh : 0u;     // the window's first byte in the sum
+    auto load = [&](int s) -> uint4 {
+        const char *base = static_cast<const char *>(p.src[s]);
+        return aligned ? atom::ld_v4(base + (sx - sh)) : fetch(base);
+    };
     float acc[V::VE];
     uint4 v[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-        if (j < R) v[j] = fetch(static_cast<const char *>(p.src[j]));
+        if (j < R) v[j] = load(j);
     V::init(acc, v[0]);
 #pragma unroll
     for (int j = 1; j < 8; ++j)
@@ -224,7 +276,7 @@ __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
         for (int s0 = 8; s0 < R; s0 += 8) {
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                if (s0 + j < R) v[j] = fetch(static_cast<const char *>(p.src[s0 + j]));
+                if (s0 + j < R) v[j] = load(s0 + j);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
                 if (s0 + j < R) V::add(acc, v[j]);
@@ -232,24 +284,24 @@ __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
     }
     const uint4 out = V::pack(acc);
     if (sg.dst_rank >= 0) {
-        put(static_cast<char *>(p.dst[sg.dst_rank]) + doff, out);
+        put_span<ES>(static_cast<char *>(p.dst[sg.dst_rank]) + doff, out, b0, nb);
     } else {
         for (int r = 0; r < R; ++r)
-            if (r != sg.skip_rank) put(static_cast<char *>(p.dst[r]) + doff, out);
+            if (r != sg.skip_rank) put_span<ES>(static_cast<char *>(p.dst[r]) + doff, out, b0, nb);
     }
 }
 
 // Units u0, u0 + stride, ... of the plan: the first one's segment is found by
 // binary search, later ones by walking forward (units only increase), so
 // the search cost fades for threads that own many units.
-template <int DT, int MAXR, class P>
+template <int DT, int MAXR, bool RING, class P>
 __device__ __forceinline__ void units_loop(const P &p, const Seg *segs, uint64_t u0,
                                            uint64_t stride) {
     if (u0 >= p.nunits) return;
     int si = seg_of_unit(segs, p.nseg, u0);
     for (uint64_t u = u0; u < p.nunits; u += stride) {
         while (si + 1 < p.nseg && segs[si + 1].unit_begin <= u) ++si;
-        do_unit<DT, MAXR>(p, segs[si], u - segs[si].unit_begin);
+        do_unit<DT, MAXR, RING>(p, segs[si], u - segs[si].unit_begin);
     }
 }
 
@@ -533,7 +585,7 @@ __device__ void run_ring(const P &p, unsigned char *smem, Ctl *ctl_p, uint32_t b
         // --------------------------------------------- Consume (reduce) --
         const int ctid = (int)threadIdx.x - 64;
         const int nct = (int)blockDim.x - 64;
-        units_loop<DT, MAXR>(p, segs, (uint64_t)bidx * nct + ctid, (uint64_t)nblk * nct);
+        units_loop<DT, MAXR, true>(p, segs, (uint64_t)bidx * nct + ctid, (uint64_t)nblk * nct);
         uint32_t k = 0;
         for (uint64_t c = bidx; c < p.nchunks; c += nblk, ++k) {
             const ChunkGeo g = chunk_geo(segs, p.nseg, c);

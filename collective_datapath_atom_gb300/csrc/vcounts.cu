@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kVcThreadsMax, 1)
         sg.dst_off = dof;
         sg.bytes = bytes;
         sg.chunk_bytes = sg.src_rank < 0 ? p.red_chunk : p.copy_chunk;
-        uint64_t chunks = 0, units = units_in(dof, 0, bytes);
+        uint64_t chunks = 0, units = units_in(unit_grid(so, dof, sg.src_rank < 0), 0, bytes);
         if (ring) {
             const Cut cut = cut_transfer(so, dof, bytes);
             if (cut.body > 0) {
@@ -253,8 +253,8 @@ __global__ void __launch_bounds__(kVcThreadsMax, 1)
     if (!ring) {
         // one-shot vector units over every thread of the grid
         const uint64_t nt = blockDim.x;
-        units_loop<DT, MAXR>(v, segs, (uint64_t)blockIdx.x * nt + threadIdx.x,
-                             (uint64_t)gridDim.x * nt);
+        units_loop<DT, MAXR, false>(v, segs, (uint64_t)blockIdx.x * nt + threadIdx.x,
+                                    (uint64_t)gridDim.x * nt);
         return;
     }
     run_ring<DT, MAXR>(v, smem, ctl, blockIdx.x, gridDim.x, nullptr, 0);

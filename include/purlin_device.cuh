@@ -219,7 +219,7 @@ struct Atom {
             *nunits = (cut.head ? 1u : 0u) + (cut.tail ? 1u : 0u);
         } else {
             *nchunks = 0;
-            *nunits = units_in(dst_off, 0, bytes);
+            *nunits = units_in(unit_grid(src_off, dst_off, src_rank < 0), 0, bytes);
         }
         return s;
     }

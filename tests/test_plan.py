@@ -180,7 +180,10 @@ def test_cut_invariants(coll, R, dtype):
                     chunk_total += -(-body // sg["chunk_bytes"])
                     unit_total += (sg["head_bytes"] > 0) + (sg["tail_bytes"] > 0)
                 else:
-                    a, b = sg["dst_off"], sg["dst_off"] + sg["bytes"]
+                    # one unit per 16-byte window: a reduce's windows follow
+                    # the sources' grid, a copy's the destination's
+                    g = sg["src_off"] if sg["src_rank"] < 0 else sg["dst_off"]
+                    a, b = g, g + sg["bytes"]
                     unit_total += -(-b // 16) - a // 16
                     if variant == 2:   # only transfers without a whole aligned window skip the ring
                         assert sg["bytes"] < 32
