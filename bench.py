@@ -51,6 +51,7 @@ KERNEL_OF_VARIANT = {1: "purlin_latency_kernel", 2: "purlin_throughput_kernel",
                      5: "purlin_packet_ar_kernel"}
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = ["collective_datapath_atom_gb300/csrc/kernels.cu",
+                  "collective_datapath_atom_gb300/csrc/ring_kernel.cuh",
                   "collective_datapath_atom_gb300/csrc/snac.cuh",
                   "collective_datapath_atom_gb300/csrc/atom.cuh"]
 

@@ -7,45 +7,23 @@
 // §3.2: push for latency, pull for bandwidth.  On one GPU these become the
 // vector kernel and the staged ring.
 //
-// Latency kernel: one thread per 16-byte destination window ("unit"); no
-//   flags, since every output has one owner.
+// Latency kernel: one thread per 16-byte window ("unit"); no flags, since
+//   every output has one owner.
 // Throughput kernel: persistent CTAs running the ring (snac::run_ring) over
-//   the launch's whole grid.
-#include <cuda_runtime.h>
-
-#include "atom.cuh"
-#include "launch.h"
-#include "snac.cuh"
+//   the launch's whole grid (ring_kernel.cuh); this unit builds it for
+//   plans without reduce chunks stored at another 16-byte phase, and
+//   kernels_phase.cu for plans with them.
+#include "ring_kernel.cuh"
 
 namespace purlin {
 
 namespace {
 
 using namespace snac;
-
-constexpr int kTputMaxThreads = 512;
-
-template <int MAXR, int MAXSEG>
-struct KParams {
-    const void *src[MAXR];
-    void *dst[MAXR];
-    Seg segs[MAXSEG];
-    const Seg *segs_dev;
-    unsigned long long *flags;   // both parities' flag sets (flag_slots each), or null
-    unsigned long long *err;
-    DevEpoch *dev_epoch;         // the device epoch, when chunks notify one another
-    uint64_t epoch_inc;          // odd: added to the device epoch by the launch
-    uint64_t nchunks;
-    uint64_t nunits;
-    int64_t timeout_ns;
-    int64_t drop_notify;
-    uint32_t flag_slots;
-    uint32_t stages;
-    uint32_t slot_stride;
-    int32_t nseg;
-    int32_t R;
-    int32_t vector_copies;   // aligned copy chunks are stored by the consumer warps too
-};
+using ringk::KParams;
+using ringk::by_class;
+using ringk::class_of;
+using ringk::fill_params;
 
 // ---------------------------------------------------------- latency kernel --
 
@@ -75,52 +53,6 @@ __global__ void __launch_bounds__(256, MAXR > 8 ? 2 : 4) purlin_latency_kernel(
     units_loop<DT, MAXR, false>(p, segs, u0, stride);
 }
 
-// ------------------------------------------------------- throughput kernel --
-
-template <int DT, int MAXR, int MAXSEG>
-__global__ void __launch_bounds__(kTputMaxThreads, 1) purlin_throughput_kernel(
-    const __grid_constant__ KParams<MAXR, MAXSEG> p) {
-    extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ Ctl ctl;
-    if (p.dev_epoch == nullptr) {
-        run_ring<DT, MAXR>(p, smem, &ctl, blockIdx.x, gridDim.x, nullptr, 0);
-        return;
-    }
-    // chunks notify one another: the launch's epoch comes from device memory
-    epoch_enter(p.dev_epoch, &ctl);
-    __syncthreads();
-    const uint64_t epoch = ctl.epoch;
-    run_ring<DT, MAXR>(p, smem, &ctl, blockIdx.x, gridDim.x,
-                       p.flags + (epoch & 1ull) * p.flag_slots, epoch);
-    epoch_leave(p.dev_epoch, p.epoch_inc, gridDim.x);   // run_ring ended with a CTA barrier
-}
-
-template <int MAXR, int MAXSEG>
-void fill_params(KParams<MAXR, MAXSEG> &p, const LaunchArgs &a) {
-    for (int r = 0; r < MAXR; ++r) {
-        p.src[r] = r < a.R ? a.src[r] : nullptr;
-        p.dst[r] = r < a.R ? a.dst[r] : nullptr;
-    }
-    const Plan &pl = *a.plan;
-    const size_t nseg = pl.segs.size();
-    for (size_t i = 0; i < (size_t)MAXSEG; ++i) p.segs[i] = i < nseg && !a.segs_dev ? pl.segs[i] : Seg{};
-    p.segs_dev = a.segs_dev;
-    p.flags = a.flags;
-    p.dev_epoch = reinterpret_cast<DevEpoch *>(a.dev_epoch);
-    p.epoch_inc = a.epoch_inc;
-    p.err = a.err;
-    p.nchunks = pl.nchunks;
-    p.nunits = pl.nunits;
-    p.timeout_ns = a.timeout_ns;
-    p.drop_notify = a.drop_notify;
-    p.flag_slots = a.flag_slots;
-    p.stages = a.stages;
-    p.slot_stride = a.slot_stride;
-    p.nseg = (int32_t)nseg;
-    p.R = a.R;
-    p.vector_copies = a.vector_copies ? 1 : 0;
-}
-
 template <int DT, int MAXR, int MAXSEG>
 cudaError_t launch_lat_t(const LaunchArgs &a) {
     KParams<MAXR, MAXSEG> p;
@@ -133,27 +65,13 @@ cudaError_t launch_lat_t(const LaunchArgs &a) {
     return cudaLaunchKernelEx(&cfg, purlin_latency_kernel<DT, MAXR, MAXSEG>, p);
 }
 
-template <int DT, int MAXR, int MAXSEG>
-cudaError_t launch_tput_t(const LaunchArgs &a) {
-    KParams<MAXR, MAXSEG> p;
-    fill_params(p, a);
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.grid);
-    cfg.blockDim = dim3((unsigned)a.block);
-    cfg.dynamicSmemBytes = a.smem;
-    cfg.stream = a.stream;
-    if (a.cooperative) {
-        // CTAs that wait on one another's flags must all be resident.
-        attr[0].id = cudaLaunchAttributeCooperative;
-        attr[0].val.cooperative = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
-    return cudaLaunchKernelEx(&cfg, purlin_throughput_kernel<DT, MAXR, MAXSEG>, p);
-}
-
 __global__ void purlin_empty_kernel() {}
+
+struct LatLaunch {
+    const LaunchArgs &a;
+    template <int DT, int MR, int MS>
+    cudaError_t run() { return launch_lat_t<DT, MR, MS>(a); }
+};
 
 }  // namespace
 
@@ -177,81 +95,22 @@ uint32_t throughput_smem(uint32_t stages, uint32_t slot_stride) {
     return ring_workspace_bytes(stages, slot_stride);
 }
 
-namespace {
-
-// Calls f.template run<DT, MAXR, MAXSEG>() for a launch class and dtype.
-template <class F>
-cudaError_t by_class(int pc, int dtype, F &&f) {
-    const bool f32 = dtype == PURLIN_F32;
-    switch (pc) {
-        case kClassSmall:
-            return f32 ? f.template run<PURLIN_F32, kSmallMaxR, kSmallMaxSeg>()
-                       : f.template run<PURLIN_BF16, kSmallMaxR, kSmallMaxSeg>();
-        case kClassBig:
-            return f32 ? f.template run<PURLIN_F32, kBigMaxR, kBigMaxSeg>()
-                       : f.template run<PURLIN_BF16, kBigMaxR, kBigMaxSeg>();
-        case kClassDev8:
-            return f32 ? f.template run<PURLIN_F32, kSmallMaxR, 1>()
-                       : f.template run<PURLIN_BF16, kSmallMaxR, 1>();
-        case kClassDev64:
-            return f32 ? f.template run<PURLIN_F32, kBigMaxR, 1>()
-                       : f.template run<PURLIN_BF16, kBigMaxR, 1>();
-    }
-    return cudaErrorInvalidValue;
-}
-
-struct LatLaunch {
-    const LaunchArgs &a;
-    template <int DT, int MR, int MS>
-    cudaError_t run() { return launch_lat_t<DT, MR, MS>(a); }
-};
-struct TputLaunch {
-    const LaunchArgs &a;
-    template <int DT, int MR, int MS>
-    cudaError_t run() { return launch_tput_t<DT, MR, MS>(a); }
-};
-struct TputConfigure {
-    int max_dyn_smem;
-    template <int DT, int MR, int MS>
-    cudaError_t run() {
-        return cudaFuncSetAttribute(purlin_throughput_kernel<DT, MR, MS>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn_smem);
-    }
-};
-struct TputOccupancy {
-    int block;
-    size_t smem;
-    int *per_sm;
-    template <int DT, int MR, int MS>
-    cudaError_t run() {
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            per_sm, purlin_throughput_kernel<DT, MR, MS>, block, smem);
-    }
-};
-
-int class_of(const LaunchArgs &a) {
-    return launch_class(a.R, a.plan->segs.size(), a.segs_dev != nullptr);
-}
-
-}  // namespace
-
 cudaError_t launch_latency(const LaunchArgs &a) { return by_class(class_of(a), a.dtype, LatLaunch{a}); }
 
 cudaError_t launch_throughput(const LaunchArgs &a) {
-    return by_class(class_of(a), a.dtype, TputLaunch{a});
+    if (a.plan->has_phase_reduce) return launch_throughput_phase(a);
+    return by_class(class_of(a), a.dtype, ringk::TputLaunch<false>{a});
 }
 
 cudaError_t configure_kernels(int max_dyn_smem) {
-    for (int pc : {kClassSmall, kClassBig, kClassDev8, kClassDev64})
-        for (int dt : {PURLIN_F32, PURLIN_BF16}) {
-            const cudaError_t e = by_class(pc, dt, TputConfigure{max_dyn_smem});
-            if (e != cudaSuccess) return e;
-        }
-    return cudaSuccess;
+    const cudaError_t e = ringk::configure_ring<false>(max_dyn_smem);
+    return e != cudaSuccess ? e : configure_kernels_phase(max_dyn_smem);
 }
 
-cudaError_t throughput_occupancy(int dtype, int pclass, int block, size_t smem, int *per_sm) {
-    return by_class(pclass, dtype, TputOccupancy{block, smem, per_sm});
+cudaError_t throughput_occupancy(int dtype, int pclass, bool phase, int block, size_t smem,
+                                 int *per_sm) {
+    if (phase) return throughput_occupancy_phase(dtype, pclass, block, smem, per_sm);
+    return by_class(pclass, dtype, ringk::TputOccupancy<false>{block, smem, per_sm});
 }
 
 }  // namespace purlin

@@ -66,7 +66,7 @@ struct VcLaunch {
 uint32_t vcounts_smem(int coll, int R, uint32_t stages, uint32_t slot_stride);
 cudaError_t launch_vcounts(const VcLaunch &a);
 cudaError_t configure_vcounts(int max_dyn_smem);
-cudaError_t vcounts_occupancy(int dtype, int R, int block, size_t smem, int *per_sm);
+cudaError_t vcounts_occupancy(int dtype, int R, int coll, int block, size_t smem, int *per_sm);
 
 // Composed AllReduce on the latency path (packets.cu).
 constexpr uint64_t kPacketStagingBytes = 2ull << 20;   // per parity: 16-byte packets
@@ -113,7 +113,16 @@ cudaError_t launch_throughput(const LaunchArgs &a);
 // Largest dynamic shared memory the throughput kernels may use; set once.
 cudaError_t configure_kernels(int max_dyn_smem);
 
-cudaError_t throughput_occupancy(int dtype, int pclass, int block, size_t smem, int *per_sm);
+// phase: the plan holds reduce chunks stored at another 16-byte phase
+// (Plan::has_phase_reduce), which a separate build of the ring kernel runs.
+cudaError_t throughput_occupancy(int dtype, int pclass, bool phase, int block, size_t smem,
+                                 int *per_sm);
+
+// The ring kernel's PHASE build (kernels_phase.cu), behind launch_throughput,
+// configure_kernels and throughput_occupancy.
+cudaError_t launch_throughput_phase(const LaunchArgs &a);
+cudaError_t configure_kernels_phase(int max_dyn_smem);
+cudaError_t throughput_occupancy_phase(int dtype, int pclass, int block, size_t smem, int *per_sm);
 
 // Shared-memory bytes a throughput launch needs for `stages` ring slots of
 // `slot_stride` bytes, their mbarriers and the staged segment table.

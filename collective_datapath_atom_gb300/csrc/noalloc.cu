@@ -146,8 +146,8 @@ extern "C" purlin_status purlin_all_reduce_noalloc(int R, const void *const src[
     if (smem > limit) return PURLIN_ERR_UNSUPPORTED;
     const int block = 32 * (2 + kConsumerWarps);
     int per_sm = 0;
-    if (throughput_occupancy(dtype, param_class(R, pl.segs.size()), block, smem, &per_sm) !=
-            cudaSuccess ||
+    const int pc = param_class(R, pl.segs.size());
+    if (throughput_occupancy(dtype, pc, pl.has_phase_reduce, block, smem, &per_sm) != cudaSuccess ||
         per_sm < 1)
         return PURLIN_ERR_UNSUPPORTED;
     int64_t grid = (int64_t)ds.sms * per_sm;

@@ -336,10 +336,13 @@ purlin_status compile_plan(const CallDesc &c, int variant, int ar_mode, uint32_t
         s.unit_begin = unit;
         uint64_t body = 0;
         if (variant == kVariantThroughput) {
-            // The body is cut on the destination side (16-byte aligned stores);
-            // a source at another 16-byte phase is staged as its aligned hull,
-            // 16 bytes longer, and shifted into place by the consumer warps.
-            const Cut cut = cut_transfer(r.src_off, r.dst_off, r.bytes);
+            // A copy's body is cut on the destination side (16-byte aligned
+            // stores); a source at another 16-byte phase is staged as its
+            // aligned hull, 16 bytes longer, and shifted into place by the
+            // consumer warps.  A reduce's body is cut on the sources' side
+            // (aligned stages, no shift), and its sums are stored at the
+            // destination's phase.
+            const Cut cut = cut_transfer(r.src_off, r.dst_off, r.bytes, reduce);
             body = cut.body;
             if (body > 0) {
                 s.tma = 1;
@@ -357,6 +360,7 @@ purlin_status compile_plan(const CallDesc &c, int variant, int ar_mode, uint32_t
             if (reduce) p.has_reduce = true;
             else p.has_copy_chunks = true;
             if (!reduce && s.shift) p.has_shifted_copies = true;
+            if (reduce && s.shift) p.has_phase_reduce = true;
             if (r.sync == kSyncNotify) {
                 notify_begin.push_back(s.chunk_begin);
                 p.notify_chunks += nch;
@@ -375,11 +379,12 @@ purlin_status compile_plan(const CallDesc &c, int variant, int ar_mode, uint32_t
     if (chunk > 0xFFFFFFF0ull) return PURLIN_ERR_INVALID_ARG;
     p.nchunks = chunk;
     p.nunits = unit;
-    // A stage holds one tile per source; a shifted tile is 16 bytes longer.
+    // A stage holds one tile per source; a shifted copy's tile (its aligned
+    // hull) is 16 bytes longer.
     uint32_t slot = 0;
     for (const Seg &s : p.segs) {
         if (!s.tma) continue;
-        const uint32_t tile = s.chunk_bytes + (s.shift ? 16u : 0u);
+        const uint32_t tile = s.chunk_bytes + (s.src_rank != kRankAll && s.shift ? 16u : 0u);
         const uint32_t nsrc = s.src_rank == kRankAll ? (uint32_t)R : 1u;
         slot = std::max<uint32_t>(slot, tile * nsrc);
     }

@@ -67,29 +67,6 @@ struct Seg {
 };
 static_assert(sizeof(Seg) == 56, "Seg layout is part of the kernel parameter block");
 
-// The ring's cut of one transfer: the bytes before the destination's first
-// 16-byte boundary (head) and after its last (tail) go through the vector
-// path; the aligned body goes through the ring in chunks.  A source at
-// another 16-byte phase (shift != 0) is staged as its aligned hull and
-// shifted into place.  Used by the host plan compiler and by the device-side
-// Atom, so both cut a transfer the same way.
-struct Cut {
-    uint64_t body;
-    uint32_t head, tail, shift;
-};
-
-PURLIN_HD inline Cut cut_transfer(uint64_t src_off, uint64_t dst_off, uint64_t bytes) {
-    Cut c;
-    const uint64_t lead = (16u - (dst_off & 15u)) & 15u;
-    const uint64_t head = lead < bytes ? lead : bytes;
-    const uint64_t rest = bytes - head;
-    c.head = (uint32_t)head;
-    c.tail = (uint32_t)(rest & 15u);
-    c.body = rest - c.tail;
-    c.shift = (uint32_t)((src_off - dst_off) & 15u);
-    return c;
-}
-
 // The offset whose 16-byte grid a segment's vector units follow.  A reduce
 // reads every source at the same offset: on the sources' grid each source
 // is one aligned 128-bit load and only the single sum is stored at another
@@ -97,6 +74,34 @@ PURLIN_HD inline Cut cut_transfer(uint64_t src_off, uint64_t dst_off, uint64_t b
 // fetched (and shifted) once and every destination store is aligned.
 PURLIN_HD inline uint64_t unit_grid(uint64_t src_off, uint64_t dst_off, bool reduce) {
     return reduce ? src_off : dst_off;
+}
+
+// The ring's cut of one transfer, on the 16-byte grid its vector units follow
+// (unit_grid): the bytes before the grid's first boundary (head) and after
+// its last (tail) go through the vector path; the aligned body goes through
+// the ring in chunks.  shift is the source's 16-byte phase relative to the
+// destination.  A copy's body is aligned on the destination: a shifted source
+// is staged as its 16-byte aligned hull and shifted into place as it is read.
+// A reduce's body is aligned on the sources: they are staged as they are,
+// and the sum is stored at the destination's phase.  Used by the host plan
+// compiler, the device-count kernel and the device-side Atom, so all cut a
+// transfer the same way.
+struct Cut {
+    uint64_t body;
+    uint32_t head, tail, shift;
+};
+
+PURLIN_HD inline Cut cut_transfer(uint64_t src_off, uint64_t dst_off, uint64_t bytes, bool reduce) {
+    Cut c;
+    const uint64_t grid = unit_grid(src_off, dst_off, reduce);
+    const uint64_t lead = (16u - (grid & 15u)) & 15u;
+    const uint64_t head = lead < bytes ? lead : bytes;
+    const uint64_t rest = bytes - head;
+    c.head = (uint32_t)head;
+    c.tail = (uint32_t)(rest & 15u);
+    c.body = rest - c.tail;
+    c.shift = (uint32_t)((src_off - dst_off) & 15u);
+    return c;
 }
 
 // Vector units covering the bytes [grid + a, grid + b) of a segment whose
@@ -121,6 +126,7 @@ struct Plan {
     bool has_reduce = false;
     bool has_copy_chunks = false;
     bool has_shifted_copies = false;  // copies the consumer warps shift into place
+    bool has_phase_reduce = false;    // reduce chunks stored at another 16-byte phase
     bool composed = false;
     int variant = kVariantNone;
 };

@@ -177,8 +177,7 @@ __device__ __forceinline__ void put_span(char *d, uint4 v, uint32_t b0, uint32_t
 // each holding at least one of the window's bytes (no load leaves the
 // source buffer's 16-byte granules), and shifted into place, so that the
 // stores to the R destinations are aligned.  A ring segment's vector units
-// are the destination bytes outside its aligned body (head and tail); a
-// reduce meets a shifted source only there and fetches it the copy's way
+// are the bytes outside its aligned body (head and tail, on the same grid)
 // (RING: the caller is the ring, whose segments may have a body; the
 // one-shot kernels' never do).
 template <int DT, int MAXR, bool RING, class P>
@@ -255,13 +254,11 @@ __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
     }
 
     // reduce (SCORE): rank order 0..R-1, binary32, one rounding at the end.
-    // Bytes of a vector outside the window are summed too and never stored.
-    // A group's loads all issue before any of its values is used.
-    const bool aligned = !RING || !sg.tma || sh == 0;   // one aligned vector per source
-    const uint32_t b0 = aligned ? sh : 0u;     // the window's first byte in the sum
+    // The window lies in one aligned vector of every source (its bytes are
+    // [sh, sh + nb) of it); bytes outside the window are summed too and never
+    // stored.  A group's loads all issue before any of its values is used.
     auto load = [&](int s) -> uint4 {
-        const char *base = static_cast<const char *>(p.src[s]);
-        return aligned ? atom::ld_v4(base + (sx - sh)) : fetch(base);
+        return atom::ld_v4(static_cast<const char *>(p.src[s]) + (sx - sh));
     };
     float acc[V::VE];
     uint4 v[8];
@@ -284,10 +281,10 @@ __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
     }
     const uint4 out = V::pack(acc);
     if (sg.dst_rank >= 0) {
-        put_span<ES>(static_cast<char *>(p.dst[sg.dst_rank]) + doff, out, b0, nb);
+        put_span<ES>(static_cast<char *>(p.dst[sg.dst_rank]) + doff, out, sh, nb);
     } else {
         for (int r = 0; r < R; ++r)
-            if (r != sg.skip_rank) put_span<ES>(static_cast<char *>(p.dst[r]) + doff, out, b0, nb);
+            if (r != sg.skip_rank) put_span<ES>(static_cast<char *>(p.dst[r]) + doff, out, sh, nb);
     }
 }
 
@@ -412,9 +409,46 @@ __device__ __forceinline__ void epoch_leave(DevEpoch *e, uint64_t inc, uint32_t 
     }
 }
 
-// flags/epoch: this launch's flag set (the parity the epoch selects) and its
-// epoch, for plans whose chunks notify or wait (else unused).
+// The consumer warps' share of a reduce chunk whose sources are staged on
+// their own 16-byte grid (tile bytes apart, from sp) while the destination
+// is at another phase: each thread sums its vectors over the sources in rank
+// order and stores the sum at the destination's phase.
 template <int DT, int MAXR, class P>
+__device__ __forceinline__ void reduce_chunk_to_phase(const P &p, const Seg &sg,
+                                                   const unsigned char *sp, uint32_t tile,
+                                                   int nvec, uint64_t doff, int ctid, int nct) {
+    using V = atom::Vec<DT>;
+    constexpr int ES = DT == PURLIN_F32 ? 4 : 2;
+    const int R = p.R;
+    for (int v = ctid; v < nvec; v += nct) {
+        const unsigned char *t = sp + 16 * (size_t)v;
+        float acc[V::VE];
+        V::init(acc, atom::lds_v4(t));
+        if (MAXR <= 8) {
+#pragma unroll
+            for (int s = 1; s < MAXR; ++s)
+                if (s < R) V::add(acc, atom::lds_v4(t + (size_t)s * tile));
+        } else {
+#pragma unroll 8
+            for (int s = 1; s < R; ++s) V::add(acc, atom::lds_v4(t + (size_t)s * tile));
+        }
+        const uint4 out = V::pack(acc);
+        const uint64_t o = doff + 16 * (uint64_t)v;
+        if (sg.dst_rank >= 0) {
+            put_span<ES>(static_cast<char *>(p.dst[sg.dst_rank]) + o, out, 0, 16);
+        } else {
+            for (int d = 0; d < R; ++d)
+                if (d != sg.skip_rank) put_span<ES>(static_cast<char *>(p.dst[d]) + o, out, 0, 16);
+        }
+    }
+}
+
+// flags/epoch: this launch's flag set (the parity the epoch selects) and its
+// epoch, for plans whose chunks notify or wait (else unused).  PHASE: the
+// plan may hold reduce chunks whose destination is at another 16-byte phase
+// than their sources (reduce_chunk_to_phase); a ring built without it runs
+// only plans that hold none, and keeps the consumer loop's code as it was.
+template <int DT, int MAXR, bool PHASE, class P>
 __device__ void run_ring(const P &p, unsigned char *smem, Ctl *ctl_p, uint32_t bidx,
                          uint32_t nblk, unsigned long long *flags, uint64_t epoch) {
     using V = atom::Vec<DT>;
@@ -479,8 +513,10 @@ __device__ void run_ring(const P &p, unsigned char *smem, Ctl *ctl_p, uint32_t b
             }
             unsigned char *sp = ring + (size_t)slot * p.slot_stride;
             const int nsrc = sg.src_rank < 0 ? R : 1;
-            // A shifted source is staged as its 16-byte aligned hull.
-            const uint32_t extra = sg.shift ? 16u : 0u;
+            // A shifted copy's source is staged as its 16-byte aligned hull; a
+            // reduce's sources are aligned on their own grid.
+            const uint32_t lead = sg.src_rank >= 0 ? sg.shift : 0u;
+            const uint32_t extra = lead ? 16u : 0u;
             const uint32_t tile = sg.chunk_bytes + extra;
             const uint32_t ld_bytes = g.bytes + extra;
             if (lane == 0) atom::mbar_arrive_expect_tx(&full[slot], ld_bytes * (uint32_t)nsrc);
@@ -490,8 +526,8 @@ __device__ void run_ring(const P &p, unsigned char *smem, Ctl *ctl_p, uint32_t b
                     sg.src_rank < 0 ? static_cast<const char *>(p.src[s])
                                     : static_cast<const char *>(sg.src_is_dst ? p.dst[sg.src_rank]
                                                                               : p.src[sg.src_rank]);
-                atom::bulk_load(sp + (size_t)s * tile, base + sg.src_off + g.off - sg.shift,
-                                ld_bytes, &full[slot], pol);
+                atom::bulk_load(sp + (size_t)s * tile, base + sg.src_off + g.off - lead, ld_bytes,
+                                &full[slot], pol);
             }
         }
         // Every load this warp issued must land before the CTA exits.
@@ -601,7 +637,7 @@ __device__ void run_ring(const P &p, unsigned char *smem, Ctl *ctl_p, uint32_t b
                 continue;
             }
             const unsigned char *sp = ring + (size_t)slot * p.slot_stride;
-            const uint32_t sh = sg.shift;
+            const uint32_t sh = reduce ? 0u : sg.shift;   // a copy's hull is shifted as it is read
             const uint32_t tile = sg.chunk_bytes + (sh ? 16u : 0u);
             const int nvec = (int)(g.bytes >> 4);
             const uint64_t doff = sg.dst_off + g.off;
@@ -617,31 +653,37 @@ __device__ void run_ring(const P &p, unsigned char *smem, Ctl *ctl_p, uint32_t b
                 if (!sh) return atom::lds_v4(t);
                 return atom::lds_v4_shifted(t, sh);
             };
-            for (int v = ctid; v < nvec; v += nct) {
-                uint4 out;
-                if (reduce) {
-                    float acc[V::VE];
-                    V::init(acc, tile_v4(0, v));
-                    if (MAXR <= 8) {
+            if (PHASE && reduce && sg.shift) {
+                // A reduce's body is aligned on the sources: its sums go to the
+                // destination's phase.
+                reduce_chunk_to_phase<DT, MAXR>(p, sg, sp, tile, nvec, doff, ctid, nct);
+            } else {
+                for (int v = ctid; v < nvec; v += nct) {
+                    uint4 out;
+                    if (reduce) {
+                        float acc[V::VE];
+                        V::init(acc, tile_v4(0, v));
+                        if (MAXR <= 8) {
 #pragma unroll
-                        for (int s = 1; s < MAXR; ++s)
-                            if (s < R) V::add(acc, tile_v4(s, v));
-                    } else {
+                            for (int s = 1; s < MAXR; ++s)
+                                if (s < R) V::add(acc, tile_v4(s, v));
+                        } else {
 #pragma unroll 8
-                        for (int s = 1; s < R; ++s) V::add(acc, tile_v4(s, v));
+                            for (int s = 1; s < R; ++s) V::add(acc, tile_v4(s, v));
+                        }
+                        out = V::pack(acc);
+                    } else {
+                        out = tile_v4(0, v);
                     }
-                    out = V::pack(acc);
-                } else {
-                    out = tile_v4(0, v);
-                }
-                const uint64_t o = doff + 16 * (uint64_t)v;
-                if (sg.dst_rank >= 0) {
-                    if (static_cast<const char *>(p.dst[sg.dst_rank]) + doff != self)
-                        atom::st_v4(static_cast<char *>(p.dst[sg.dst_rank]) + o, out);
-                } else {
-                    for (int d = 0; d < R; ++d)
-                        if (d != sg.skip_rank && static_cast<const char *>(p.dst[d]) + doff != self)
-                            atom::st_v4(static_cast<char *>(p.dst[d]) + o, out);
+                    const uint64_t o = doff + 16 * (uint64_t)v;
+                    if (sg.dst_rank >= 0) {
+                        if (static_cast<const char *>(p.dst[sg.dst_rank]) + doff != self)
+                            atom::st_v4(static_cast<char *>(p.dst[sg.dst_rank]) + o, out);
+                    } else {
+                        for (int d = 0; d < R; ++d)
+                            if (d != sg.skip_rank && static_cast<const char *>(p.dst[d]) + doff != self)
+                                atom::st_v4(static_cast<char *>(p.dst[d]) + o, out);
+                    }
                 }
             }
             if (sg.sync == kSyncNotify) {

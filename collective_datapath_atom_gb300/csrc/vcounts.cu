@@ -92,7 +92,9 @@ uint32_t vcounts_smem(int coll, int R, uint32_t stages, uint32_t slot_stride) {
 
 namespace {
 
-template <int DT, int MAXR>
+// PHASE: built for ReduceScatterV, whose ragged blocks put reduce chunks at
+// another 16-byte phase than their sources (snac::run_ring).
+template <int DT, int MAXR, bool PHASE>
 __global__ void __launch_bounds__(kVcThreadsMax, 1)
     purlin_vcounts_kernel(const __grid_constant__ VcParams<MAXR> p) {
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -191,7 +193,7 @@ __global__ void __launch_bounds__(kVcThreadsMax, 1)
         sg.chunk_bytes = sg.src_rank < 0 ? p.red_chunk : p.copy_chunk;
         uint64_t chunks = 0, units = units_in(unit_grid(so, dof, sg.src_rank < 0), 0, bytes);
         if (ring) {
-            const Cut cut = cut_transfer(so, dof, bytes);
+            const Cut cut = cut_transfer(so, dof, bytes, sg.src_rank < 0);
             if (cut.body > 0) {
                 sg.tma = 1;
                 sg.head = (uint8_t)cut.head;
@@ -257,10 +259,10 @@ __global__ void __launch_bounds__(kVcThreadsMax, 1)
                                     (uint64_t)gridDim.x * nt);
         return;
     }
-    run_ring<DT, MAXR>(v, smem, ctl, blockIdx.x, gridDim.x, nullptr, 0);
+    run_ring<DT, MAXR, PHASE>(v, smem, ctl, blockIdx.x, gridDim.x, nullptr, 0);
 }
 
-template <int DT, int MAXR>
+template <int DT, int MAXR, bool PHASE>
 cudaError_t launch_vc_t(const VcLaunch &a) {
     VcParams<MAXR> p;
     for (int r = 0; r < MAXR; ++r) {
@@ -286,41 +288,61 @@ cudaError_t launch_vc_t(const VcLaunch &a) {
     cfg.blockDim = dim3((unsigned)a.block);
     cfg.dynamicSmemBytes = a.smem;
     cfg.stream = a.stream;
-    return cudaLaunchKernelEx(&cfg, purlin_vcounts_kernel<DT, MAXR>, p);
+    return cudaLaunchKernelEx(&cfg, purlin_vcounts_kernel<DT, MAXR, PHASE>, p);
+}
+
+// Calls f(kernel) with the device-count kernel for a dtype, R and collective.
+template <class F>
+cudaError_t with_vc_kernel(int dtype, int R, int coll, F &&f) {
+    const bool phase = coll == PURLIN_COLL_REDUCE_SCATTER_V;
+    const bool f32 = dtype == PURLIN_F32, small = R <= 8;
+    if (phase) {
+        if (f32) return small ? f(purlin_vcounts_kernel<PURLIN_F32, 8, true>)
+                              : f(purlin_vcounts_kernel<PURLIN_F32, kVcMaxRanks, true>);
+        return small ? f(purlin_vcounts_kernel<PURLIN_BF16, 8, true>)
+                     : f(purlin_vcounts_kernel<PURLIN_BF16, kVcMaxRanks, true>);
+    }
+    if (f32) return small ? f(purlin_vcounts_kernel<PURLIN_F32, 8, false>)
+                          : f(purlin_vcounts_kernel<PURLIN_F32, kVcMaxRanks, false>);
+    return small ? f(purlin_vcounts_kernel<PURLIN_BF16, 8, false>)
+                 : f(purlin_vcounts_kernel<PURLIN_BF16, kVcMaxRanks, false>);
 }
 
 }  // namespace
 
 cudaError_t launch_vcounts(const VcLaunch &a) {
-    if (a.dtype == PURLIN_F32)
-        return a.R <= 8 ? launch_vc_t<PURLIN_F32, 8>(a) : launch_vc_t<PURLIN_F32, kVcMaxRanks>(a);
-    return a.R <= 8 ? launch_vc_t<PURLIN_BF16, 8>(a) : launch_vc_t<PURLIN_BF16, kVcMaxRanks>(a);
+    const bool phase = a.coll == PURLIN_COLL_REDUCE_SCATTER_V;
+    if (a.dtype == PURLIN_F32) {
+        if (phase)
+            return a.R <= 8 ? launch_vc_t<PURLIN_F32, 8, true>(a)
+                            : launch_vc_t<PURLIN_F32, kVcMaxRanks, true>(a);
+        return a.R <= 8 ? launch_vc_t<PURLIN_F32, 8, false>(a)
+                        : launch_vc_t<PURLIN_F32, kVcMaxRanks, false>(a);
+    }
+    if (phase)
+        return a.R <= 8 ? launch_vc_t<PURLIN_BF16, 8, true>(a)
+                        : launch_vc_t<PURLIN_BF16, kVcMaxRanks, true>(a);
+    return a.R <= 8 ? launch_vc_t<PURLIN_BF16, 8, false>(a)
+                    : launch_vc_t<PURLIN_BF16, kVcMaxRanks, false>(a);
 }
 
 cudaError_t configure_vcounts(int max_dyn_smem) {
-    cudaError_t e;
-#define PURLIN_SET(DT, MR)                                                                    \
-    e = cudaFuncSetAttribute(purlin_vcounts_kernel<DT, MR>,                                  \
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn_smem);     \
-    if (e != cudaSuccess) return e;
-    PURLIN_SET(PURLIN_F32, 8)
-    PURLIN_SET(PURLIN_F32, kVcMaxRanks)
-    PURLIN_SET(PURLIN_BF16, 8)
-    PURLIN_SET(PURLIN_BF16, kVcMaxRanks)
-#undef PURLIN_SET
+    for (int coll : {PURLIN_COLL_ALL_TO_ALL_V, PURLIN_COLL_REDUCE_SCATTER_V})
+        for (int dtype : {PURLIN_F32, PURLIN_BF16})
+            for (int R : {8, kVcMaxRanks}) {
+                const cudaError_t e = with_vc_kernel(dtype, R, coll, [&](auto kernel) {
+                    return cudaFuncSetAttribute(
+                        kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn_smem);
+                });
+                if (e != cudaSuccess) return e;
+            }
     return cudaSuccess;
 }
 
-cudaError_t vcounts_occupancy(int dtype, int R, int block, size_t smem, int *per_sm) {
-    if (dtype == PURLIN_F32)
-        return R <= 8 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                            per_sm, purlin_vcounts_kernel<PURLIN_F32, 8>, block, smem)
-                      : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                            per_sm, purlin_vcounts_kernel<PURLIN_F32, kVcMaxRanks>, block, smem);
-    return R <= 8 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                        per_sm, purlin_vcounts_kernel<PURLIN_BF16, 8>, block, smem)
-                  : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                        per_sm, purlin_vcounts_kernel<PURLIN_BF16, kVcMaxRanks>, block, smem);
+cudaError_t vcounts_occupancy(int dtype, int R, int coll, int block, size_t smem, int *per_sm) {
+    return with_vc_kernel(dtype, R, coll, [&](auto kernel) {
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, kernel, block, smem);
+    });
 }
 
 }  // namespace purlin

@@ -45,8 +45,9 @@ purlin_status run_vcounts(purlin_ctx *ctx, purlin_collective coll, const void *c
     const int64_t chunk_opt = ctx->opt[PURLIN_OPT_CHUNK_BYTES];
     const uint32_t chunk = (uint32_t)(chunk_opt > 0 ? chunk_opt : shape.chunk) & ~15u;
     const bool reduce = coll == PURLIN_COLL_REDUCE_SCATTER_V;
-    // Any count may put a source at another 16-byte phase: room for the hull.
-    const uint32_t slot = reduce ? (chunk + 16u) * (uint32_t)c.R : chunk + 16u;
+    // Any count may put a copy's source at another 16-byte phase: room for its
+    // hull.  A reduce stages its sources on their own grid.
+    const uint32_t slot = reduce ? chunk * (uint32_t)c.R : chunk + 16u;
     const uint32_t slot_stride = (slot + 127u) & ~127u;
     // AllToAllV: 3 stages and 6 consumer warps (two CTAs per SM) measured
     // best for both 16-byte aligned counts (the MoE dispatch: equal to the
@@ -64,7 +65,7 @@ purlin_status run_vcounts(purlin_ctx *ctx, purlin_collective coll, const void *c
                                                       : kReduceConsumerWarps;
     const int block = 32 * (2 + cw);
     int per_sm = 0;
-    if (vcounts_occupancy(dtype, c.R, block, smem, &per_sm) != cudaSuccess || per_sm < 1)
+    if (vcounts_occupancy(dtype, c.R, coll, block, smem, &per_sm) != cudaSuccess || per_sm < 1)
         return PURLIN_ERR_UNSUPPORTED;
 
     VcLaunch a;

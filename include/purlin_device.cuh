@@ -131,8 +131,15 @@ __device__ purlin_status collective_t(const purlin_device_coll &c, const SnacArg
                              c.nseg,
                              c.R,
                              c.vector_copies};
-    snac::run_ring<DT, MAXR>(v, ws, ctl, (uint32_t)a.bIdx, (uint32_t)a.blocks,
-                             c.flags ? c.flags + (epoch & 1ull) * c.flag_slots : nullptr, epoch);
+    unsigned long long *flags = c.flags ? c.flags + (epoch & 1ull) * c.flag_slots : nullptr;
+    // Ragged reduce blocks store their sums at another 16-byte phase: that
+    // build of the ring, for descriptors that need it only.
+    if (c.phase_reduce)
+        snac::run_ring<DT, MAXR, true>(v, ws, ctl, (uint32_t)a.bIdx, (uint32_t)a.blocks, flags,
+                                       epoch);
+    else
+        snac::run_ring<DT, MAXR, false>(v, ws, ctl, (uint32_t)a.bIdx, (uint32_t)a.blocks, flags,
+                                        epoch);
     // (run_ring ends with a CTA barrier.)  One thread reads the error word
     // so that every thread returns the same status.
     if (threadIdx.x == 0) {
@@ -209,7 +216,7 @@ struct Atom {
         s.dst_rank = 0;
         s.skip_rank = -1;
         s.chunk_bytes = chunk;
-        const Cut cut = cut_transfer(src_off, dst_off, bytes);
+        const Cut cut = cut_transfer(src_off, dst_off, bytes, src_rank < 0);
         if (cut.body > 0) {
             s.tma = 1;
             s.head = (uint8_t)cut.head;
@@ -242,8 +249,10 @@ struct Atom {
                      1,
                      nsrc,
                      0};
-        snac::run_ring<DT, MAXR>(v, ws, reinterpret_cast<snac::Ctl *>(ws + kCtl), 0u, 1u, nullptr,
-                                 0);
+        // One transfer whose reduce sources and destination share a phase
+        // (reduce() requires 16-byte aligned buffers).
+        snac::run_ring<DT, MAXR, false>(v, ws, reinterpret_cast<snac::Ctl *>(ws + kCtl), 0u, 1u,
+                                        nullptr, 0);
         return *reinterpret_cast<volatile unsigned long long *>(ws + kErr) != 0ull
                    ? PURLIN_ERR_TIMEOUT
                    : PURLIN_OK;

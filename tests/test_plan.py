@@ -173,8 +173,10 @@ def test_cut_invariants(coll, R, dtype):
                     body = sg["bytes"] - sg["head_bytes"] - sg["tail_bytes"]
                     assert body > 0 and body % 16 == 0
                     assert sg["head_bytes"] < 16 and sg["tail_bytes"] < 16
-                    assert (sg["dst_off"] + sg["head_bytes"]) % 16 == 0
-                    assert (sg["src_off"] + sg["head_bytes"]) % 16 == sg["shift"]
+                    # the body is aligned on the grid the segment's units follow:
+                    # a reduce's sources, a copy's destination
+                    g = sg["src_off"] if sg["src_rank"] < 0 else sg["dst_off"]
+                    assert (g + sg["head_bytes"]) % 16 == 0
                     assert (sg["src_off"] - sg["dst_off"]) % 16 == sg["shift"]
                     assert sg["chunk_bytes"] % 16 == 0
                     chunk_total += -(-body // sg["chunk_bytes"])
@@ -202,12 +204,14 @@ def test_cut_invariants(coll, R, dtype):
                 if sg["tma"]:
                     assert max(sg["chunk_bytes"] * (R if sg["src_rank"] < 0 else 1),
                                sg["chunk_bytes"]) <= 1 << 20
-                    # the staged source hull starts on the 16-byte boundary at or
-                    # before the first body byte and ends on the one at or after
-                    # the last: never past the granule holding the buffer's end
-                    h0 = sg["src_off"] + sg["head_bytes"] - sg["shift"]
+                    # the staged source range starts on the 16-byte boundary at
+                    # or before the first body byte and ends on the one at or
+                    # after the last (a shifted copy's hull): never past the
+                    # granule holding the buffer's end
+                    lead = sg["shift"] if sg["src_rank"] >= 0 else 0
+                    h0 = sg["src_off"] + sg["head_bytes"] - lead
                     body = sg["bytes"] - sg["head_bytes"] - sg["tail_bytes"]
-                    h1 = h0 + body + (16 if sg["shift"] else 0)
+                    h1 = h0 + body + (16 if lead else 0)
                     assert h0 >= 0 and h0 % 16 == 0
                     for s_ in srcs:
                         assert h1 <= -(-src_len[s_] // 16) * 16
