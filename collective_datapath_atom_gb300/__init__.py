@@ -95,7 +95,7 @@ class purlin_device_coll(ctypes.Structure):
                 ("R", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("vector_copies", ctypes.c_int32), ("blocks", ctypes.c_int32),
                 ("threads", ctypes.c_int32), ("composed", ctypes.c_int32),
-                ("coll", ctypes.c_int32), ("phase_reduce", ctypes.c_int32),
+                ("coll", ctypes.c_int32), ("ragged", ctypes.c_int32),
                 ("owner", ctypes.c_void_p)]
 
 

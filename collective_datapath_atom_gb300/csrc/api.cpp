@@ -366,8 +366,8 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
         const int block = 32 * (2 + rs.consumer_warps);
         const int pclass = launch_class(c.R, pl.segs.size(), e->segs_dev != nullptr);
         int per_sm = 0;
-        const bool phase = pl.has_phase_reduce;
-        if (throughput_occupancy(c.dtype, pclass, phase, block, smem, &per_sm) != cudaSuccess ||
+        const bool ragged = ragged_ring(pl);
+        if (throughput_occupancy(c.dtype, pclass, ragged, block, smem, &per_sm) != cudaSuccess ||
             per_sm < 1)
             return PURLIN_ERR_UNSUPPORTED;
         int64_t grid = (int64_t)ctx->sms * std::min(per_sm, std::max(1, shape.ctas_per_sm));

@@ -81,7 +81,7 @@ purlin_status purlin_device_prepare(purlin_ctx *ctx, purlin_collective coll,
     d.threads = 32 * (2 + rs.consumer_warps);
     d.composed = pl.composed ? 1 : 0;
     d.coll = coll;
-    d.phase_reduce = pl.has_phase_reduce ? 1 : 0;
+    d.ragged = ragged_ring(pl) ? 1 : 0;
 
     DeviceCollMem m;
     auto fail = [&](purlin_status s) {

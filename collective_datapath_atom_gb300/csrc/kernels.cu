@@ -11,8 +11,8 @@
 //   every output has one owner.
 // Throughput kernel: persistent CTAs running the ring (snac::run_ring) over
 //   the launch's whole grid (ring_kernel.cuh); this unit builds it for
-//   plans without reduce chunks stored at another 16-byte phase, and
-//   kernels_phase.cu for plans with them.
+//   plans whose ring chunks share their destination's 16-byte phase, and
+//   kernels_ragged.cu for plans with chunks at another phase.
 #include "ring_kernel.cuh"
 
 namespace purlin {
@@ -98,18 +98,18 @@ uint32_t throughput_smem(uint32_t stages, uint32_t slot_stride) {
 cudaError_t launch_latency(const LaunchArgs &a) { return by_class(class_of(a), a.dtype, LatLaunch{a}); }
 
 cudaError_t launch_throughput(const LaunchArgs &a) {
-    if (a.plan->has_phase_reduce) return launch_throughput_phase(a);
+    if (ragged_ring(*a.plan)) return launch_throughput_ragged(a);
     return by_class(class_of(a), a.dtype, ringk::TputLaunch<false>{a});
 }
 
 cudaError_t configure_kernels(int max_dyn_smem) {
     const cudaError_t e = ringk::configure_ring<false>(max_dyn_smem);
-    return e != cudaSuccess ? e : configure_kernels_phase(max_dyn_smem);
+    return e != cudaSuccess ? e : configure_kernels_ragged(max_dyn_smem);
 }
 
-cudaError_t throughput_occupancy(int dtype, int pclass, bool phase, int block, size_t smem,
+cudaError_t throughput_occupancy(int dtype, int pclass, bool ragged, int block, size_t smem,
                                  int *per_sm) {
-    if (phase) return throughput_occupancy_phase(dtype, pclass, block, smem, per_sm);
+    if (ragged) return throughput_occupancy_ragged(dtype, pclass, block, smem, per_sm);
     return by_class(pclass, dtype, ringk::TputOccupancy<false>{block, smem, per_sm});
 }
 

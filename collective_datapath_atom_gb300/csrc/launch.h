@@ -113,16 +113,16 @@ cudaError_t launch_throughput(const LaunchArgs &a);
 // Largest dynamic shared memory the throughput kernels may use; set once.
 cudaError_t configure_kernels(int max_dyn_smem);
 
-// phase: the plan holds reduce chunks stored at another 16-byte phase
-// (Plan::has_phase_reduce), which a separate build of the ring kernel runs.
-cudaError_t throughput_occupancy(int dtype, int pclass, bool phase, int block, size_t smem,
+// ragged: the plan has ring chunks at another 16-byte phase than their
+// destination (ragged_ring), which a separate build of the ring kernel runs.
+cudaError_t throughput_occupancy(int dtype, int pclass, bool ragged, int block, size_t smem,
                                  int *per_sm);
 
-// The ring kernel's PHASE build (kernels_phase.cu), behind launch_throughput,
-// configure_kernels and throughput_occupancy.
-cudaError_t launch_throughput_phase(const LaunchArgs &a);
-cudaError_t configure_kernels_phase(int max_dyn_smem);
-cudaError_t throughput_occupancy_phase(int dtype, int pclass, int block, size_t smem, int *per_sm);
+// The ring kernel's RAGGED build (kernels_ragged.cu), behind
+// launch_throughput, configure_kernels and throughput_occupancy.
+cudaError_t launch_throughput_ragged(const LaunchArgs &a);
+cudaError_t configure_kernels_ragged(int max_dyn_smem);
+cudaError_t throughput_occupancy_ragged(int dtype, int pclass, int block, size_t smem, int *per_sm);
 
 // Shared-memory bytes a throughput launch needs for `stages` ring slots of
 // `slot_stride` bytes, their mbarriers and the staged segment table.

@@ -147,7 +147,7 @@ extern "C" purlin_status purlin_all_reduce_noalloc(int R, const void *const src[
     const int block = 32 * (2 + kConsumerWarps);
     int per_sm = 0;
     const int pc = param_class(R, pl.segs.size());
-    if (throughput_occupancy(dtype, pc, pl.has_phase_reduce, block, smem, &per_sm) != cudaSuccess ||
+    if (throughput_occupancy(dtype, pc, ragged_ring(pl), block, smem, &per_sm) != cudaSuccess ||
         per_sm < 1)
         return PURLIN_ERR_UNSUPPORTED;
     int64_t grid = (int64_t)ds.sms * per_sm;

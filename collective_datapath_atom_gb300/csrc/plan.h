@@ -131,6 +131,11 @@ struct Plan {
     int variant = kVariantNone;
 };
 
+// A plan with ring chunks at another 16-byte phase than their destination
+// (reduce chunks stored at the destination's phase, or copies shifted into
+// place): the ring kernel's RAGGED build runs it.
+inline bool ragged_ring(const Plan &p) { return p.has_phase_reduce || p.has_shifted_copies; }
+
 // Arguments of one call, as the C ABI received them.
 struct CallDesc {
     purlin_collective coll;

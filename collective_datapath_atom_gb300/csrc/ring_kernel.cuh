@@ -1,8 +1,8 @@
 // ring_kernel.cuh -- the ring kernel (snac::run_ring over the launch's
 // whole grid), its parameter block and its launch, shared by the two
-// translation units that build it: kernels.cu (plans whose reduce chunks
-// store at their sources' 16-byte phase) and kernels_phase.cu (plans with
-// reduce chunks stored at another phase, PHASE).  Internal to the library.
+// translation units that build it: kernels.cu (plans whose ring chunks share
+// their destination's 16-byte phase) and kernels_ragged.cu (plans with
+// chunks at another phase, RAGGED).  Internal to the library.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -42,21 +42,22 @@ struct KParams {
 
 // ------------------------------------------------------- throughput kernel --
 
-// PHASE: built for plans with reduce chunks stored at another 16-byte phase.
-template <int DT, int MAXR, int MAXSEG, bool PHASE>
+// RAGGED: built for plans with ring chunks at another 16-byte phase than their
+// destination (ragged_ring).
+template <int DT, int MAXR, int MAXSEG, bool RAGGED>
 __global__ void __launch_bounds__(kTputMaxThreads, 1) purlin_throughput_kernel(
     const __grid_constant__ KParams<MAXR, MAXSEG> p) {
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ Ctl ctl;
     if (p.dev_epoch == nullptr) {
-        run_ring<DT, MAXR, PHASE>(p, smem, &ctl, blockIdx.x, gridDim.x, nullptr, 0);
+        run_ring<DT, MAXR, RAGGED>(p, smem, &ctl, blockIdx.x, gridDim.x, nullptr, 0);
         return;
     }
     // chunks notify one another: the launch's epoch comes from device memory
     epoch_enter(p.dev_epoch, &ctl);
     __syncthreads();
     const uint64_t epoch = ctl.epoch;
-    run_ring<DT, MAXR, PHASE>(p, smem, &ctl, blockIdx.x, gridDim.x,
+    run_ring<DT, MAXR, RAGGED>(p, smem, &ctl, blockIdx.x, gridDim.x,
                               p.flags + (epoch & 1ull) * p.flag_slots, epoch);
     epoch_leave(p.dev_epoch, p.epoch_inc, gridDim.x);   // run_ring ended with a CTA barrier
 }
@@ -87,7 +88,7 @@ void fill_params(KParams<MAXR, MAXSEG> &p, const LaunchArgs &a) {
     p.vector_copies = a.vector_copies ? 1 : 0;
 }
 
-template <int DT, int MAXR, int MAXSEG, bool PHASE>
+template <int DT, int MAXR, int MAXSEG, bool RAGGED>
 cudaError_t launch_tput_t(const LaunchArgs &a) {
     KParams<MAXR, MAXSEG> p;
     fill_params(p, a);
@@ -104,7 +105,7 @@ cudaError_t launch_tput_t(const LaunchArgs &a) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, purlin_throughput_kernel<DT, MAXR, MAXSEG, PHASE>, p);
+    return cudaLaunchKernelEx(&cfg, purlin_throughput_kernel<DT, MAXR, MAXSEG, RAGGED>, p);
 }
 
 // Calls f.template run<DT, MAXR, MAXSEG>() for a launch class and dtype.
@@ -132,22 +133,22 @@ inline int class_of(const LaunchArgs &a) {
     return launch_class(a.R, a.plan->segs.size(), a.segs_dev != nullptr);
 }
 
-template <bool PHASE>
+template <bool RAGGED>
 struct TputLaunch {
     const LaunchArgs &a;
     template <int DT, int MR, int MS>
-    cudaError_t run() { return launch_tput_t<DT, MR, MS, PHASE>(a); }
+    cudaError_t run() { return launch_tput_t<DT, MR, MS, RAGGED>(a); }
 };
-template <bool PHASE>
+template <bool RAGGED>
 struct TputConfigure {
     int max_dyn_smem;
     template <int DT, int MR, int MS>
     cudaError_t run() {
-        return cudaFuncSetAttribute(purlin_throughput_kernel<DT, MR, MS, PHASE>,
+        return cudaFuncSetAttribute(purlin_throughput_kernel<DT, MR, MS, RAGGED>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn_smem);
     }
 };
-template <bool PHASE>
+template <bool RAGGED>
 struct TputOccupancy {
     int block;
     size_t smem;
@@ -155,16 +156,16 @@ struct TputOccupancy {
     template <int DT, int MR, int MS>
     cudaError_t run() {
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            per_sm, purlin_throughput_kernel<DT, MR, MS, PHASE>, block, smem);
+            per_sm, purlin_throughput_kernel<DT, MR, MS, RAGGED>, block, smem);
     }
 };
 
-// The ring kernels of one PHASE for every launch class and dtype.
-template <bool PHASE>
+// The ring kernels of one build (RAGGED or not) for every launch class and dtype.
+template <bool RAGGED>
 cudaError_t configure_ring(int max_dyn_smem) {
     for (int pc : {kClassSmall, kClassBig, kClassDev8, kClassDev64})
         for (int dt : {PURLIN_F32, PURLIN_BF16}) {
-            const cudaError_t e = by_class(pc, dt, TputConfigure<PHASE>{max_dyn_smem});
+            const cudaError_t e = by_class(pc, dt, TputConfigure<RAGGED>{max_dyn_smem});
             if (e != cudaSuccess) return e;
         }
     return cudaSuccess;

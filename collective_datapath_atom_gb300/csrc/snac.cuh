@@ -443,12 +443,52 @@ __device__ __forceinline__ void reduce_chunk_to_phase(const P &p, const Seg &sg,
     }
 }
 
+// The 16 bytes that start at byte 4K + r/8 of the 32-byte pair (a, b) (r: 0,
+// 8, 16 or 24 bits): with the word offset K fixed at compile time the window
+// is four funnel shifts, with no selects.
+template <int K>
+__device__ __forceinline__ uint4 window_at(const uint4 &a, const uint4 &b, uint32_t r) {
+    static_assert(K >= 0 && K <= 3, "word offset");
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    return make_uint4(__funnelshift_r(w[K], w[K + 1], r), __funnelshift_r(w[K + 1], w[K + 2], r),
+                      __funnelshift_r(w[K + 2], w[K + 3], r), __funnelshift_r(w[K + 3], w[K + 4], r));
+}
+
+// The consumer warps' share of a copy chunk staged as its 16-byte aligned
+// hull (sp) whose source sits 4K + r/8 bytes past the destination's phase:
+// each vector is read as the two aligned 128-bit shared vectors holding it
+// (two conflict-free accesses per warp, against five 32-bit loads at a
+// 16-byte lane stride, each a 4-way bank conflict) and shifted into place.
+template <int K, class P>
+__device__ __forceinline__ void copy_chunk_shifted(const P &p, const Seg &sg,
+                                                   const unsigned char *sp, uint32_t r, int nvec,
+                                                   uint64_t doff, const char *self, int ctid,
+                                                   int nct) {
+    const int R = p.R;
+    for (int v = ctid; v < nvec; v += nct) {
+        const unsigned char *t = sp + 16 * (size_t)v;
+        const uint4 out = window_at<K>(atom::lds_v4(t), atom::lds_v4(t + 16), r);
+        const uint64_t o = doff + 16 * (uint64_t)v;
+        if (sg.dst_rank >= 0) {
+            if (static_cast<const char *>(p.dst[sg.dst_rank]) + doff != self)
+                atom::st_v4(static_cast<char *>(p.dst[sg.dst_rank]) + o, out);
+        } else {
+            for (int d = 0; d < R; ++d)
+                if (d != sg.skip_rank && static_cast<const char *>(p.dst[d]) + doff != self)
+                    atom::st_v4(static_cast<char *>(p.dst[d]) + o, out);
+        }
+    }
+}
+
 // flags/epoch: this launch's flag set (the parity the epoch selects) and its
-// epoch, for plans whose chunks notify or wait (else unused).  PHASE: the
-// plan may hold reduce chunks whose destination is at another 16-byte phase
-// than their sources (reduce_chunk_to_phase); a ring built without it runs
-// only plans that hold none, and keeps the consumer loop's code as it was.
-template <int DT, int MAXR, bool PHASE, class P>
+// epoch, for plans whose chunks notify or wait (else unused).  RAGGED: the
+// plan may hold chunks at another 16-byte phase than their destination:
+// reduce chunks whose sums are stored at the destination's phase
+// (reduce_chunk_to_phase, required for them) and shifted copies
+// (copy_chunk_shifted).  A ring built without it takes no reduce chunk at
+// another phase, shifts copies through its generic path, and keeps the
+// consumer loop's code as it was.
+template <int DT, int MAXR, bool RAGGED, class P>
 __device__ void run_ring(const P &p, unsigned char *smem, Ctl *ctl_p, uint32_t bidx,
                          uint32_t nblk, unsigned long long *flags, uint64_t epoch) {
     using V = atom::Vec<DT>;
@@ -653,10 +693,19 @@ __device__ void run_ring(const P &p, unsigned char *smem, Ctl *ctl_p, uint32_t b
                 if (!sh) return atom::lds_v4(t);
                 return atom::lds_v4_shifted(t, sh);
             };
-            if (PHASE && reduce && sg.shift) {
+            if (RAGGED && reduce && sg.shift) {
                 // A reduce's body is aligned on the sources: its sums go to the
                 // destination's phase.
                 reduce_chunk_to_phase<DT, MAXR>(p, sg, sp, tile, nvec, doff, ctid, nct);
+            } else if (RAGGED && sh) {
+                // a copy's hull, shifted with the word offset fixed per loop
+                const uint32_t r = (sh & 3u) * 8u;
+                switch (sh >> 2) {
+                    case 0: copy_chunk_shifted<0>(p, sg, sp, r, nvec, doff, self, ctid, nct); break;
+                    case 1: copy_chunk_shifted<1>(p, sg, sp, r, nvec, doff, self, ctid, nct); break;
+                    case 2: copy_chunk_shifted<2>(p, sg, sp, r, nvec, doff, self, ctid, nct); break;
+                    default: copy_chunk_shifted<3>(p, sg, sp, r, nvec, doff, self, ctid, nct); break;
+                }
             } else {
                 for (int v = ctid; v < nvec; v += nct) {
                     uint4 out;

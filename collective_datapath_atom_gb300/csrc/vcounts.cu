@@ -92,9 +92,11 @@ uint32_t vcounts_smem(int coll, int R, uint32_t stages, uint32_t slot_stride) {
 
 namespace {
 
-// PHASE: built for ReduceScatterV, whose ragged blocks put reduce chunks at
-// another 16-byte phase than their sources (snac::run_ring).
-template <int DT, int MAXR, bool PHASE>
+// RAGGED: built for ReduceScatterV, whose ragged blocks put reduce chunks at
+// another 16-byte phase than their destination (snac::run_ring).  The copies
+// (AllGatherV, AllToAllV) take the other build, whose generic shifted-copy
+// path serves any phase.
+template <int DT, int MAXR, bool RAGGED>
 __global__ void __launch_bounds__(kVcThreadsMax, 1)
     purlin_vcounts_kernel(const __grid_constant__ VcParams<MAXR> p) {
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -259,10 +261,10 @@ __global__ void __launch_bounds__(kVcThreadsMax, 1)
                                     (uint64_t)gridDim.x * nt);
         return;
     }
-    run_ring<DT, MAXR, PHASE>(v, smem, ctl, blockIdx.x, gridDim.x, nullptr, 0);
+    run_ring<DT, MAXR, RAGGED>(v, smem, ctl, blockIdx.x, gridDim.x, nullptr, 0);
 }
 
-template <int DT, int MAXR, bool PHASE>
+template <int DT, int MAXR, bool RAGGED>
 cudaError_t launch_vc_t(const VcLaunch &a) {
     VcParams<MAXR> p;
     for (int r = 0; r < MAXR; ++r) {
@@ -288,7 +290,7 @@ cudaError_t launch_vc_t(const VcLaunch &a) {
     cfg.blockDim = dim3((unsigned)a.block);
     cfg.dynamicSmemBytes = a.smem;
     cfg.stream = a.stream;
-    return cudaLaunchKernelEx(&cfg, purlin_vcounts_kernel<DT, MAXR, PHASE>, p);
+    return cudaLaunchKernelEx(&cfg, purlin_vcounts_kernel<DT, MAXR, RAGGED>, p);
 }
 
 // Calls f(kernel) with the device-count kernel for a dtype, R and collective.

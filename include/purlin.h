@@ -405,8 +405,8 @@ typedef struct purlin_device_coll {
     int32_t threads;                     /* suggested block size */
     int32_t composed;                    /* 1: CTAs wait on one another (all must be resident) */
     int32_t coll;                        /* purlin_collective */
-    int32_t phase_reduce;                /* 1: reduce chunks are stored at another 16-byte
-                                            phase than their sources (ragged blocks) */
+    int32_t ragged;                      /* 1: ring chunks at another 16-byte phase than their
+                                            destination (ragged blocks) */
     void *owner;                         /* library bookkeeping (host address) */
 } purlin_device_coll;
 

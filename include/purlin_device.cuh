@@ -132,9 +132,9 @@ __device__ purlin_status collective_t(const purlin_device_coll &c, const SnacArg
                              c.R,
                              c.vector_copies};
     unsigned long long *flags = c.flags ? c.flags + (epoch & 1ull) * c.flag_slots : nullptr;
-    // Ragged reduce blocks store their sums at another 16-byte phase: that
-    // build of the ring, for descriptors that need it only.
-    if (c.phase_reduce)
+    // Ragged blocks (chunks at another 16-byte phase than their
+    // destination): that build of the ring, for descriptors that need it only.
+    if (c.ragged)
         snac::run_ring<DT, MAXR, true>(v, ws, ctl, (uint32_t)a.bIdx, (uint32_t)a.blocks, flags,
                                        epoch);
     else
