@@ -104,6 +104,57 @@ PURLIN_HD inline Cut cut_transfer(uint64_t src_off, uint64_t dst_off, uint64_t b
     return c;
 }
 
+// The order in which a ring CTA takes its chunks (position pos of its walk
+// -> chunk_at(order, pos)).  A composed AllReduce's plan numbers its reducing
+// chunks [0, nr) (each notifies) before its gathering chunks [nr, nr + ng)
+// (gathering chunk G waits on reducing chunks numbered below (G + 1) R).
+// Taken in that order, every CTA runs a read-heavy phase and then a
+// write-heavy one that starts on flags.  The walk instead puts gathering
+// chunk G right after reducing chunk min(nr, (G + lag + 1) R) - 1: lag
+// groups of R behind the chunks it depends on, enough for their flags to
+// have gone out (a CTA publishes its flags in batches of up to `batch`
+// chunks), and those chunks stay earlier in every CTA's walk (the launch is
+// cooperative, so the earliest unfinished chunk can always proceed).  Other
+// plans (ng == 0) keep their own order.  Chunk counts stay below 2^32.
+struct ChunkOrder {
+    uint32_t nr = 0;     // reducing chunks, numbered first
+    uint32_t ng = 0;     // gathering chunks after them; 0: the plan's own order
+    uint32_t g1 = 0;     // gathering chunks interleaved; the rest follow the last reducing chunk
+    uint32_t base = 0;   // (lag + 1) R: the walk position of gathering chunk 0, when interleaved
+    uint32_t R = 1;
+};
+
+PURLIN_HD inline ChunkOrder make_chunk_order(uint64_t nr, uint64_t ng, int R, uint32_t ctas,
+                                             int batch) {
+    ChunkOrder o;
+    o.nr = (uint32_t)nr;
+    o.ng = (uint32_t)ng;
+    o.R = (uint32_t)R;
+    uint32_t lag = (uint32_t)((uint64_t)(batch + 4) * ctas / ((uint64_t)R + 1u));
+    lag = lag > 0 ? lag : 1u;
+    // gathering chunk G is interleaved while (G + lag + 1) R < nr
+    const uint32_t groups = (o.nr + o.R - 1) / o.R;
+    const uint32_t g1 = groups > lag + 1 ? groups - lag - 1 : 0u;
+    o.g1 = g1 < o.ng ? g1 : o.ng;
+    o.base = (lag + 1) * o.R;
+    return o;
+}
+
+// The chunk at position pos of the walk: gathering chunk G < g1 sits at
+// position (R + 1) G + base, the others at nr + G, and the reducing chunks
+// fill the other positions in their own order.
+PURLIN_HD inline uint64_t chunk_at(const ChunkOrder &o, uint64_t pos64) {
+    if (o.ng == 0) return pos64;
+    const uint32_t pos = (uint32_t)pos64;
+    if (pos >= o.nr + o.g1) return pos;   // gathering chunk pos - nr, numbered pos
+    if (pos < o.base) return pos;         // before the first interleaved gathering chunk
+    const uint32_t x = pos - o.base;
+    const uint32_t q = x / (o.R + 1u);
+    if (x == q * (o.R + 1u) && q < o.g1) return (uint64_t)o.nr + q;
+    const uint32_t before = (x + o.R) / (o.R + 1u);   // gathering chunks placed earlier
+    return pos - (before < o.g1 ? before : o.g1);      // (all g1, once ng < nr / R runs out)
+}
+
 // Vector units covering the bytes [grid + a, grid + b) of a segment whose
 // units follow the 16-byte grid of offset `grid`: one unit per window.
 PURLIN_HD inline uint64_t units_in(uint64_t grid, uint64_t a, uint64_t b) {

@@ -443,6 +443,22 @@ __device__ __forceinline__ void reduce_chunk_to_phase(const P &p, const Seg &sg,
     }
 }
 
+// ------------------------------------------------------- chunk order --
+
+// For plans whose chunks notify and wait (flags given): the first waiting
+// segment's first chunk ends the reducing chunks (ChunkOrder in plan.h).
+// Every thread calls it (measured: as fast as one thread's result shared
+// through the control block, and the other collectives keep their speed).
+__device__ __forceinline__ ChunkOrder chunk_order(const Seg *segs, int nseg, uint64_t nchunks,
+                                                  int R, uint32_t nblk, bool composed) {
+    if (!composed) return ChunkOrder{};
+    for (int i = 0; i < nseg; ++i)
+        if (segs[i].sync == kSyncWait && segs[i].tma)
+            return make_chunk_order(segs[i].chunk_begin, nchunks - segs[i].chunk_begin, R, nblk,
+                                    kNotifyBatch);
+    return ChunkOrder{};
+}
+
 // The 16 bytes that start at byte 4K + r/8 of the 32-byte pair (a, b) (r: 0,
 // 8, 16 or 24 bits): with the word offset K fixed at compile time the window
 // is four funnel shifts, with no selects.
@@ -527,6 +543,8 @@ __device__ void run_ring(const P &p, unsigned char *smem, Ctl *ctl_p, uint32_t b
         atom::mbar_init_fence();
     }
     __syncthreads();
+    // (the staged table is complete)
+    const ChunkOrder order = chunk_order(segs, p.nseg, p.nchunks, R, nblk, flags != nullptr);
 
     if (warp == 0) {
         // ---------------------------------------------------------- Stage --
@@ -534,7 +552,8 @@ __device__ void run_ring(const P &p, unsigned char *smem, Ctl *ctl_p, uint32_t b
         // of source s, so the R loads of a chunk go out in parallel.
         const uint64_t pol = atom::policy_evict_first();
         uint32_t k = 0;
-        for (uint64_t c = bidx; c < p.nchunks; c += nblk, ++k) {
+        for (uint64_t pos = bidx; pos < p.nchunks; pos += nblk, ++k) {
+            const uint64_t c = chunk_at(order, pos);
             const uint32_t slot = k % S;
             bool ok = true;
             if (k >= S)
@@ -595,7 +614,8 @@ __device__ void run_ring(const P &p, unsigned char *smem, Ctl *ctl_p, uint32_t b
             }
             npend = 0;
         };
-        for (uint64_t c = bidx; c < p.nchunks; c += nblk, ++k) {
+        for (uint64_t pos = bidx; pos < p.nchunks; pos += nblk, ++k) {
+            const uint64_t c = chunk_at(order, pos);
             const ChunkGeo g = chunk_geo(segs, p.nseg, c);
             const Seg &sg = *g.sg;
             const uint32_t slot = k % S;
@@ -663,7 +683,8 @@ __device__ void run_ring(const P &p, unsigned char *smem, Ctl *ctl_p, uint32_t b
         const int nct = (int)blockDim.x - 64;
         units_loop<DT, MAXR, true>(p, segs, (uint64_t)bidx * nct + ctid, (uint64_t)nblk * nct);
         uint32_t k = 0;
-        for (uint64_t c = bidx; c < p.nchunks; c += nblk, ++k) {
+        for (uint64_t pos = bidx; pos < p.nchunks; pos += nblk, ++k) {
+            const uint64_t c = chunk_at(order, pos);
             const ChunkGeo g = chunk_geo(segs, p.nseg, c);
             const Seg &sg = *g.sg;
             const bool reduce = sg.src_rank < 0;
