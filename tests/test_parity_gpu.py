@@ -551,10 +551,14 @@ def test_composed_allreduce_wide_R(P, R):
     try:
         P.purlin_set_option(ctx, P.PURLIN_OPT_VARIANT, 2)
         P.purlin_set_option(ctx, P.PURLIN_OPT_AR_MODE, 2)
-        for k, n in enumerate((R * 16 * 3 + 5, 70001)):
+        # the last case, with 256-byte chunks, has enough reducing chunks for
+        # the ring to interleave its gathering chunks (more than lag + 1
+        # groups of R: lag = 12 * 152 // (R + 1) groups on 152 CTAs)
+        for k, (n, chunk) in enumerate(((R * 16 * 3 + 5, 0), (70001, 0), (300007, 256))):
+            P.purlin_set_option(ctx, P.PURLIN_OPT_CHUNK_BYTES, chunk)
             ins = gen_inputs([n] * R, 1, seed=5000 + k + R)
             got, _ = run(P, ctx, "all_reduce", ins, [n * 2] * R, 1, n)
-            assert_same(got, oracle.all_reduce(ins, 1), f"composed R={R} n={n}")
+            assert_same(got, oracle.all_reduce(ins, 1), f"composed R={R} n={n} chunk={chunk}")
             assert P.purlin_last_launch(ctx)["variant"] == 3
     finally:
         ctx.close()
