@@ -599,6 +599,11 @@ __device__ void run_ring(const P &p, unsigned char *smem, Ctl *ctl_p, uint32_t b
         // Lane d issues the bulk store to destination d; each lane tracks its
         // own bulk groups, and lane 0 hands a stage back once every lane's
         // stores have read it.
+        // In a ragged plan the consumer warps store most chunks and this warp
+        // mostly waits: it takes the segments' ragged head and tail windows
+        // while the first stages load, and the consumer warps start on the
+        // chunks at once.
+        if (RAGGED) units_loop<DT, MAXR, true>(p, segs, (uint64_t)bidx * 32 + lane, (uint64_t)nblk * 32);
         const uint64_t pol = atom::policy_evict_first();
         uint32_t k = 0;
         int owed = -1;             // slot whose release waits on the newest bulk group
@@ -681,7 +686,8 @@ __device__ void run_ring(const P &p, unsigned char *smem, Ctl *ctl_p, uint32_t b
         // --------------------------------------------- Consume (reduce) --
         const int ctid = (int)threadIdx.x - 64;
         const int nct = (int)blockDim.x - 64;
-        units_loop<DT, MAXR, true>(p, segs, (uint64_t)bidx * nct + ctid, (uint64_t)nblk * nct);
+        if (!RAGGED)
+            units_loop<DT, MAXR, true>(p, segs, (uint64_t)bidx * nct + ctid, (uint64_t)nblk * nct);
         uint32_t k = 0;
         for (uint64_t pos = bidx; pos < p.nchunks; pos += nblk, ++k) {
             const uint64_t c = chunk_at(order, pos);
