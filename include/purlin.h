@@ -330,7 +330,8 @@ typedef struct {
     int32_t sync;          /* 0 none, 1 notify a flag after writing, 2 wait on a flag before reading */
     int32_t tma;           /* 1 if the 16-byte-aligned body goes through the TMA ring */
     int32_t shift;         /* tma: 16-byte phase of the source relative to the destination */
-    uint64_t head_bytes;   /* bytes before the aligned body (vector path) */
+    uint64_t head_bytes;   /* bytes before the aligned body (vector path); the body is aligned
+                              on the sources for a reduce, on the destination for a copy */
     uint64_t tail_bytes;   /* bytes after it (vector path) */
     uint64_t chunk_begin;  /* index of the segment's first TMA chunk */
     uint64_t chunk_bytes;  /* bytes per source per TMA chunk */
