@@ -41,8 +41,8 @@ Policy policy_for(purlin_collective coll, int R) {
     switch (coll) {
         case PURLIN_COLL_REDUCE_SCATTER:
             return {clamp16(98304 / (uint64_t)R, 1024, 16384), 2, 32ull << 20, false, 0, 1};
-        case PURLIN_COLL_REDUCE_SCATTER_V:   // ragged blocks: the ring shifts, the vector path need not
-            return {clamp16(98304 / (uint64_t)R, 1024, 16384), 2, 64ull << 20, false, 0, 1};
+        case PURLIN_COLL_REDUCE_SCATTER_V:   // both paths read ragged blocks aligned
+            return {clamp16(98304 / (uint64_t)R, 1024, 16384), 2, 32ull << 20, false, 0, 1};
         case PURLIN_COLL_ALL_REDUCE:
             // (composed mode: the gather chunks are stored by the consumer warps)
             return {clamp16(32768 / (uint64_t)R, 512, 8192), 3, 16ull << 20, true, 0, 1};

@@ -28,10 +28,11 @@ constexpr int kShiftedCopyConsumerWarps = 6;
 // Crossover: per-rank message bytes up to which the one-shot vector kernel
 // beats the staged ring.  At 64 registers it runs four CTAs of 256 threads
 // per SM, which keeps enough loads in flight that for reductions it wins up
-// to tens of MiB: ReduceScatterV 64 MiB (ragged blocks: the ring shifts its
-// sources, the vector path reads them aligned), ReduceScatter 32 MiB,
-// AllReduce 16 MiB (at 32 MiB the two variants trade places from box to
-// box), AllGather 1 MiB, AllGatherV 2 MiB, AllToAll(V) 256 KiB.
+// to tens of MiB: ReduceScatter and ReduceScatterV 32 MiB (ragged blocks
+// read aligned on both paths; at 64 MiB the ring leads, 0.97 of the copy
+// peak against 0.92), AllReduce 16 MiB (at 32 MiB the two variants trade
+// places from box to box), AllGather 1 MiB, AllGatherV 2 MiB, AllToAll(V)
+// 256 KiB.
 // Ring shape:
 //   ReduceScatter(V)  one destination per reduced chunk: large per-source
 //                     chunks (96 KiB per stage), 2 stages;
