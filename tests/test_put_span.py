@@ -1,16 +1,19 @@
-"""The vector path's store at another 16-byte phase (put_span and
-put_span_words in csrc/snac.cuh), compiled on the host from the shipped
-source text.
+"""Byte shuffles of the vector path and the ring, compiled on the host from
+the shipped source text of csrc/snac.cuh: the store at another 16-byte
+phase (put_span, put_span_words) and the fixed-offset window of the ragged
+ring's shifted copies (window_at).
 
 A ReduceScatter(V) window on the sources' grid ends at an arbitrary
 destination phase: put_span stores bytes [b0, b0 + nb) of a 16-byte sum at
 an address aligned only to the element size.  The functions are cut out of
-the header, compiled with g++ against stand-ins for the three device
-intrinsics they use (a 128-bit store, a byte shift of a vector pair, a
-funnel shift), and run for every destination phase, first byte and length:
+the header, compiled with g++ against stand-ins for the device intrinsics
+they use (a 128-bit store, a byte shift of a vector pair, a funnel shift,
+make_uint4), and run for every destination phase, first byte and length:
 exactly the window's bytes must change, to the right values, and every
-store must be naturally aligned and inside the window.  Two planted
-mistakes in the cut-out text must be caught.
+store must be naturally aligned and inside the window.  window_at must
+return bytes [4K + r/8, 4K + r/8 + 16) of its 32-byte pair for every word
+offset K and bit shift r.  Planted mistakes in the cut-out text must be
+caught.
 """
 import os
 import re
@@ -27,6 +30,7 @@ PRELUDE = r"""
 #include <cstdio>
 #include <cstring>
 struct uint4 { uint32_t x, y, z, w; };
+static uint4 make_uint4(uint32_t x, uint32_t y, uint32_t z, uint32_t w) { return uint4{x, y, z, w}; }
 static int bad = 0;
 static uint8_t *lo_, *hi_;
 static void check(const char *p, int size) {
@@ -142,3 +146,61 @@ def test_the_harness_catches_a_planted_mistake(compile_and_run, plant):
     assert plant[0] in body
     res = compile_and_run(body.replace(plant[0], plant[1]), "planted")
     assert res.returncode != 0 and "FAIL" in res.stdout
+
+
+WINDOW_MAIN = r"""
+template <int K> static void check_k() {
+    uint8_t pair[32];
+    for (int i = 0; i < 32; ++i) pair[i] = (uint8_t)(i * 29 + 7);
+    uint4 a, b;
+    std::memcpy(&a, pair, 16);
+    std::memcpy(&b, pair + 16, 16);
+    for (uint32_t r = 0; r < 32; r += 8) {
+        const uint4 w = window_at<K>(a, b, r);
+        uint8_t got[16];
+        std::memcpy(got, &w, 16);
+        const uint32_t sh = 4 * K + r / 8;   // the window starts at byte sh of the pair
+        for (int i = 0; i < 16; ++i)
+            if (got[i] != pair[sh + i]) {
+                std::printf("K=%d r=%u: byte %d\n", K, r, i);
+                bad = 1;
+                return;
+            }
+    }
+}
+int main() {
+    check_k<0>();
+    check_k<1>();
+    check_k<2>();
+    check_k<3>();
+    std::printf(bad ? "FAIL\n" : "ok\n");
+    return bad;
+}
+"""
+
+
+def cut_window():
+    text = open(SNAC).read()
+    start = text.index("template <int K>\n__device__ __forceinline__ uint4 window_at(")
+    end = text.index("\n}\n", start) + 3
+    body = text[start:end].replace("__device__ __forceinline__", "static inline")
+    assert "window_at(" in body and "__device__" not in body
+    return body
+
+
+def test_window_at_is_the_byte_window_of_the_pair(tmp_path):
+    gxx = shutil.which("g++")
+    if gxx is None:
+        pytest.skip("no host C++ compiler")
+    for name, body in (("shipped", cut_window()),
+                       ("planted", cut_window().replace("w[K + 3], w[K + 4], r)",
+                                                        "w[K + 3], w[K + 3], r)"))):
+        src = tmp_path / f"{name}.cpp"
+        src.write_text(PRELUDE + body + WINDOW_MAIN)
+        exe = tmp_path / name
+        subprocess.run([gxx, "-std=c++17", "-O1", str(src), "-o", str(exe)], check=True)
+        res = subprocess.run([str(exe)], capture_output=True, text=True)
+        if name == "shipped":
+            assert res.returncode == 0, res.stdout
+        else:
+            assert res.returncode != 0 and "FAIL" in res.stdout
