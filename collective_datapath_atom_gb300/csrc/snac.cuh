@@ -51,7 +51,7 @@
 namespace purlin {
 namespace snac {
 
-constexpr int kNotifyBatch = 8;                   // flags published behind one fence
+constexpr int kNotifyBatch = 4;                   // flags published behind one fence
 constexpr uint64_t kRingWaitNs = 2000000000ull;   // 2 s bound on a ring wait
 constexpr int kSmemSegs = 64;                     // segment table entries staged in the ring's workspace
 

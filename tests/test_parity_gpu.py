@@ -553,7 +553,8 @@ def test_composed_allreduce_wide_R(P, R):
         P.purlin_set_option(ctx, P.PURLIN_OPT_AR_MODE, 2)
         # the last case, with 256-byte chunks, has enough reducing chunks for
         # the ring to interleave its gathering chunks (more than lag + 1
-        # groups of R: lag = 12 * 152 // (R + 1) groups on 152 CTAs)
+        # groups of R: lag = 8 * 152 // (R + 1) groups on 152 CTAs, with the
+        # ring's flag batches of 4)
         for k, (n, chunk) in enumerate(((R * 16 * 3 + 5, 0), (70001, 0), (300007, 256))):
             P.purlin_set_option(ctx, P.PURLIN_OPT_CHUNK_BYTES, chunk)
             ins = gen_inputs([n] * R, 1, seed=5000 + k + R)
