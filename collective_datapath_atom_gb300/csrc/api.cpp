@@ -48,8 +48,8 @@ Policy policy_for(purlin_collective coll, int R) {
             return {clamp16(32768 / (uint64_t)R, 512, 8192), 3, 16ull << 20, true, 0, 1};
         case PURLIN_COLL_ALL_GATHER:
             return {16384, 4, 1ull << 20, true, 8, 1};
-        case PURLIN_COLL_ALL_GATHER_V:
-            return {16384, 4, 2ull << 20, true, 8, 1};
+        case PURLIN_COLL_ALL_GATHER_V:   // a Zipf split's largest input is 1.18x the mean
+            return {16384, 4, 3ull << 20, true, 8, 1};
         default:   // AllToAll(V): two CTAs per SM
             return {16384, 3, 256ull << 10, false, 0, 2};
     }

@@ -31,7 +31,7 @@ constexpr int kShiftedCopyConsumerWarps = 6;
 // to tens of MiB: ReduceScatter and ReduceScatterV 32 MiB (ragged blocks
 // read aligned on both paths; at 64 MiB the ring leads, 0.97 of the copy
 // peak against 0.92), AllReduce 16 MiB (at 32 MiB the two variants trade
-// places from box to box), AllGather 1 MiB, AllGatherV 2 MiB, AllToAll(V)
+// places from box to box), AllGather 1 MiB, AllGatherV 3 MiB, AllToAll(V)
 // 256 KiB.
 // Ring shape:
 //   ReduceScatter(V)  one destination per reduced chunk: large per-source
