@@ -120,12 +120,16 @@ purlin_status ring_shape(const purlin_ctx *ctx, const CallDesc &c, const Policy 
     return PURLIN_OK;
 }
 
-// Per-parity flag slots for a grid of `grid` CTAs (a multiple of the grid,
-// so a slot is always reused by the CTA that owns its chunks) and the odd
-// epoch increment that keeps every generation of a call distinct.
-void flag_geometry(uint64_t notify_chunks, int64_t grid, uint32_t *slots, uint64_t *epoch_inc) {
+// Per-parity flag slots for a grid of `grid` CTAs and the odd epoch
+// increment that keeps every generation of a call distinct.  The slots are a
+// multiple of the grid: when a call reuses them, notifying chunks number
+// their flags by walk position (flag_at in plan.h), and positions pos and
+// pos + slots then belong to the same CTA.  Those positions stay below the
+// call's chunk count.
+void flag_geometry(uint64_t notify_chunks, uint64_t nchunks, int64_t grid, uint32_t *slots,
+                   uint64_t *epoch_inc) {
     *slots = (kFlagSlots / (uint32_t)grid) * (uint32_t)grid;
-    uint64_t gens = (notify_chunks + *slots - 1) / *slots;
+    uint64_t gens = notify_chunks <= *slots ? 1 : (nchunks + *slots - 1) / *slots;
     if (gens == 0) gens = 1;
     *epoch_inc = gens | 1ull;   // odd: the parity flips every call
 }
@@ -382,9 +386,10 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
         a.cooperative = pl.composed;
         a.vector_copies = vector_copies;
         if (pl.composed) {
-            // flag slot reuse stays on one CTA (slots a multiple of the grid),
-            // so a later generation of a slot implies the earlier one landed.
-            flag_geometry(pl.notify_chunks, grid, &a.flag_slots, &epoch_inc);
+            // A reused flag slot is numbered by walk position, which keeps it
+            // on one CTA (slots a multiple of the grid), so a later
+            // generation of a slot implies the earlier one landed.
+            flag_geometry(pl.notify_chunks, pl.nchunks, grid, &a.flag_slots, &epoch_inc);
             a.dev_epoch = ctx->dev_epoch;
             a.epoch_inc = epoch_inc;
         }

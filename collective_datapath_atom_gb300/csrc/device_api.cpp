@@ -94,7 +94,7 @@ purlin_status purlin_device_prepare(purlin_ctx *ctx, purlin_collective coll,
         cudaMalloc(&m.err, sizeof(unsigned long long)) != cudaSuccess)
         return fail(PURLIN_ERR_OOM);
     if (pl.composed) {
-        flag_geometry(pl.notify_chunks, blocks, &d.flag_slots, &d.epoch_inc);
+        flag_geometry(pl.notify_chunks, pl.nchunks, blocks, &d.flag_slots, &d.epoch_inc);
         if (cudaMalloc(&m.flags, 2 * (size_t)d.flag_slots * sizeof(unsigned long long)) !=
             cudaSuccess)
             return fail(PURLIN_ERR_OOM);

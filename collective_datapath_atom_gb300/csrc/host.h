@@ -118,7 +118,8 @@ namespace host {
 
 purlin_status ring_shape(const purlin_ctx *ctx, const CallDesc &c, const Policy &shape,
                          const Plan &pl, uint32_t limit, RingShape *out);
-void flag_geometry(uint64_t notify_chunks, int64_t grid, uint32_t *slots, uint64_t *epoch_inc);
+void flag_geometry(uint64_t notify_chunks, uint64_t nchunks, int64_t grid, uint32_t *slots,
+                   uint64_t *epoch_inc);
 int ring_ar_mode(const purlin_ctx *ctx);
 Policy call_policy(const purlin_ctx *ctx, const CallDesc &c);
 

@@ -155,6 +155,38 @@ PURLIN_HD inline uint64_t chunk_at(const ChunkOrder &o, uint64_t pos64) {
     return pos - (before < o.g1 ? before : o.g1);      // (all g1, once ng < nr / R runs out)
 }
 
+// The walk position of reducing chunk d < nr: the inverse of chunk_at on the
+// reducing chunks.  Before base they keep their own positions; after it each
+// group of R follows one interleaved gathering chunk, until all g1 of them
+// are placed.
+PURLIN_HD inline uint64_t walk_pos(const ChunkOrder &o, uint64_t d) {
+    if (o.ng == 0 || d < o.base) return d;
+    const uint64_t q1 = (d - o.base) / o.R + 1u;   // gathering chunks placed before d
+    return d + (q1 < o.g1 ? q1 : o.g1);
+}
+
+// The flag a notifying chunk d publishes (slot, generation), with F slots per
+// parity.  When every notifying chunk has a slot of its own, slot = d.  When
+// slots are reused (more than F notifying chunks), chunks are numbered by
+// their walk position: F is a multiple of the grid, so position pos and
+// pos + F belong to the same CTA, which publishes them in that order, and a
+// slot's value only grows during a call.  Numbered by chunk instead, chunks d
+// and d + F can sit on different CTAs under the interleaved walk, and a
+// consumer of d could pass on d + F's flag before d is stored.  Every
+// position of a call is below its chunk count, so ceil(nchunks / F)
+// generations cover it.
+struct FlagAt {
+    uint64_t slot, gen;
+};
+
+PURLIN_HD inline FlagAt flag_at(const ChunkOrder &o, uint64_t F, uint64_t d) {
+    const uint64_t i = o.nr <= F ? d : walk_pos(o, d);
+    FlagAt f;
+    f.slot = i % F;
+    f.gen = i / F;
+    return f;
+}
+
 // Vector units covering the bytes [grid + a, grid + b) of a segment whose
 // units follow the 16-byte grid of offset `grid`: one unit per window.
 PURLIN_HD inline uint64_t units_in(uint64_t grid, uint64_t a, uint64_t b) {

@@ -351,11 +351,12 @@ __device__ __forceinline__ bool ring_wait(uint64_t *bar, uint32_t parity, volati
 // acquire before the bulk load lane 0 issues next.
 template <class P>
 __device__ void acquire_range(const P &p, const unsigned long long *flags, uint64_t epoch,
-                              uint64_t d0, uint64_t d1, int lane) {
+                              const ChunkOrder &order, uint64_t d0, uint64_t d1, int lane) {
     for (uint64_t d = d0 + (uint64_t)lane; d < d1; d += 32) {
         if (error_set(p.err)) break;
-        const unsigned long long *f = flags + (d % p.flag_slots);
-        const unsigned long long want = epoch + d / p.flag_slots;
+        const FlagAt fa = flag_at(order, p.flag_slots, d);
+        const unsigned long long *f = flags + fa.slot;
+        const unsigned long long want = epoch + fa.gen;
         if (atom::flag_acquire(f) >= want) continue;
         const uint64_t t0 = atom::globaltimer_ns();
         uint32_t ns = 32;
@@ -376,9 +377,10 @@ __device__ void acquire_range(const P &p, const unsigned long long *flags, uint6
 // ordered before this store by the caller).
 template <class P>
 __device__ __forceinline__ void notify_chunk(const P &p, unsigned long long *flags, uint64_t epoch,
-                                             uint64_t c) {
+                                             const ChunkOrder &order, uint64_t c) {
     if ((int64_t)c == p.drop_notify) return;   // host-side fault injection
-    atom::flag_release(flags + (c % p.flag_slots), epoch + c / p.flag_slots);
+    const FlagAt fa = flag_at(order, p.flag_slots, c);
+    atom::flag_release(flags + fa.slot, epoch + fa.gen);
 }
 
 // ------------------------------------------------------ device epoch --
@@ -568,7 +570,7 @@ __device__ void run_ring(const P &p, unsigned char *smem, Ctl *ctl_p, uint32_t b
                 const uint64_t nred = (sg.bytes - sg.head - sg.tail + rc - 1) / rc;
                 const uint64_t d0 = g.ci * ratio;
                 const uint64_t d1 = d0 + ratio < nred ? d0 + ratio : nred;
-                acquire_range(p, flags, epoch, sg.dep_chunk + d0, sg.dep_chunk + d1, lane);
+                acquire_range(p, flags, epoch, order, sg.dep_chunk + d0, sg.dep_chunk + d1, lane);
             }
             unsigned char *sp = ring + (size_t)slot * p.slot_stride;
             const int nsrc = sg.src_rank < 0 ? R : 1;
@@ -615,7 +617,7 @@ __device__ void run_ring(const P &p, unsigned char *smem, Ctl *ctl_p, uint32_t b
         auto publish = [&]() {
             if (lane == 0 && npend > 0) {
                 atom::fence_acq_rel_gpu();   // the consumer warps' stores, at GPU scope
-                for (int i = 0; i < npend; ++i) notify_chunk(p, flags, epoch, pend[i]);
+                for (int i = 0; i < npend; ++i) notify_chunk(p, flags, epoch, order, pend[i]);
             }
             npend = 0;
         };

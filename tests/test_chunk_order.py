@@ -134,3 +134,106 @@ def test_interleaving_starts_after_the_lag_and_plans_without_flags_keep_their_or
     assert sorted(few) == list(range(4100))
     assert [c for c in few if c >= 4000] == list(range(4000, 4100))
     assert few[-1] == 3999 and few[203 * 8 + 99 * 9] == 4099
+
+
+FLAG_DRIVER = r"""
+#include <cstdio>
+#include "plan.h"
+int main() {
+    unsigned long long nr, ng, ctas, batch, F;
+    int R;
+    while (std::scanf("%llu %llu %d %llu %llu %llu", &nr, &ng, &R, &ctas, &batch, &F) == 6) {
+        const purlin::ChunkOrder o = purlin::make_chunk_order(nr, ng, R, (uint32_t)ctas, (int)batch);
+        for (unsigned long long d = 0; d < nr; ++d) {
+            const purlin::FlagAt f = purlin::flag_at(o, F, d);
+            std::printf("%llu %llu %llu ", (unsigned long long)purlin::walk_pos(o, d),
+                        (unsigned long long)f.slot, (unsigned long long)f.gen);
+        }
+        std::printf("\n");
+    }
+    return 0;
+}
+"""
+
+
+@pytest.fixture(scope="module")
+def flags(tmp_path_factory):
+    """flags(cases) -> per (nr, ng, R, ctas, batch, F) case, a list of
+    (walk position, slot, generation) for every notifying chunk d < nr."""
+    gxx = shutil.which("g++")
+    if gxx is None:
+        pytest.skip("no host C++ compiler")
+    d = tmp_path_factory.mktemp("flag_at")
+    src = d / "driver.cpp"
+    src.write_text(FLAG_DRIVER)
+    exe = d / "driver"
+    subprocess.run([gxx, "-std=c++17", "-O1",
+                    "-I", os.path.join(ROOT, "collective_datapath_atom_gb300", "csrc"),
+                    str(src), "-o", str(exe)], check=True)
+
+    def run(cases):
+        text = "".join(" ".join(str(v) for v in c) + "\n" for c in cases)
+        out = subprocess.run([str(exe)], input=text, capture_output=True, text=True, check=True)
+        res = []
+        for line in out.stdout.splitlines():
+            v = [int(x) for x in line.split()]
+            res.append(list(zip(v[0::3], v[1::3], v[2::3])))
+        return res
+
+    return run
+
+
+def _slots_per_parity(ctas):
+    return (65536 // ctas) * ctas   # the context's flag_geometry: a multiple of the grid
+
+
+@pytest.mark.parametrize("R", [2, 3, 8, 31])
+def test_reused_flag_slots_stay_on_one_cta_in_walk_order(walk, flags, R):
+    """A consumer of notifying chunk d waits for its slot to reach this
+    call's generation for d.  That is sound only if the slot's earlier
+    generations are published before d and its later ones after: the slot's
+    chunks must sit on one CTA, in walk order.  Checked with the walk itself
+    (chunk_at), for plans with more notifying chunks than slots (the slots
+    are then numbered by walk position) and plans with fewer (one slot per
+    chunk, generation 0)."""
+    for ctas in (7, 152, 304):
+        F = _slots_per_parity(ctas)
+        cases = []
+        for nr in (F - 1, F, F + 1, 2 * F + 12345, 3 * F + 7):
+            ng = -(-nr // R)
+            cases.append((nr, ng, R, ctas, 4, F))
+        seqs = walk([c[:5] for c in cases])
+        for (nr, ng, _, _, _, _), seq, fl in zip(cases, seqs, flags(cases)):
+            assert len(fl) == nr
+            by_slot = {}
+            for d, (pos, slot, gen) in enumerate(fl):
+                assert seq[pos] == d, "walk_pos is not the inverse of chunk_at"
+                assert slot < F
+                if nr <= F:
+                    assert (slot, gen) == (d, 0)
+                else:
+                    assert (slot, gen) == (pos % F, pos // F)
+                    assert gen < -(-(nr + ng) // F)   # the epoch increment covers it
+                by_slot.setdefault(slot, []).append((gen, pos))
+            for slot, uses in by_slot.items():
+                uses.sort()
+                owners = {pos % ctas for _, pos in uses}
+                assert len(owners) == 1, (nr, slot, uses[:4])
+                positions = [pos for _, pos in uses]
+                assert positions == sorted(positions)
+                gens = [g for g, _ in uses]
+                assert all(a < b for a, b in zip(gens, gens[1:])), (slot, gens)
+
+
+def test_chunk_numbered_slots_would_cross_ctas(walk):
+    """The reason for walk-position numbering: under the interleaved walk,
+    notifying chunks d and d + F (numbered by chunk) usually land on
+    different CTAs, so a consumer of d could pass on d + F's flag."""
+    ctas, R = 152, 8
+    F = _slots_per_parity(ctas)
+    nr = F + 5000
+    ng = -(-nr // R)
+    seq, = walk([(nr, ng, R, ctas, 4)])
+    pos = {c: p for p, c in enumerate(seq)}
+    crossing = sum(pos[d] % ctas != pos[d + F] % ctas for d in range(nr - F))
+    assert crossing > 0
