@@ -35,15 +35,20 @@ _lib = None
 _CFLAGS = ["-O2", "-std=c99", "-fno-fast-math", "-ffp-contract=off", "-fPIC", "-shared"]
 
 
-def build(force: bool = False) -> str:
-    """Compile ``purlin_oracle.c`` into ``liboracle.so`` beside it."""
-    if force or not os.path.exists(_LIB_PATH) or (
-        os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
-    ):
-        tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", *_CFLAGS, "-o", tmp, _SRC])
-        os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+_OMP_LIB_PATH = os.path.join(_HERE, "liboracle_omp.so")
+
+
+def build(force: bool = False, openmp: bool = False) -> str:
+    """Compile ``purlin_oracle.c`` into ``liboracle.so`` beside it, or with
+    ``openmp`` into ``liboracle_omp.so``: the same loops, their element
+    ranges split over the host's cores (the CPU baseline's second leg)."""
+    path = _OMP_LIB_PATH if openmp else _LIB_PATH
+    if force or not os.path.exists(path) or os.path.getmtime(path) < os.path.getmtime(_SRC):
+        tmp = path + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", *_CFLAGS, *(["-fopenmp"] if openmp else []), "-o", tmp,
+                               _SRC])
+        os.replace(tmp, path)
+    return path
 
 
 def _bind(lib):
@@ -64,6 +69,11 @@ def _bind(lib):
         f = getattr(lib, name)
         f.restype = ctypes.c_int
         f.argtypes = [ctypes.c_int, szp, ctypes.c_int, vpp, vpp]
+    lib.oracle_threads.restype = ctypes.c_int
+    lib.oracle_threads.argtypes = [ctypes.c_int]
+    lib.oracle_all_reduce_one.restype = ctypes.c_int
+    lib.oracle_all_reduce_one.argtypes = [ctypes.c_int, ctypes.c_size_t, ctypes.c_int, vpp,
+                                          ctypes.c_void_p]
     lib.oracle_reduce_at.restype = ctypes.c_int
     lib.oracle_reduce_at.argtypes = [ctypes.c_int, ctypes.c_int, vpp, ctypes.c_size_t,
                                      ctypes.c_void_p]
@@ -96,6 +106,29 @@ def compile_variant(src_text: str, out_path: str) -> str:
 def source_text() -> str:
     with open(_SRC) as f:
         return f.read()
+
+
+class openmp:
+    """Context manager: route this module's functions to the OpenMP build
+    with ``threads`` threads (0: the runtime's default) inside a ``with``
+    block; ``.threads`` is the count the element loops then use."""
+
+    def __init__(self, threads: int = 0):
+        self._want = threads
+        self._saved = None
+        self.threads = 1
+
+    def __enter__(self):
+        global _lib
+        self._saved = _lib
+        _lib = _bind(ctypes.CDLL(build(openmp=True)))
+        self.threads = int(_lib.oracle_threads(self._want))
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self._saved
+        return False
 
 
 class use_library:
@@ -206,6 +239,15 @@ def all_reduce(inputs: Sequence[np.ndarray], dtype: int) -> list[np.ndarray]:
     R, n = len(inputs), int(inputs[0].size)
     out = _outs(R, n, dtype)
     _check(_load().oracle_all_reduce(R, n, dtype, _ptrs(inputs), _ptrs(out)), "all_reduce")
+    return out
+
+
+def all_reduce_one(inputs: Sequence[np.ndarray], dtype: int) -> np.ndarray:
+    """One AllReduce output, rnd(sum_s in_s[i]): every destination's value."""
+    R, n = len(inputs), int(inputs[0].size)
+    out = np.zeros(n, dtype=_np_dtype(dtype))
+    _check(_load().oracle_all_reduce_one(R, n, dtype, _ptrs(inputs),
+                                         ctypes.c_void_p(out.ctypes.data)), "all_reduce_one")
     return out
 
 

@@ -38,13 +38,38 @@
  * Build: gcc -O2 -fno-fast-math -ffp-contract=off -std=c99 -shared -fPIC.
  * Each float addition below is one IEEE binary32 addition (FLT_EVAL_METHOD
  * 0 on both x86-64 SSE and AArch64), so the result is fixed by the order.
+ *
+ * The same source is also built with -fopenmp, for the CPU baseline leg of
+ * the benchmark over all host cores.  Only the element loops are split
+ * across threads (PARALLEL_ELEMENTS); each element is still computed by one
+ * thread with the same operations in the same order, so both builds give
+ * the same bits.  Without -fopenmp the macro is empty.
  */
 #include <stddef.h>
 #include <stdint.h>
 #include <string.h>
 
+#ifdef _OPENMP
+#include <omp.h>
+#define PARALLEL_ELEMENTS _Pragma("omp parallel for schedule(static)")
+#else
+#define PARALLEL_ELEMENTS
+#endif
+
 #define ORACLE_F32 0
 #define ORACLE_BF16 1
+
+/* Threads the element loops use: sets the count first when k > 0.  The
+ * single-threaded build ignores k and returns 1. */
+int oracle_threads(int k) {
+#ifdef _OPENMP
+    if (k > 0) omp_set_num_threads(k);
+    return omp_get_max_threads();
+#else
+    (void)k;
+    return 1;
+#endif
+}
 
 /* ------------------------------------------------------------------ */
 /* bf16 codec, written from the definition of the formats.             */
@@ -148,6 +173,7 @@ int oracle_all_gather(int R, size_t n, int dtype, const void *const *in, void *c
     if (R < 1 || es == 0) return -1;
     for (int d = 0; d < R; ++d)
         for (int s = 0; s < R; ++s)
+            PARALLEL_ELEMENTS
             for (size_t i = 0; i < n; ++i)
                 copy_elem(out[d], (size_t)s * n + i, in[s], i, es);
     return 0;
@@ -163,6 +189,7 @@ int oracle_all_gather_v(int R, const size_t *counts, int dtype, const void *cons
     exclusive_scan(R, counts, 1, D);
     for (int d = 0; d < R; ++d)
         for (int s = 0; s < R; ++s)
+            PARALLEL_ELEMENTS
             for (size_t i = 0; i < counts[s]; ++i)
                 copy_elem(out[d], D[s] + i, in[s], i, es);
     return 0;
@@ -175,6 +202,7 @@ int oracle_reduce_scatter(int R, size_t n, int dtype, const void *const *in, voi
     if (R < 1 || elem_size(dtype) == 0 || n % (size_t)R != 0) return -1;
     size_t M = n / (size_t)R;
     for (int r = 0; r < R; ++r)
+        PARALLEL_ELEMENTS
         for (size_t i = 0; i < M; ++i)
             store_rounded(dtype, out[r], i, ordered_sum(R, dtype, in, (size_t)r * M + i));
     return 0;
@@ -189,6 +217,7 @@ int oracle_reduce_scatter_v(int R, const size_t *counts, int dtype, const void *
     size_t D[1024];
     exclusive_scan(R, counts, 1, D);
     for (int r = 0; r < R; ++r)
+        PARALLEL_ELEMENTS
         for (size_t i = 0; i < counts[r]; ++i)
             store_rounded(dtype, out[r], i, ordered_sum(R, dtype, in, D[r] + i));
     return 0;
@@ -201,8 +230,19 @@ int oracle_reduce_scatter_v(int R, const size_t *counts, int dtype, const void *
 int oracle_all_reduce(int R, size_t n, int dtype, const void *const *in, void *const *out) {
     if (R < 1 || elem_size(dtype) == 0) return -1;
     for (int d = 0; d < R; ++d)
+        PARALLEL_ELEMENTS
         for (size_t i = 0; i < n; ++i)
             store_rounded(dtype, out[d], i, ordered_sum(R, dtype, in, i));
+    return 0;
+}
+
+/* One AllReduce output: every destination holds the same values by the
+ * contract above, out[i] = rnd(sum_s in_s[i]), so a test of a large call
+ * needs this array only once. */
+int oracle_all_reduce_one(int R, size_t n, int dtype, const void *const *in, void *out) {
+    if (R < 1 || elem_size(dtype) == 0) return -1;
+    PARALLEL_ELEMENTS
+    for (size_t i = 0; i < n; ++i) store_rounded(dtype, out, i, ordered_sum(R, dtype, in, i));
     return 0;
 }
 
@@ -215,6 +255,7 @@ int oracle_all_to_all(int R, size_t n, int dtype, const void *const *in, void *c
     size_t M = n / (size_t)R;
     for (int d = 0; d < R; ++d)
         for (int s = 0; s < R; ++s)
+            PARALLEL_ELEMENTS
             for (size_t i = 0; i < M; ++i)
                 copy_elem(out[d], (size_t)s * M + i, in[s], (size_t)d * M + i, es);
     return 0;
@@ -233,6 +274,7 @@ int oracle_all_to_all_v(int R, const size_t *C, int dtype, const void *const *in
         exclusive_scan(R, C + d, (size_t)R, Q); /* column d: C[0][d], C[1][d], ... */
         for (int s = 0; s < R; ++s) {
             exclusive_scan(R, C + (size_t)s * R, 1, S); /* row s */
+            PARALLEL_ELEMENTS
             for (size_t i = 0; i < C[(size_t)s * R + d]; ++i)
                 copy_elem(out[d], Q[s] + i, in[s], S[d] + i, es);
         }

@@ -155,6 +155,7 @@ def check_golden_score_order():
     outs = oracle.all_reduce(ins, F32)
     for o in outs:
         assert np.array_equal(o.view(np.uint32), want), (o.view(np.uint32), want)
+    assert np.array_equal(oracle.all_reduce_one(ins, F32).view(np.uint32), want)
 
 
 def check_golden_round_once():
@@ -164,6 +165,42 @@ def check_golden_round_once():
         want = _bf16_from_hex(case["output_bf16_hex"])
         for o in oracle.all_reduce(ins, BF16):
             assert np.array_equal(o, want), (o, want)
+        assert np.array_equal(oracle.all_reduce_one(ins, BF16), want)
+
+
+def _specials_match(got_bits, want_hex, dtype):
+    """The fixture's rule: "nan" matches any NaN, every other value bit for bit."""
+    got_bits = np.asarray(got_bits).astype(np.uint32)
+    exp_mask, man_mask = (0x7F800000, 0x007FFFFF) if dtype == F32 else (0x7F80, 0x007F)
+    for i, w in enumerate(want_hex):
+        g = int(got_bits[i])
+        if w == "nan":
+            assert (g & exp_mask) == exp_mask and (g & man_mask) != 0, (i, hex(g))
+        else:
+            assert g == int(w, 16), (i, hex(g), w)
+
+
+def check_golden_specials():
+    """NaN, infinities, overflow and subnormals in the ordered sum, worked by
+    hand (tests/golden/score_specials.json): AllReduce, ReduceScatterV over
+    a split of the same elements, and single points."""
+    g = _load_golden("score_specials.json")
+    for name, dtype in (("f32", F32), ("bf16", BF16)):
+        case = g[name]
+        ins = [_f32_from_hex(r) if dtype == F32 else _bf16_from_hex(r) for r in case["inputs_hex"]]
+        want = case["output_hex"]
+        for o in oracle.all_reduce(ins, dtype):
+            _specials_match(_bits(o), want, dtype)
+        _specials_match(_bits(oracle.all_reduce_one(ins, dtype)), want, dtype)
+        n = len(want)
+        counts = [n // 3 + (1 if r < n % 3 else 0) for r in range(3)]
+        outs = oracle.reduce_scatter_v(ins, counts, dtype)
+        at = 0
+        for r, c in enumerate(counts):
+            _specials_match(_bits(outs[r]), want[at:at + c], dtype)
+            at += c
+        for i in range(n):
+            _specials_match(_bits(np.array([oracle.reduce_at(ins, dtype, i)])), [want[i]], dtype)
 
 
 def _run_collective(case, dtype):
@@ -209,6 +246,8 @@ def check_exact_integer_sums():
                 ins = [_as_dtype(x.astype(np.float32), dtype) for x in ints]
                 for o in oracle.all_reduce(ins, dtype):
                     assert np.array_equal(_f32_of(o, dtype), exact.astype(np.float64))
+                assert np.array_equal(_f32_of(oracle.all_reduce_one(ins, dtype), dtype),
+                                      exact.astype(np.float64))
                 rs = oracle.reduce_scatter(ins, dtype)
                 for r in range(R):
                     assert np.array_equal(_f32_of(rs[r], dtype),
@@ -346,6 +385,7 @@ def check_points_match_full():
         xs = [rng.standard_normal(n).astype(np.float32) for _ in range(R)]
         ins = xs if dtype == F32 else [ref_bf16_rne(x.view(np.uint32)) for x in xs]
         full = oracle.all_reduce(ins, dtype)[0]
+        assert np.array_equal(_bits(oracle.all_reduce_one(ins, dtype)), _bits(full))
         for i in (0, 1, 31, 63):
             assert _bits(np.array([oracle.reduce_at(ins, dtype, i)]))[0] == _bits(full)[i]
     C = rng.integers(0, 4, size=(4, 4))
@@ -360,6 +400,7 @@ def check_points_match_full():
 
 PINS = [check_codec_definition, check_codec_specials, check_codec_vs_torch,
         check_golden_score_order, check_golden_round_once, check_golden_contracts,
+        check_golden_specials,
         check_exact_integer_sums, check_error_bound, check_all_gather_concat,
         check_rs_then_ag_is_ar, check_a2a_inverse, check_uniform_v_equals_plain,
         check_single_rank_is_copy, check_points_match_full]
@@ -478,3 +519,35 @@ def test_planted_mistake_is_caught(name, tmp_path):
     caught = proc.returncode != 0 or any(
         line.startswith("FAILED:") and line != "FAILED:" for line in proc.stdout.splitlines())
     assert caught, f"no pin caught the planted mistake {name}: {proc.stdout[-500:]}"
+
+
+def test_openmp_build_gives_the_same_bits():
+    """The CPU baseline's OpenMP build splits the element loops over threads;
+    each element keeps its one thread and its order, so every collective
+    returns the single-threaded build's bits."""
+    rng = np.random.default_rng(23)
+    R, n = 8, 8 * 4099
+    xs32 = [rng.standard_normal(n).astype(np.float32) for _ in range(R)]
+    xs16 = [ref_bf16_rne(x.view(np.uint32)) for x in xs32]
+    counts = list(rng.multinomial(n, np.ones(R) / R))
+    C = rng.integers(0, 600, size=(R, R))
+    a2av = [ref_bf16_rne(rng.standard_normal(int(C[s].sum())).astype(np.float32).view(np.uint32))
+            for s in range(R)]
+
+    def run_all():
+        out = []
+        for dtype, xs in ((F32, xs32), (BF16, xs16)):
+            out += oracle.all_reduce(xs, dtype) + [oracle.all_reduce_one(xs, dtype)]
+            out += oracle.reduce_scatter(xs, dtype) + oracle.reduce_scatter_v(xs, counts, dtype)
+            out += oracle.all_gather(xs, dtype) + oracle.all_gather_v(
+                [x[:c] for x, c in zip(xs, counts)], counts, dtype)
+            out += oracle.all_to_all(xs, dtype)
+        return out + oracle.all_to_all_v(a2av, C, BF16)
+
+    serial = run_all()
+    with oracle.openmp(4) as omp:
+        assert omp.threads == 4
+        parallel = run_all()
+    assert len(serial) == len(parallel)
+    for a, b in zip(serial, parallel):
+        assert np.array_equal(_bits(a), _bits(b))
