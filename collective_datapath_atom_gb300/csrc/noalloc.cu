@@ -36,8 +36,9 @@
 // than any value already stored); the error word is cleared per call.
 // Calls whose kernels overlap on the GPU (e.g. issued on two streams
 // without ordering) race on the flags and give wrong results: order them.
-// A device-side wait that expires is recorded in the error word but not
-// reported by this entry point.
+// A device-side wait that expires (100 ms bound) is recorded in the error
+// word, which no call reads back and the next call clears: a caller cannot
+// learn that it happened, and that call's outputs are then unspecified.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -140,8 +141,9 @@ extern "C" purlin_status purlin_all_reduce_noalloc(int R, const void *const src[
 
     const uint32_t slot_stride = (pl.slot_bytes + 127u) & ~127u;
     const uint32_t limit = (uint32_t)ds.max_smem - 1024;
-    uint32_t stages = kStages;
-    while (stages > 2 && throughput_smem(stages, slot_stride) > limit) --stages;
+    const uint32_t stages = kStages;
+    // Two 96 KiB stages and the ring's barriers and table: about 193 KiB of
+    // dynamic shared memory per CTA.  A device with less returns UNSUPPORTED.
     const uint32_t smem = throughput_smem(stages, slot_stride);
     if (smem > limit) return PURLIN_ERR_UNSUPPORTED;
     const int block = 32 * (2 + kConsumerWarps);

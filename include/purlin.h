@@ -234,9 +234,13 @@ purlin_status purlin_all_to_all_v_device_counts(purlin_ctx *ctx, const void *con
  * sets kernel attributes and zeroes the array with a blocking cudaMemset:
  * make it before any stream capture.  Every call shares the array (it keeps
  * the previous call's contents; the error word is cleared per call), so
- * calls that overlap on the GPU race: order them on one stream.  Device-side
- * timeouts are not reported here.  Errors as for purlin_all_reduce, plus
- * CUDA if the set-up or the launch fails. */
+ * calls that overlap on the GPU race: order them on one stream.  A caller
+ * cannot learn that a device-side wait expired: the kernel records it in the
+ * array's error word (100 ms bound per wait, then the launch ends early and
+ * that call's outputs are unspecified), but nothing reads that word back and
+ * the next call clears it.  Needs about 193 KiB of dynamic shared memory per
+ * CTA (two 96 KiB stages); a device with less returns UNSUPPORTED.  Errors
+ * as for purlin_all_reduce, plus CUDA if the set-up or the launch fails. */
 purlin_status purlin_all_reduce_noalloc(int R, const void *const src[], void *const dst[],
                                         size_t n, purlin_dtype dtype, purlin_op op,
                                         purlin_layout layout, purlin_stream stream);

@@ -4,9 +4,9 @@ Some callers cannot call cudaMalloc when they reduce: code running under
 CUDA graph capture, or an engine that has already given all free device
 memory to its own pool.  This entry point keeps its scratch (flags and an
 error word) in a fixed device array inside the library instead of memory the
-context allocates.  Its output must equal, bit for bit, the output of the
-context entry point purlin_all_reduce in the composed mode, which runs the
-same kernel on the same fixed rank order.
+context allocates.  Its output must equal, bit for bit, the CPU oracle's
+AllReduce and the output of the context entry point purlin_all_reduce in
+the composed mode, which runs the same kernel on the same fixed rank order.
 
 This file is collected last so that a run stopping at its first failure has
 already run every other test.  It builds what it needs and also passes when
@@ -17,6 +17,7 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 import workloads
 
 torch = pytest.importorskip("torch")
@@ -36,12 +37,21 @@ def P():
     return mod
 
 
+def _host_inputs(R, n, dtype, seed):
+    return workloads.normals(seed, R, n, workloads.F32 if dtype == 0 else workloads.BF16)
+
+
 def _inputs(R, n, dtype, seed):
+    xs = _host_inputs(R, n, dtype, seed)
     if dtype == 0:
-        xs = workloads.normals(seed, R, n, workloads.F32)
         return [torch.from_numpy(x).cuda() for x in xs]
-    xs = workloads.normals(seed, R, n, workloads.BF16)
     return [torch.from_numpy(x.view(np.int16)).cuda() for x in xs]
+
+
+def _oracle_on_device(xs, dtype):
+    """The oracle's AllReduce output (the same for every destination)."""
+    want = oracle.all_reduce_one(xs, dtype)
+    return torch.from_numpy(want if dtype == 0 else want.view(np.int16)).cuda()
 
 
 def _call_noalloc(P, R, src, dst, n, dtype, stream):
@@ -65,7 +75,9 @@ def test_noalloc_matches_context_allreduce_twice(P, dtype, R, n):
         P.purlin_set_option(ctx, P.PURLIN_OPT_AR_MODE, 2)
         tdt = src_dtype = torch.float32 if dtype == 0 else torch.int16
         for call in range(2):    # two calls in a row share (and reuse) the static scratch
-            src = _inputs(R, n, dtype, seed=100 + call)
+            xs = _host_inputs(R, n, dtype, seed=100 + call)
+            src = [torch.from_numpy(x if dtype == 0 else x.view(np.int16)).cuda() for x in xs]
+            exact = _oracle_on_device(xs, dtype)
             want = [torch.empty(n, dtype=tdt, device="cuda") for _ in range(R)]
             got = [torch.full((n,), -1, dtype=src_dtype, device="cuda") for _ in range(R)]
             P.purlin_all_reduce(ctx, src, want, n, dtype)
@@ -74,6 +86,7 @@ def test_noalloc_matches_context_allreduce_twice(P, dtype, R, n):
             assert st == P.PURLIN_OK, P.status_string(st)
             torch.cuda.synchronize()
             for d in range(R):
+                assert torch.equal(got[d], exact), f"call {call} rank {d}: differs from the oracle"
                 assert torch.equal(got[d], want[d]), f"call {call} rank {d}"
     finally:
         ctx.close()
@@ -99,13 +112,26 @@ def test_noalloc_rejects_sizes_past_its_scratch(P):
     R = 8
     # 8192 chunks of 12 KiB per source is the limit at R = 8: 96 MiB per rank
     limit_elems = 8192 * ((98304 // R) & ~15) // 2    # bf16 elements per rank
-    src = [torch.empty(limit_elems + 4096, dtype=torch.int16, device="cuda") for _ in range(R)]
-    dst = [torch.empty(limit_elems + 4096, dtype=torch.int16, device="cuda") for _ in range(R)]
+    # small integers: every bf16 sum is exact, and the call at the limit uses
+    # the last flag of the array
+    rng = np.random.default_rng(3)
+    ints = [rng.integers(-8, 9, size=limit_elems + 4096).astype(np.float32) for _ in range(R)]
+    xs = [(x.view(np.uint32) >> 16).astype(np.uint16) for x in ints]   # exact in bf16
+    src = [torch.from_numpy(x.view(np.int16)).cuda() for x in xs]
+    dst = [torch.full((limit_elems + 4096,), -1, dtype=torch.int16, device="cuda")
+           for _ in range(R)]
     st = _call_noalloc(P, R, src, dst, limit_elems + 4096, 1, stream)
     assert st == P.PURLIN_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert all(bool((t == -1).all().item()) for t in dst), "a refused call wrote its outputs"
     st = _call_noalloc(P, R, src, dst, limit_elems, 1, stream)
     assert st == P.PURLIN_OK
     torch.cuda.synchronize()
+    want = _oracle_on_device([x[:limit_elems] for x in xs], 1)
+    for d in range(R):
+        assert torch.equal(dst[d][:limit_elems], want), f"rank {d} at the size limit"
+        assert bool((dst[d][limit_elems:] == -1).all().item()), "wrote past n"
+    del src, dst, want
     big_r = 32
     srcs = [torch.empty(64, dtype=torch.int16, device="cuda") for _ in range(big_r)]
     dsts = [torch.empty(64, dtype=torch.int16, device="cuda") for _ in range(big_r)]
