@@ -278,24 +278,28 @@ def oracle_sample_time(w, budget_s: float = 10.0):
 
 
 def run_reference(args, rank, world):
-    """Reference arm: the CPU oracle, timed as it stands, on host cores.
-    Each step is one oracle run over a sample sized so the whole run takes
-    about a minute."""
+    """Reference arm: the CPU oracle, timed as it stands, on the host's
+    cores (its OpenMP build over every core this process may use).  Each
+    step is one oracle run over a sample sized so the whole run takes about
+    a minute."""
     if rank != 0:
         return
     w = _workload_by_name(args.workload)
     import oracle
 
-    oracle.build()
-    per_step = max(0.02, 60.0 / max(1, args.steps + args.warmup))
-    fn, nbytes, desc = calibrated_sample(w, per_step)
-    for _ in range(args.warmup):
-        fn()
-    times = []
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        fn()
-        times.append(time.perf_counter() - t0)
+    cores = len(os.sched_getaffinity(0))
+    oracle.build(openmp=True)
+    with oracle.openmp(cores) as omp:
+        threads = omp.threads
+        per_step = max(0.02, 60.0 / max(1, args.steps + args.warmup))
+        fn, nbytes, desc = calibrated_sample(w, per_step)
+        for _ in range(args.warmup):
+            fn()
+        times = []
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            fn()
+            times.append(time.perf_counter() - t0)
     total = float(np.sum(times))
     value = nbytes * args.steps / total / 1e9
     line = {
@@ -306,7 +310,8 @@ def run_reference(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == workloads.BF16 else "f32", "data": "synthetic",
         "config": {"workload": w.name, "R": w.R, "elements_per_rank": w.n},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "build": f"OpenMP, {threads} threads", "cpu_model": cpu_model(),
                          "sample": desc},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -380,10 +385,203 @@ def time_steps(torch, stream, run, src, dst, steps, flush_buf, events_out, back_
     return ms
 
 
-def empty_kernel_floor(torch, P_unused=None):
-    """Launch floor with the same method (events around one launch; and a
-    CUDA graph of 1000 launches / 1000)."""
-    return None
+def _graph_per_call_us(torch, stream, fn, k, reps=5):
+    """Device time per call from a CUDA graph of k calls (median of reps
+    replays): the host's launch cost drops out."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(k):
+            fn()
+    g.replay()
+    stream.synchronize()
+    t = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        t.append(e0.elapsed_time(e1) * 1e3 / k)
+    del g
+    return float(np.median(t))
+
+
+def _graph_flushed_us(torch, stream, fn, flush, k):
+    """Device time per call with the L2 flushed before every call and no
+    launch cost: a graph of k (flush, call) pairs minus a graph of k
+    flushes, per call."""
+    both = _graph_per_call_us(torch, stream, lambda: (flush.zero_(), fn()), k)
+    only = _graph_per_call_us(torch, stream, lambda: flush.zero_(), k)
+    return both - only
+
+
+def _back_to_back_us(torch, stream, fn, k):
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(k):
+            fn()
+        e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / k
+
+
+def config_rows(P, ctx, torch, device, stream, flush, peak):
+    """Every workload of the measurement table, at its full size, timed on
+    this GPU in this run (the bench line's ``configs``).  Per row: the
+    median of single launches with the L2 flushed before each (the launch
+    floor included), the average of back-to-back launches where the inputs
+    exceed the L2, and for messages of up to 32 MiB per rank the device time
+    per call in a CUDA graph, L2 flushed and warm.  Effective GB/s =
+    algorithmic read+write bytes / time; frac = that / the measured copy
+    peak.  Inputs: the small exact-integer AllReduce from the host
+    generator; the large ones N(0,1) drawn on the device from a seeded
+    generator (the values do not change the work; the parity tests use the
+    host-generated workloads)."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(4)
+    l2 = int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0) or 0)
+    rows = []
+
+    def normals(n):
+        return torch.randn(n, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+    def measure(name, fn, algo, in_bytes, reps, graph=False):
+        fn()
+        P.purlin_check(ctx)
+        info = P.purlin_last_launch(ctx)
+        single = _events_us(torch, stream, fn, reps, flush)[0]
+        row = {"config": name, "variant": info["variant"], "grid": info["grid"],
+               "algorithmic_bytes": algo, "us_single_flushed": single,
+               "gbs_single_flushed": algo / (single * 1e-6) / 1e9}
+        row["frac_single_flushed"] = row["gbs_single_flushed"] / peak
+        if in_bytes > l2:
+            b2b = _back_to_back_us(torch, stream, fn, max(3, reps // 2))
+            row.update({"us_back_to_back": b2b, "gbs_back_to_back": algo / (b2b * 1e-6) / 1e9,
+                        "frac_back_to_back": algo / (b2b * 1e-6) / 1e9 / peak})
+        if graph:
+            k = 100 if algo < (64 << 20) else 20
+            gf = _graph_flushed_us(torch, stream, fn, flush, k)
+            gw = _graph_per_call_us(torch, stream, fn, k)
+            row.update({"us_graph_flushed": gf, "gbs_graph_flushed": algo / (gf * 1e-6) / 1e9,
+                        "frac_graph_flushed": algo / (gf * 1e-6) / 1e9 / peak,
+                        "us_graph_warm": gw, "gbs_graph_warm": algo / (gw * 1e-6) / 1e9})
+        P.purlin_check(ctx)
+        rows.append(row)
+
+    # config 1: AllReduce fp32 8 x 4096, exact integer values (latency-bound)
+    w = workloads.AR_F32_R8_4096
+    src = [torch.from_numpy(x).to(device) for x in workloads.inputs_for(w)]
+    dst = [torch.empty(w.n, dtype=torch.float32, device=device) for _ in range(8)]
+    torch.cuda.synchronize()
+    measure(w.name, lambda: P.purlin_all_reduce(ctx, src, dst, w.n, 0), 2 * 8 * w.n * 4,
+            8 * w.n * 4, 200, graph=True)
+    del src, dst
+
+    # config 3: ReduceScatter bf16 8 x 128 Mi
+    w = workloads.RS_BF16_R8_128MI
+    src = [normals(w.n) for _ in range(8)]
+    dst = [torch.empty(w.n // 8, dtype=torch.bfloat16, device=device) for _ in range(8)]
+    torch.cuda.synchronize()
+    measure(w.name, lambda: P.purlin_reduce_scatter(ctx, src, dst, w.n, 1),
+            8 * w.n * 2 + w.n * 2, 8 * w.n * 2, 10)
+    del src, dst
+    torch.cuda.empty_cache()
+
+    # config 4: AllToAllV bf16, MoE dispatch (Zipf(1.2) count matrix)
+    C, _ = workloads.moe_dispatch(payload=False)
+    counts = (C * workloads.MOE_HIDDEN).reshape(-1)
+    Cm = counts.reshape(8, 8)
+    src = [normals(int(Cm[s].sum())) for s in range(8)]
+    dst = [torch.empty(int(Cm[:, d].sum()), dtype=torch.bfloat16, device=device)
+           for d in range(8)]
+    torch.cuda.synchronize()
+    cl = counts.tolist()
+    measure(workloads.A2AV_BF16_R8_MOE.name, lambda: P.purlin_all_to_all_v(ctx, src, dst, cl, 1),
+            2 * int(counts.sum()) * 2, int(counts.sum()) * 2, 10)
+    del src, dst
+    torch.cuda.empty_cache()
+
+    # config 5: AllReduce bf16, batch x 4096 per rank, the whole sweep
+    for b in workloads.AR_BF16_SWEEP_BATCHES:
+        n = b * workloads.HIDDEN
+        src = [normals(n) for _ in range(8)]
+        dst = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(8)]
+        torch.cuda.synchronize()
+        measure(workloads.ar_sweep_workload(b).name,
+                lambda: P.purlin_all_reduce(ctx, src, dst, n, 1), 2 * 8 * n * 2, 8 * n * 2,
+                100 if n <= (1 << 20) else 20, graph=2 * n <= (32 << 20))
+        del src, dst
+        torch.cuda.empty_cache()
+    return rows
+
+
+def small_message_rows():
+    """Messages of 2 KiB per rank and less against the two launch floors,
+    timed from C through the public ABI (no Python in the timed path): per
+    collective one call between events (median of 200) and the device time
+    per call in a CUDA graph of 1000 calls; the floors are an empty kernel
+    and a kernel whose one thread loads and stores 16 bytes, timed the same
+    two ways."""
+    exe = os.path.join(ROOT, "collective_datapath_atom_gb300", "purlin_bench")
+    rows = []
+    for coll in ("AR", "RS", "AG", "A2A", "AGV", "RSV", "A2AV"):
+        lo = "256" if coll in ("AR", "AG") else "2048"
+        res = subprocess.run([exe, coll, lo, "2048", "1000", "200", "10", "42"],
+                             capture_output=True, text=True, check=True)
+        for line in res.stdout.splitlines():
+            r = json.loads(line)
+            rows.append({k: r[k] for k in (
+                "coll", "bytes_per_rank", "single_us", "graph_us", "floor_single_us",
+                "floor_graph_us", "x_floor_single", "x_floor_graph", "touch_single_us",
+                "touch_graph_us", "x_touch_single", "x_touch_graph")})
+    return rows
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+
+    return platform.machine()
+
+
+def cpu_baseline_legs(w, seconds: float):
+    """The oracle as it stands on the host: its single-threaded build, then
+    its OpenMP build over every core this process may run on."""
+    import oracle
+
+    oracle.build()
+    gbs1, desc1, dt1, reps1 = oracle_sample_time(w, budget_s=seconds)
+    cores = len(os.sched_getaffinity(0))
+    try:
+        oracle.build(openmp=True)
+        with oracle.openmp(cores) as omp:
+            gbsn, descn, dtn, repsn = oracle_sample_time(w, budget_s=seconds)
+            used = omp.threads
+    except (OSError, subprocess.CalledProcessError) as e:
+        return {"value": gbs1, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"{desc1}; {reps1} reps, {dt1 * 1e3:.1f} ms each",
+                "openmp": f"unavailable: {e}", "cpu_model": cpu_model()}
+    return {"value": gbsn, "unit": "GB/s", "cores": used, "kind": "oracle",
+            "build": f"OpenMP, {used} threads (sched_getaffinity: {cores} cores)",
+            "sample": f"{descn}; {repsn} reps, {dtn * 1e3:.1f} ms each",
+            "cpu_model": cpu_model(),
+            "single_core": {"value": gbs1, "unit": "GB/s", "cores": 1,
+                            "sample": f"{desc1}; {reps1} reps, {dt1 * 1e3:.1f} ms each"}}
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -499,14 +697,24 @@ def run_gpu(args, rank, world, local_rank):
                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
                "ms_per_step": e2e_ms}
 
+    # the headline workload back to back (no flush between steps): the
+    # output left dirty in the L2 by one step is written back during the next
+    b2b = None
+    if not args.no_configs:
+        k = max(10, min(args.steps, 200))
+        b2b_us = _back_to_back_us(torch, stream, lambda: run(src, dst), k)
+        b2b = {"us": b2b_us, "steps": k, "gbs": algo_bytes / (b2b_us * 1e-6) / 1e9,
+               "frac": algo_bytes / (b2b_us * 1e-6) / 1e9 / peak}
+        P.purlin_check(ctx)
+
+    configs = small = None
+    if rank == 0 and not args.no_configs:
+        configs = config_rows(P, ctx, torch, device, stream, flush_buf, peak)
+        small = small_message_rows()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        import oracle
-
-        oracle.build()
-        gbs, desc, dt, reps = oracle_sample_time(w, budget_s=args.cpu_seconds)
-        cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"{desc}; {reps} reps, {dt * 1e3:.1f} ms each"}
+        cpu = cpu_baseline_legs(w, args.cpu_seconds)
 
     line = {
         "metric": "effective HBM GB/s (algorithmic read+write bytes / device time)",
@@ -524,6 +732,9 @@ def run_gpu(args, rank, world, local_rank):
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
                      "kernel": KERNEL_OF_VARIANT.get(info["variant"], "none")},
+        "back_to_back": b2b,
+        "configs": configs,
+        "small_messages": small,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps,
@@ -788,6 +999,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="only the headline workload (no per-config rows, no small messages)")
     ap.add_argument("--flush", action="store_true",
                     help="flush L2 before every timed step even when the inputs exceed it")
     ap.add_argument("--device-counts", action="store_true",

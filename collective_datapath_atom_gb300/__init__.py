@@ -140,6 +140,7 @@ _SIGNATURES = {
                                                  ctypes.c_int, ctypes.c_int, purlin_layout,
                                                  ctypes.c_void_p]),
     "purlin_empty_launch": (ctypes.c_int, [ctypes.c_void_p]),
+    "purlin_touch_launch": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "purlin_check": (ctypes.c_int, [_CTX]),
     "purlin_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "purlin_set_option": (ctypes.c_int, [_CTX, ctypes.c_int, ctypes.c_int64]),
@@ -352,6 +353,11 @@ def purlin_all_reduce_noalloc(R, src, dst, n, dtype, op=None, layout=None, strea
 
 def purlin_empty_launch(stream=None):
     _ok(lib.purlin_empty_launch(ctypes.c_void_p(_stream_handle(stream))), "purlin_empty_launch")
+
+
+def purlin_touch_launch(src_ptr: int, dst_ptr: int, stream=None):
+    _ok(lib.purlin_touch_launch(ctypes.c_void_p(src_ptr), ctypes.c_void_p(dst_ptr),
+                                ctypes.c_void_p(_stream_handle(stream))), "purlin_touch_launch")
 
 
 def purlin_check(ctx) -> int:

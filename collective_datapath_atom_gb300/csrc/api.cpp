@@ -545,6 +545,15 @@ purlin_status purlin_empty_launch(purlin_stream stream) {
                                                                           : PURLIN_ERR_CUDA;
 }
 
+purlin_status purlin_touch_launch(const void *src, void *dst, purlin_stream stream) {
+    if (src == nullptr || dst == nullptr) return PURLIN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15u)
+        return PURLIN_ERR_ALIGNMENT;
+    return launch_touch(src, dst, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PURLIN_OK
+               : PURLIN_ERR_CUDA;
+}
+
 purlin_status purlin_check(purlin_ctx *ctx) {
     if (ctx == nullptr) return PURLIN_ERR_INVALID_ARG;
     if (cudaStreamSynchronize(ctx->stream) != cudaSuccess) return PURLIN_ERR_CUDA;

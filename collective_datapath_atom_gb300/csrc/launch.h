@@ -108,6 +108,7 @@ int launch_class(int R, size_t nseg, bool device_table);
 
 cudaError_t launch_latency(const LaunchArgs &a);
 cudaError_t launch_empty(cudaStream_t stream);
+cudaError_t launch_touch(const void *src, void *dst, cudaStream_t stream);
 cudaError_t launch_throughput(const LaunchArgs &a);
 
 // Largest dynamic shared memory the throughput kernels may use; set once.

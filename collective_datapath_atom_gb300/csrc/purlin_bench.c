@@ -16,6 +16,8 @@
  *   graph_us    device time per call from a CUDA graph of `graphLaunches`
  *               calls, replayed `runs` times (0 = skipped);
  *   floor_*     the same two measurements of an empty <<<1,32>>> kernel;
+ *   touch_*     and of a kernel whose one thread loads 16 bytes and stores
+ *               them (the least a kernel that touches memory does);
  *   algbw_gbs   totalBytes / graph time (or single time without graphs);
  *   eff_gbs     bytes every rank buffer reads plus writes / the same time.
  * The V collectives split the size with the Zipf(s = 0.125) partition of the
@@ -117,7 +119,15 @@ static void call_once(const Call *c) {
     }
 }
 
-static void empty_once(void) { PK(purlin_empty_launch(stream)); }
+static void *touch_buf;   /* 32 bytes: the touch kernel copies the first 16 to the last 16 */
+
+/* empty: 1 = the empty kernel, 2 = the one-load-one-store kernel */
+static void empty_once(int kind) {
+    if (kind == 2)
+        PK(purlin_touch_launch(touch_buf, (char *)touch_buf + 16, stream));
+    else
+        PK(purlin_empty_launch(stream));
+}
 
 static float single_us(void (*fn)(const Call *), const Call *c, int runs, int empty) {
     cudaEvent_t e0, e1;
@@ -126,7 +136,7 @@ static float single_us(void (*fn)(const Call *), const Call *c, int runs, int em
     float *t = (float *)malloc(sizeof(float) * (size_t)runs);
     for (int i = 0; i < runs; ++i) {
         CK(cudaEventRecord(e0, stream));
-        if (empty) empty_once(); else fn(c);
+        if (empty) empty_once(empty); else fn(c);
         CK(cudaEventRecord(e1, stream));
         CK(cudaEventSynchronize(e1));
         CK(cudaEventElapsedTime(&t[i], e0, e1));
@@ -144,7 +154,7 @@ static float graph_us(const Call *c, int launches, int runs, int empty) {
     cudaGraphExec_t ge;
     CK(cudaStreamBeginCapture(stream, cudaStreamCaptureModeThreadLocal));
     for (int i = 0; i < launches; ++i) {
-        if (empty) empty_once(); else call_once(c);
+        if (empty) empty_once(empty); else call_once(c);
     }
     CK(cudaStreamEndCapture(stream, &g));
     CK(cudaGraphInstantiate(&ge, g, 0));
@@ -253,8 +263,12 @@ int main(int argc, char **argv) {
 
     CK(cudaStreamCreateWithFlags(&stream, cudaStreamNonBlocking));
     PK(purlin_init(R, stream, &ctx));
+    CK(cudaMalloc(&touch_buf, 32));
+    CK(cudaMemset(touch_buf, 0, 32));
     const float floor_single = single_us(NULL, NULL, runs * 4, 1);
     const float floor_graph = graph_launches > 0 ? graph_us(NULL, 1000, runs, 1) : 0.0f;
+    const float touch_single = single_us(NULL, NULL, runs * 4, 2);
+    const float touch_graph = graph_launches > 0 ? graph_us(NULL, 1000, runs, 2) : 0.0f;
 
     for (size_t bytes = min_b; bytes <= max_b; bytes *= 2) {
         shape(&c, bytes);
@@ -287,11 +301,14 @@ int main(int argc, char **argv) {
                "\"variant\": %d, \"grid\": %d, \"single_us\": %.3f, \"graph_us\": %.3f, "
                "\"floor_single_us\": %.3f, \"floor_graph_us\": %.3f, "
                "\"x_floor_single\": %.3f, \"x_floor_graph\": %.3f, "
+               "\"touch_single_us\": %.3f, \"touch_graph_us\": %.3f, "
+               "\"x_touch_single\": %.3f, \"x_touch_graph\": %.3f, "
                "\"algbw_gbs\": %.2f, \"eff_gbs\": %.2f}\n",
                argv[1], bytes, (unsigned long long)total, info.variant, info.grid, s_us, g_us,
                floor_single, floor_graph, s_us / floor_single,
-               floor_graph > 0 ? g_us / floor_graph : 0.0, total / (t * 1e-6) / 1e9,
-               traffic / (t * 1e-6) / 1e9);
+               floor_graph > 0 ? g_us / floor_graph : 0.0, touch_single, touch_graph,
+               s_us / touch_single, touch_graph > 0 ? g_us / touch_graph : 0.0,
+               total / (t * 1e-6) / 1e9, traffic / (t * 1e-6) / 1e9);
         fflush(stdout);
         for (int r = 0; r < R; ++r) {
             CK(cudaFree(c.src[r]));
@@ -300,6 +317,7 @@ int main(int argc, char **argv) {
         (void)max_elems;
     }
     PK(purlin_finalize(ctx));
+    CK(cudaFree(touch_buf));
     CK(cudaStreamDestroy(stream));
     return 0;
 }

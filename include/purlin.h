@@ -252,6 +252,13 @@ purlin_status purlin_all_reduce_noalloc(int R, const void *const src[], void *co
  * same way as a collective.  Returns CUDA if the launch fails. */
 purlin_status purlin_empty_launch(purlin_stream stream);
 
+/* Enqueue one kernel (<<<1, 32>>>) in which one thread copies the 16 bytes
+ * at device address `src` to `dst`: the least a kernel that touches memory
+ * does (one load round trip and one store), the second floor small-message
+ * latency is compared against.  Both pointers 16-byte aligned (ALIGNMENT
+ * otherwise), non-NULL (INVALID_ARG); CUDA if the launch fails. */
+purlin_status purlin_touch_launch(const void *src, void *dst, purlin_stream stream);
+
 /* ----------------------------------------------------------------- status */
 
 /* Wait for the context's stream, then read and clear the device error word.
