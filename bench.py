@@ -805,6 +805,11 @@ def sweep(args):
         rows.append(row)
         print(json.dumps(row), flush=True)
 
+    sections = set(args.rows.split(",")) if args.rows else None
+
+    def want(name):
+        return sections is None or name in sections
+
     def bufs(n_in, n_out, dtype=1):
         tdt = torch.float32 if dtype == 0 else torch.bfloat16
         src = [torch.randn(n_in, generator=gen, device=device, dtype=torch.float32).to(tdt)
@@ -820,7 +825,7 @@ def sweep(args):
     # ---- small messages (<= 2 KiB per rank) against the empty-kernel floor,
     # timed from C through the public ABI (no Python in the timed path)
     exe = os.path.join(ROOT, "collective_datapath_atom_gb300", "purlin_bench")
-    for coll in ("AR", "RS", "AG", "A2A", "AGV", "RSV", "A2AV"):
+    for coll in ("AR", "RS", "AG", "A2A", "AGV", "RSV", "A2AV") if want("small") else ():
         res = subprocess.run([exe, coll, "256", "2048", "200", "200", "10", "42"],
                              capture_output=True, text=True, check=True)
         for line in res.stdout.splitlines():
@@ -831,7 +836,7 @@ def sweep(args):
     # ---- the pages' V-collective sweep ("Purlin: Separating Orchestration from the Datapath of Collectives"
     # §C.4): Zipf(0.125)
     # split of a total T per rank, 1 KiB .. 1 GiB, through the C ABI
-    for coll in ("AGV", "RSV", "A2AV"):
+    for coll in ("AGV", "RSV", "A2AV") if want("vsweep") else ():
         res = subprocess.run([exe, coll, "1024", str(1 << 30), "10", "10", "2", "42"],
                              capture_output=True, text=True, check=True)
         for line in res.stdout.splitlines():
@@ -841,7 +846,7 @@ def sweep(args):
             emit(r)
 
     # ---- AllReduce bf16 sweep, batch x 4096, both variants, L2 flushed
-    for b in workloads.AR_BF16_SWEEP_BATCHES:
+    for b in workloads.AR_BF16_SWEEP_BATCHES if want("ar_sweep") else ():
         n = b * workloads.HIDDEN
         src, dst = bufs(n, n)
         algo = 2 * 8 * n * 2
@@ -871,7 +876,8 @@ def sweep(args):
 
     # ---- the large workloads, L2 flushed
     for name in (workloads.AG_BF16_R8_8MI.name, workloads.RS_BF16_R8_128MI.name,
-                 workloads.A2AV_BF16_R8_MOE.name, workloads.AR_F32_R8_4096.name):
+                 workloads.A2AV_BF16_R8_MOE.name,
+                 workloads.AR_F32_R8_4096.name) if want("workload") else ():
         w, ins, src, dst, call, algo, _, _ = setup_workload(name, device)
         torch.cuda.synchronize()
         run = make_runner(P, ctx, w, call)
@@ -896,7 +902,7 @@ def sweep(args):
     dev_cases = [(workloads.AG_BF16_R8_8MI.name, 0), (workloads.RS_BF16_R8_128MI.name, 0),
                  (workloads.ar_sweep_workload(32768).name, 1),
                  (workloads.ar_sweep_workload(32768).name, 2)]
-    for name, mode in dev_cases:
+    for name, mode in dev_cases if want("device_api") else ():
         w, ins, src, dst, call, algo, _, _ = setup_workload(name, device)
         torch.cuda.synchronize()
         setopt(2, mode)
@@ -926,9 +932,12 @@ def sweep(args):
     # the count matrix already on the GPU, against the host-count call and
     # against what a host-count caller must do with GPU counts (copy them
     # to the host first); also a decode-size dispatch (64 tokens per rank)
-    w, ins, src, dst, call, algo, _, _ = setup_workload(workloads.A2AV_BF16_R8_MOE.name, device)
+    if want("device_counts"):
+        w, ins, src, dst, call, algo, _, _ = setup_workload(workloads.A2AV_BF16_R8_MOE.name,
+                                                            device)
     H = workloads.MOE_HIDDEN
-    for label, tokens in (("moe_16384tok", workloads.MOE_TOKENS), ("moe_64tok", 64)):
+    for label, tokens in (("moe_16384tok", workloads.MOE_TOKENS),
+                          ("moe_64tok", 64)) if want("device_counts") else ():
         if tokens == workloads.MOE_TOKENS:
             counts = call[1]
             s_in = src
@@ -962,14 +971,53 @@ def sweep(args):
                   "p90": p90, "wall_us_per_call": wall, "gbs": algo_c / (med * 1e-6) / 1e9,
                   "frac": algo_c / (med * 1e-6) / 1e9 / peak})
         del d_out
-    del ins, src, dst
+    if want("device_counts"):
+        del ins, src, dst
     torch.cuda.empty_cache()
 
-    nbytes = 1 << 30
+    # ---- the packet channel (latency path, 16-byte payload+flag packets)
+    # against the chunk-flag path, both inside a user kernel that computes
+    # relu of its inputs and AllReduces the result: the packet-streaming
+    # kernel (no grid barrier; each unit moves as soon as it is computed)
+    # against relu, grid barrier, then the device-side composed AllReduce
+    # (per-chunk flags) or the fused one (no cross-CTA flags).  Single
+    # launches with the L2 flushed (median of 100), and per call in a CUDA
+    # graph of 100 (L2 warm).
+    if want("packet_channel"):
+        ch = P.purlin_packet_channel_create(ctx, 1 << 20, 2 * sms)
+        for per_rank in (256, 2048, 16 << 10, 64 << 10, 256 << 10, 1 << 20):
+            n = per_rank // 2
+            src, dst = bufs(n, n)
+            ptr_s, ptr_d = [t.data_ptr() for t in src], [t.data_ptr() for t in dst]
+            cases = [("packets", lambda: X.packet_stream(ch, ptr_s, ptr_d, n, 1, True,
+                                                         stream=stream))]
+            descs = []
+            for mode, label in ((2, "chunk_flags"), (1, "fused")):
+                setopt(2, mode)
+                d = P.purlin_device_prepare(ctx, P.PURLIN_COLL_ALL_REDUCE, src, dst, n=n, dtype=1,
+                                            blocks=sms)
+                descs.append(d)
+                cases.append((label, (lambda d=d: X.relu_collective(d, n, stream=stream))))
+            setopt(0)
+            for label, fn in cases:
+                fn()
+                torch.cuda.synchronize()
+                med, p10, p90 = _events_us(torch, stream, fn, 100, flush)
+                g_us = _graph_us(torch, stream, fn, 100)
+                emit({"row": "packet_channel", "bytes_per_rank": per_rank, "path": label,
+                      "us_single": med, "p10": p10, "p90": p90, "us_graph": g_us})
+            assert P.purlin_packet_channel_check(ch, stream) == P.PURLIN_OK
+            for d in descs:
+                assert P.purlin_device_check(d, stream) == P.PURLIN_OK
+                P.purlin_device_release(ctx, d)
+            del src, dst
+        P.purlin_packet_channel_release(ctx, ch)
+
+    nbytes = 1 << 30 if want("atom_copy") else 16
     a = torch.empty(nbytes, dtype=torch.uint8, device=device)
     b = torch.empty(nbytes, dtype=torch.uint8, device=device)
     status = torch.zeros(1, dtype=torch.int32, device=device)
-    for ctas in (1, 2, 4, 8, 16, 38, 76, sms, 2 * sms, 3 * sms):
+    for ctas in (1, 2, 4, 8, 16, 38, 76, sms, 2 * sms, 3 * sms) if want("atom_copy") else ():
         per = (nbytes + ctas - 1) // ctas
         per = (per + 15) // 16 * 16
         fn = lambda: X.atom_copy(b, a, nbytes, per, status, stream=stream)   # noqa: E731
@@ -1010,6 +1058,9 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="measure every workload, both variants and the launch floor")
     ap.add_argument("--report", default="", help="with --sweep: also write the rows here")
+    ap.add_argument("--rows", default="",
+                    help="with --sweep: comma-separated sections to run (small, vsweep, ar_sweep, "
+                         "workload, device_api, device_counts, packet_channel, atom_copy)")
     args = ap.parse_args()
     if args.sweep:
         sweep(args)

@@ -99,6 +99,14 @@ class purlin_device_coll(ctypes.Structure):
                 ("owner", ctypes.c_void_p)]
 
 
+class purlin_packet_channel(ctypes.Structure):
+    """A payload+flag packet channel between CTAs of one launch (include/purlin.h)."""
+    _fields_ = [("staging", ctypes.c_void_p), ("state", ctypes.c_void_p),
+                ("capacity", ctypes.c_uint64), ("timeout_ns", ctypes.c_int64),
+                ("drop_unit", ctypes.c_int64), ("ctas", ctypes.c_int32),
+                ("pad", ctypes.c_int32), ("owner", ctypes.c_void_p)]
+
+
 class PurlinError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = int(status)
@@ -157,6 +165,11 @@ _SIGNATURES = {
     "purlin_device_check": (ctypes.c_int, [ctypes.POINTER(purlin_device_coll), ctypes.c_void_p]),
     "purlin_device_release": (ctypes.c_int, [_CTX, ctypes.POINTER(purlin_device_coll)]),
     "purlin_device_coll_size": (ctypes.c_size_t, []),
+    "purlin_packet_channel_create": (ctypes.c_int, [_CTX, ctypes.c_size_t, ctypes.c_int,
+                                                    ctypes.POINTER(purlin_packet_channel)]),
+    "purlin_packet_channel_check": (ctypes.c_int, [ctypes.POINTER(purlin_packet_channel),
+                                                   ctypes.c_void_p]),
+    "purlin_packet_channel_release": (ctypes.c_int, [_CTX, ctypes.POINTER(purlin_packet_channel)]),
 }
 
 
@@ -443,3 +456,22 @@ def purlin_device_check(desc: purlin_device_coll, stream=None) -> int:
 
 def purlin_device_release(ctx, desc: purlin_device_coll):
     _ok(lib.purlin_device_release(ctx.handle, ctypes.byref(desc)), "purlin_device_release")
+
+
+def purlin_packet_channel_create(ctx, capacity_bytes: int, ctas: int) -> purlin_packet_channel:
+    ch = purlin_packet_channel()
+    _ok(lib.purlin_packet_channel_create(ctx.handle, int(capacity_bytes), int(ctas),
+                                         ctypes.byref(ch)), "purlin_packet_channel_create")
+    return ch
+
+
+def purlin_packet_channel_check(ch: purlin_packet_channel, stream=None) -> int:
+    """Wait for the stream, then read and clear the channel's error word
+    (returns the status; does not raise)."""
+    return int(lib.purlin_packet_channel_check(ctypes.byref(ch),
+                                               ctypes.c_void_p(_stream_handle(stream))))
+
+
+def purlin_packet_channel_release(ctx, ch: purlin_packet_channel):
+    _ok(lib.purlin_packet_channel_release(ctx.handle, ctypes.byref(ch)),
+        "purlin_packet_channel_release")

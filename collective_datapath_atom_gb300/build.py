@@ -20,7 +20,7 @@ LIB = os.path.join(HERE, "libpurlin.so")
 BENCH = os.path.join(HERE, "purlin_bench")
 EXAMPLES_DIR = os.path.join(HERE, "examples")
 EXAMPLES_LIB = os.path.join(HERE, "libpurlin_examples.so")
-SOURCES = ["plan.cpp", "api.cpp", "device_api.cpp", "vcounts_api.cpp", "kernels.cu",
+SOURCES = ["plan.cpp", "api.cpp", "device_api.cpp", "channel_api.cpp", "vcounts_api.cpp", "kernels.cu",
            "kernels_ragged.cu", "noalloc.cu", "vcounts.cu", "packets.cu"]
 EXAMPLE_SOURCES = ["device_examples.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

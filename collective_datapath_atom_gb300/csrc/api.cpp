@@ -473,6 +473,10 @@ purlin_status purlin_finalize(purlin_ctx *ctx) {
     if (cudaStreamSynchronize(ctx->stream) != cudaSuccess) st = PURLIN_ERR_CUDA;
     for (CacheEntry &e : ctx->lru) drop_entry(e);
     for (DeviceCollMem &m : ctx->device_colls) free_device_coll(m);
+    for (ChannelMem &m : ctx->channels) {
+        if (m.staging) cudaFree(m.staging);
+        if (m.state) cudaFree(m.state);
+    }
     if (ctx->flags) cudaFree(ctx->flags);
     if (ctx->packets) cudaFree(ctx->packets);
     if (ctx->err) cudaFree(ctx->err);

@@ -68,6 +68,12 @@ struct DeviceCollMem {
 
 void free_device_coll(DeviceCollMem &m);
 
+// Device memory of one packet channel (purlin_packet_channel_create).
+struct ChannelMem {
+    unsigned char *staging = nullptr;
+    unsigned long long *state = nullptr;
+};
+
 struct CacheEntry {
     std::string key;
     Plan plan;
@@ -111,6 +117,7 @@ struct purlin_ctx {
     std::list<purlin::host::CacheEntry> lru;
     std::unordered_map<std::string, std::list<purlin::host::CacheEntry>::iterator> index;
     std::list<purlin::host::DeviceCollMem> device_colls;   // memory of purlin_device_prepare descriptors
+    std::list<purlin::host::ChannelMem> channels;          // memory of packet channels
 };
 
 namespace purlin {

@@ -128,21 +128,7 @@ __global__ void __launch_bounds__(kPktThreads) purlin_packet_ar_kernel(
             continue;
         }
         uint64_t v;
-        if (!atom::packet_load(pk, flag, &v)) {
-            if (error_set(p.err)) break;   // an earlier wait of this launch gave up
-            const uint64_t t0 = atom::globaltimer_ns();
-            uint32_t ns = 0;
-            bool ok = false;
-            while (!(ok = atom::packet_load(pk, flag, &v))) {
-                if ((int64_t)(atom::globaltimer_ns() - t0) > p.timeout_ns) {
-                    record_error(p.err, PURLIN_ERR_TIMEOUT, kSitePacketWait, u);
-                    break;
-                }
-                if (ns) __nanosleep(ns);
-                ns = ns < 256 ? ns + 32 : 256;
-            }
-            if (!ok) break;
-        }
+        if (!packet_wait(pk, flag, p.timeout_ns, p.err, u, &v)) break;
         for (int d = 0; d < p.R; ++d) store_unit<DT>(static_cast<char *>(p.dst[d]), off, valid, v);
     }
     __syncthreads();

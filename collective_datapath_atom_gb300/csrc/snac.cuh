@@ -64,6 +64,7 @@ enum ErrSite : uint64_t {
     kSiteDeviceArgs = 5,   // a device-API call with arguments that do not match its descriptor
     kSiteDeviceCounts = 6, // device-resident counts that exceed the declared capacities
     kSitePacketWait = 7,   // a latency-path packet that never arrived
+    kSiteChannelArgs = 8,  // a packet-channel unit past the channel's capacity
 };
 
 struct Ctl {
@@ -381,6 +382,31 @@ __device__ __forceinline__ void notify_chunk(const P &p, unsigned long long *fla
     if ((int64_t)c == p.drop_notify) return;   // host-side fault injection
     const FlagAt fa = flag_at(order, p.flag_slots, c);
     atom::flag_release(flags + fa.slot, epoch + fa.gen);
+}
+
+// ------------------------------------------------------------ packets --
+
+// Bounded wait for the packet at pk to carry `flag`: true with its payload,
+// or false once `timeout_ns` has passed (TIMEOUT recorded at the packet
+// site with `where`) or when an earlier wait of the launch already gave up
+// (the error word is set), so a lost packet costs one timeout, not one per
+// unit.  The poll backs off in steps of 32 ns up to 256 ns.
+__device__ __forceinline__ bool packet_wait(const unsigned char *pk, uint32_t flag,
+                                            int64_t timeout_ns, unsigned long long *err,
+                                            uint64_t where, uint64_t *payload) {
+    if (atom::packet_load(pk, flag, payload)) return true;
+    if (error_set(err)) return false;
+    const uint64_t t0 = atom::globaltimer_ns();
+    uint32_t ns = 0;
+    while (!atom::packet_load(pk, flag, payload)) {
+        if ((int64_t)(atom::globaltimer_ns() - t0) > timeout_ns) {
+            record_error(err, PURLIN_ERR_TIMEOUT, kSitePacketWait, where);
+            return false;
+        }
+        if (ns) __nanosleep(ns);
+        ns = ns < 256 ? ns + 32 : 256;
+    }
+    return true;
 }
 
 // ------------------------------------------------------ device epoch --

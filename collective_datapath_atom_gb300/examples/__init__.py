@@ -6,7 +6,8 @@ from __future__ import annotations
 import ctypes
 import os
 
-from .. import (_addr, _ok, _ptr_array, _stream_handle, _VPP, purlin_device_coll)
+from .. import (_addr, _ok, _ptr_array, _stream_handle, _VPP, purlin_device_coll,
+                purlin_packet_channel)
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                         "libpurlin_examples.so")
@@ -25,6 +26,10 @@ _SIGNATURES = {
                                                   ctypes.c_size_t, ctypes.c_size_t, ctypes.c_int,
                                                   ctypes.c_void_p, ctypes.c_void_p]),
     "purlin_example_atom_smem_bytes": (ctypes.c_size_t, []),
+    "purlin_example_packet_stream": (ctypes.c_int, [
+        ctypes.POINTER(purlin_packet_channel), _VPP, _VPP, ctypes.c_int, ctypes.c_size_t,
+        ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "purlin_example_packet_stream_threads": (ctypes.c_int, []),
 }
 
 
@@ -80,3 +85,19 @@ def atom_reduce(dst, srcs, elems: int, elems_per_block: int, dtype: int, status,
 
 def atom_smem_bytes() -> int:
     return int(lib.purlin_example_atom_smem_bytes())
+
+
+def packet_stream(ch, src, dst, n: int, dtype: int, relu: bool = True, stream=None):
+    """Producer CTAs compute the rank-order sum of relu(src) per 8-byte unit
+    and stream it through the packet channel; consumer CTAs write it to every
+    dst (device_examples.h)."""
+    ps, _k1 = _ptr_array(src)
+    pd, _k2 = _ptr_array(dst)
+    _ok(lib.purlin_example_packet_stream(ctypes.byref(ch), ps, pd, len(src), int(n), int(dtype),
+                                         1 if relu else 0,
+                                         ctypes.c_void_p(_stream_handle(stream))),
+        "purlin_example_packet_stream")
+
+
+def packet_stream_threads() -> int:
+    return int(lib.purlin_example_packet_stream_threads())

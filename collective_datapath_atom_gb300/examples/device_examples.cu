@@ -10,6 +10,7 @@
 //     unrelated work.
 // The tests drive these entry points and compare with the CPU oracle.
 #include <cooperative_groups.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "../../include/purlin_device.cuh"
@@ -82,6 +83,115 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     const size_t others = gridDim.x - (unsigned)c.blocks;
     const size_t tid = (size_t)(blockIdx.x - (unsigned)c.blocks) * blockDim.x + threadIdx.x;
     for (size_t i = tid; i < words; i += others * blockDim.x) fill[i] = (uint32_t)(i * 2654435761ull);
+}
+
+// ---------------------------------------------------- packet streaming --
+//
+// A compute kernel that streams its results to consumer CTAs through a
+// packet channel, with no grid barrier between computing and moving: CTAs
+// [0, G) compute y = relu(x) (or x) of every rank input for their 8-byte
+// units, add the R results in rank order in binary32 from rank 0's value,
+// round once, and send each unit's sum as a packet; CTAs [G, 2G) receive
+// every unit as soon as its packet lands and write it to all R outputs.  The
+// result is the AllReduce of the computed inputs, and the inputs are never
+// rewritten.
+
+struct StreamArgs {
+    const void *src[PURLIN_MAX_RANKS];
+    void *dst[PURLIN_MAX_RANKS];
+    purlin_packet_channel ch;
+    uint64_t nbytes;   // bytes per rank buffer
+    int32_t R;
+    int32_t G;         // producer CTAs; as many consume
+    int32_t relu;
+};
+
+constexpr int kStreamThreads = 256;
+
+// `valid` bytes (2, 4, 6 or 8) of a buffer at byte `off`, zero above.
+template <int ES>
+__device__ __forceinline__ uint64_t load8(const void *base, uint64_t off, uint32_t valid) {
+    const char *p = static_cast<const char *>(base) + off;
+    if (valid == 8) return *reinterpret_cast<const uint64_t *>(p);
+    uint64_t v = 0;
+    for (uint32_t j = 0; j < valid; j += ES)
+        v |= (ES == 4 ? (uint64_t)*reinterpret_cast<const uint32_t *>(p + j)
+                      : (uint64_t)*reinterpret_cast<const uint16_t *>(p + j)) << (8 * j);
+    return v;
+}
+
+template <int ES>
+__device__ __forceinline__ void store8(void *base, uint64_t off, uint32_t valid, uint64_t v) {
+    char *p = static_cast<char *>(base) + off;
+    if (valid == 8) {
+        *reinterpret_cast<uint64_t *>(p) = v;
+        return;
+    }
+    for (uint32_t j = 0; j < valid; j += ES) {
+        if (ES == 4) *reinterpret_cast<uint32_t *>(p + j) = (uint32_t)(v >> (8 * j));
+        else *reinterpret_cast<uint16_t *>(p + j) = (uint16_t)(v >> (8 * j));
+    }
+}
+
+// The producer's work for one unit: relu (optional) of each rank's elements,
+// summed in rank order in binary32 and rounded once.
+template <int DT>
+__device__ __forceinline__ uint64_t compute_unit(const StreamArgs &a, uint64_t off,
+                                                 uint32_t valid) {
+    constexpr int ES = DT == PURLIN_F32 ? 4 : 2;
+    constexpr int N = 8 / ES;   // elements per unit
+    float acc[N];
+    for (int s = 0; s < a.R; ++s) {
+        const uint64_t w = load8<ES>(a.src[s], off, valid);
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+            uint32_t bits;
+            if (DT == PURLIN_F32) {
+                bits = (uint32_t)(w >> (32 * j));
+                if (a.relu) bits = relu_f32(bits);
+            } else {
+                uint16_t h = (uint16_t)(w >> (16 * j));
+                if (a.relu) h = relu_bf16(h);
+                bits = (uint32_t)h << 16;
+            }
+            const float x = __uint_as_float(bits);
+            acc[j] = s == 0 ? x : __fadd_rn(acc[j], x);
+        }
+    }
+    uint64_t out = 0;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+        if (DT == PURLIN_F32) {
+            out |= (uint64_t)__float_as_uint(acc[j]) << (32 * j);
+        } else {
+            const __nv_bfloat16 h = __float2bfloat16_rn(acc[j]);
+            out |= (uint64_t)__bfloat16_as_ushort(h) << (16 * j);
+        }
+    }
+    return out;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kStreamThreads)
+    packet_stream_kernel(const __grid_constant__ StreamArgs a) {
+    constexpr int ES = DT == PURLIN_F32 ? 4 : 2;
+    const purlin::device::Packets pk = purlin::device::channel_open(a.ch);
+    const bool producer = (int)blockIdx.x < a.G;
+    const uint64_t b = producer ? blockIdx.x : blockIdx.x - (unsigned)a.G;
+    const uint64_t units = (a.nbytes + 7) / 8;
+    const uint64_t stride = (uint64_t)a.G * blockDim.x;
+    for (uint64_t u = b * blockDim.x + threadIdx.x; u < units; u += stride) {
+        const uint64_t off = 8 * u;
+        const uint32_t valid = (uint32_t)(a.nbytes - off < 8 ? a.nbytes - off : 8);
+        if (producer) {
+            purlin::device::send(a.ch, pk, u, compute_unit<DT>(a, off, valid));
+            continue;
+        }
+        uint64_t v;
+        if (!purlin::device::recv(a.ch, pk, u, &v)) break;
+        for (int d = 0; d < a.R; ++d) store8<ES>(a.dst[d], off, valid, v);
+    }
+    purlin::device::channel_close(a.ch);
 }
 
 // The README's sample: each CTA copies its slice of `total` bytes.
@@ -189,6 +299,43 @@ purlin_status purlin_example_subset(const purlin_device_coll *c, int extra_block
                             static_cast<cudaStream_t>(stream), c->composed != 0, *c,
                             static_cast<uint32_t *>(fill), words));
 }
+
+purlin_status purlin_example_packet_stream(const purlin_packet_channel *ch,
+                                          const void *const src[], void *const dst[], int R,
+                                          size_t n, purlin_dtype dtype, int relu,
+                                          purlin_stream stream) {
+    if (ch == nullptr || ch->state == nullptr || src == nullptr || dst == nullptr)
+        return PURLIN_ERR_INVALID_ARG;
+    if (R < 1 || R > PURLIN_MAX_RANKS || ch->ctas < 2 || (ch->ctas & 1) != 0)
+        return PURLIN_ERR_INVALID_ARG;
+    if (dtype != PURLIN_F32 && dtype != PURLIN_BF16) return PURLIN_ERR_INVALID_ARG;
+    const uint64_t es = dtype == PURLIN_F32 ? 4 : 2;
+    const uint64_t nbytes = (uint64_t)n * es;
+    if ((nbytes + 7) / 8 > ch->capacity) return PURLIN_ERR_INVALID_ARG;
+    StreamArgs a = {};
+    for (int r = 0; r < R; ++r) {
+        if (src[r] == nullptr || dst[r] == nullptr) return PURLIN_ERR_INVALID_ARG;
+        if (((reinterpret_cast<uintptr_t>(src[r]) | reinterpret_cast<uintptr_t>(dst[r])) & 7u) != 0)
+            return PURLIN_ERR_ALIGNMENT;
+        a.src[r] = src[r];
+        a.dst[r] = dst[r];
+    }
+    a.ch = *ch;
+    a.nbytes = nbytes;
+    a.R = R;
+    a.G = ch->ctas / 2;
+    a.relu = relu;
+    if (n == 0) return PURLIN_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // producers and consumers wait on one another: a cooperative launch
+    if (dtype == PURLIN_F32)
+        return status_of(launch(packet_stream_kernel<PURLIN_F32>, ch->ctas, kStreamThreads, 0, st,
+                                true, a));
+    return status_of(launch(packet_stream_kernel<PURLIN_BF16>, ch->ctas, kStreamThreads, 0, st,
+                            true, a));
+}
+
+int purlin_example_packet_stream_threads(void) { return kStreamThreads; }
 
 purlin_status purlin_example_atom_copy(void *dst, const void *src, size_t bytes,
                                        size_t bytes_per_block, int *status,

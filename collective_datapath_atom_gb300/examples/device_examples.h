@@ -33,6 +33,22 @@ purlin_status purlin_example_subset(const purlin_device_coll *coll, int extra_bl
                                     unsigned int *fill, size_t words, int threads,
                                     purlin_stream stream);
 
+/* A compute kernel that streams its results through a packet channel:
+ * ch->ctas / 2 producer CTAs compute, for every 8-byte unit of the n-element
+ * rank buffers, the rank-order binary32 sum of relu(src[s]) (or of src[s]
+ * when relu is 0; relu as above) rounded once to dtype, and send it as a
+ * packet; the other ch->ctas / 2 CTAs receive each unit and write it to all
+ * R outputs.  The outputs equal the AllReduce of the computed inputs; the
+ * inputs are not modified.  ch->ctas even and at least 2, the units within
+ * the channel's capacity, buffers 8-byte aligned; a cooperative launch of
+ * ch->ctas CTAs of purlin_example_packet_stream_threads() threads.  Packet
+ * errors are read with purlin_packet_channel_check. */
+purlin_status purlin_example_packet_stream(const purlin_packet_channel *ch,
+                                          const void *const src[], void *const dst[], int R,
+                                          size_t n, purlin_dtype dtype, int relu,
+                                          purlin_stream stream);
+int purlin_example_packet_stream_threads(void);
+
 /* The README's sample: CTA b copies bytes [b*per_block, (b+1)*per_block) of
  * src to dst with the Atom (4 stages of 16 KiB, 320 threads).  dst and src
  * 2-byte aligned, bytes even; the first non-OK Atom status lands in *status

@@ -452,6 +452,63 @@ purlin_status purlin_device_release(purlin_ctx *ctx, purlin_device_coll *coll);
 /* sizeof(purlin_device_coll) as this library was built (for bindings). */
 size_t purlin_device_coll_size(void);
 
+/* A payload+flag packet channel between the CTAs of one kernel launch
+ * ("Purlin: Separating Orchestration from the Datapath of Collectives" §3.2:
+ * the latency path puts payload and notification in one 16-byte packet, so
+ * a consumer sees data and readiness in one access, with no separate flag
+ * store and no fence, at twice the bytes; §4.1: two staging buffers; §4.3:
+ * the epoch is the notification value and its parity picks the buffer).
+ * It serves a producer that is not the owner of the chunks its consumers
+ * read, e.g. CTAs of a compute kernel that stream each result to consumer
+ * CTAs as soon as it exists, instead of writing all of it, passing a grid
+ * barrier and starting a collective.
+ *
+ * The unit of transfer is 8 payload bytes: unit u of a launch travels as
+ * the packet at staging + 16 u of the launch's packet set, two 8-byte lines
+ * {4 payload bytes, 32-bit flag}, each written and read as one single-copy
+ * atomic access; a consumer takes a packet once both lines carry the
+ * launch's flag.  In a kernel, exactly `ctas` CTAs call
+ * purlin::device::channel_open (include/purlin_device.cuh) before their
+ * first send or receive and channel_close after their last (every thread of
+ * those CTAs); producers call send(u, payload) once per unit and consumers
+ * recv(u) (a bounded wait).  The launch must keep producers and consumers
+ * resident together (a cooperative launch).  One round per launch: the flag
+ * is the low 32 bits of the channel's epoch, which the last CTA to close
+ * advances by one, so the next launch uses the other packet set and a new
+ * flag (no reset between launches, and a launch replayed from a CUDA graph
+ * is correct too).  Fields other than timeout_ns and drop_unit name device
+ * memory the library owns until purlin_packet_channel_release or
+ * purlin_finalize; the caller must not write it. */
+typedef struct purlin_packet_channel {
+    unsigned char *staging;    /* device: 2 packet sets of `capacity` 16-byte packets */
+    unsigned long long *state; /* device: [0] error word, [2] epoch, [3] CTAs closed */
+    uint64_t capacity;         /* 8-byte payload units per launch */
+    int64_t timeout_ns;        /* bound on one packet wait (PURLIN_OPT_SPIN_TIMEOUT_NS) */
+    int64_t drop_unit;         /* fault injection: the unit whose packet send() skips, or -1
+                                  (PURLIN_OPT_DROP_NOTIFY at creation) */
+    int32_t ctas;              /* CTAs that open and close the channel in every launch */
+    int32_t pad;
+    void *owner;               /* library bookkeeping (host address) */
+} purlin_packet_channel;
+
+/* Allocate a channel of capacity_bytes payload bytes per launch (rounded up
+ * to 8; 2 x 2 x that many bytes of staging) for `ctas` CTAs per launch, and
+ * zero it (blocking calls; not during graph capture).  INVALID_ARG for
+ * capacity 0 or above 2^34 bytes, ctas < 1 or > 65535; OOM, CUDA. */
+purlin_status purlin_packet_channel_create(purlin_ctx *ctx, size_t capacity_bytes, int ctas,
+                                           purlin_packet_channel *out);
+
+/* Wait for `stream`, then read and clear the channel's error word.  OK,
+ * TIMEOUT (a receive gave up: that launch's outputs are unspecified),
+ * INVALID_ARG (a unit past the capacity was sent or received; it was
+ * skipped) or CUDA. */
+purlin_status purlin_packet_channel_check(const purlin_packet_channel *ch, purlin_stream stream);
+
+/* Free a channel's device memory (synchronises the device) and clear it.
+ * Releasing a cleared channel is a no-op; INVALID_ARG if it was not created
+ * on this context. */
+purlin_status purlin_packet_channel_release(purlin_ctx *ctx, purlin_packet_channel *ch);
+
 #ifdef __cplusplus
 }
 #endif

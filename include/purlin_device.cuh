@@ -49,6 +49,22 @@
  * Both return PURLIN_OK, PURLIN_ERR_ALIGNMENT / PURLIN_ERR_INVALID_ARG
  * (nothing moved), or PURLIN_ERR_TIMEOUT (a ring wait expired), the same
  * value in every thread.
+ *
+ * Packet channels.  purlin_packet_channel (include/purlin.h) carries 8-byte
+ * payload units between CTAs of one launch as 16-byte payload+flag packets
+ * (paper summary §3.2, the latency path).  In each of the channel's `ctas`
+ * CTAs, every thread calls
+ *
+ *     purlin::device::Packets pk = purlin::device::channel_open(ch);
+ *     ... send(ch, pk, u, payload) / recv(ch, pk, u, &payload) ...
+ *     purlin::device::channel_close(ch);
+ *
+ * send() stores unit u's packet (one thread, one 16-byte store, no fence);
+ * recv() waits, bounded by ch.timeout_ns, until unit u's packet of this
+ * launch has arrived and returns its payload, or returns false (TIMEOUT in
+ * the channel's error word: purlin_packet_channel_check).  Each unit is sent
+ * once and may be received by any number of threads.  Producers and
+ * consumers must be resident together (a cooperative launch).
  */
 #pragma once
 
@@ -163,6 +179,60 @@ __device__ inline purlin_status collective(const purlin_device_coll &c, const Sn
                         : collective_t<PURLIN_F32, PURLIN_MAX_RANKS>(c, a);
     return c.R <= 8 ? collective_t<PURLIN_BF16, 8>(c, a)
                     : collective_t<PURLIN_BF16, PURLIN_MAX_RANKS>(c, a);
+}
+
+// ----------------------------------------------------------- packets --
+
+// One launch's view of a packet channel: its packet set and flag.
+struct Packets {
+    unsigned char *set;   // the launch's packet set (16 bytes per unit)
+    uint32_t flag;        // the launch's notification value
+};
+
+// Every thread of each of the channel's ch.ctas CTAs, before its first send
+// or receive.  The epoch only moves once all of them have closed, so every
+// thread of the launch reads the same value.
+__device__ __forceinline__ Packets channel_open(const purlin_packet_channel &ch) {
+    const unsigned long long e = *reinterpret_cast<const volatile unsigned long long *>(ch.state + 2);
+    return Packets{ch.staging + (e & 1ull) * ch.capacity * 16ull, (uint32_t)e};
+}
+
+// Unit u's payload, from one thread: one 16-byte packet store.  A unit past
+// the capacity is skipped and recorded (INVALID_ARG).
+__device__ __forceinline__ void send(const purlin_packet_channel &ch, const Packets &pk, uint64_t u,
+                                     uint64_t payload) {
+    if (u >= ch.capacity) {
+        snac::record_error(ch.state, PURLIN_ERR_INVALID_ARG, snac::kSiteChannelArgs, u);
+        return;
+    }
+    if ((int64_t)u == ch.drop_unit) return;   // host-side fault injection
+    atom::packet_store(pk.set + 16ull * u, payload, pk.flag);
+}
+
+// Unit u's payload of this launch, waiting for it (bounded).  False when the
+// wait expired (TIMEOUT recorded), when an earlier wait of the launch gave
+// up, or for a unit past the capacity (INVALID_ARG recorded).
+__device__ __forceinline__ bool recv(const purlin_packet_channel &ch, const Packets &pk, uint64_t u,
+                                     uint64_t *payload) {
+    if (u >= ch.capacity) {
+        snac::record_error(ch.state, PURLIN_ERR_INVALID_ARG, snac::kSiteChannelArgs, u);
+        return false;
+    }
+    return snac::packet_wait(pk.set + 16ull * u, pk.flag, ch.timeout_ns, ch.state, u, payload);
+}
+
+// Every thread of each entering CTA, after its last send or receive.  The
+// last CTA of the launch to close advances the epoch: the next launch uses
+// the other packet set and the next flag.
+__device__ __forceinline__ void channel_close(const purlin_packet_channel &ch) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long *epoch = ch.state + 2, *done = ch.state + 3;
+        if (atomicAdd(done, 1ull) == (unsigned long long)ch.ctas - 1ull) {
+            *done = 0;
+            atomicAdd(epoch, 1ull);
+        }
+    }
 }
 
 // One CTA's ring over a single transfer.
