@@ -283,6 +283,13 @@ __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
     const uint4 out = V::pack(acc);
     if (sg.dst_rank >= 0) {
         put_span<ES>(static_cast<char *>(p.dst[sg.dst_rank]) + doff, out, sh, nb);
+    } else if (MAXR <= 8) {
+        // static indices: the destination pointers are read from the
+        // parameters directly, not one indexed load per store
+#pragma unroll
+        for (int r = 0; r < MAXR; ++r)
+            if (r < R && r != sg.skip_rank)
+                put_span<ES>(static_cast<char *>(p.dst[r]) + doff, out, sh, nb);
     } else {
         for (int r = 0; r < R; ++r)
             if (r != sg.skip_rank) put_span<ES>(static_cast<char *>(p.dst[r]) + doff, out, sh, nb);
