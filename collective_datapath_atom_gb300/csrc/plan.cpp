@@ -336,13 +336,16 @@ purlin_status compile_plan(const CallDesc &c, int variant, int ar_mode, uint32_t
         s.unit_begin = unit;
         uint64_t body = 0;
         if (variant == kVariantThroughput) {
-            // A copy's body is cut on the destination side (16-byte aligned
-            // stores); a source at another 16-byte phase is staged as its
-            // aligned hull, 16 bytes longer, and shifted into place by the
-            // consumer warps.  A reduce's body is cut on the sources' side
-            // (aligned stages, no shift), and its sums are stored at the
-            // destination's phase.
-            const Cut cut = cut_transfer(r.src_off, r.dst_off, r.bytes, reduce);
+            // A copy's body is cut on the destination side, from a 128-byte
+            // line (whole-line stores); a source at another 16-byte phase is
+            // staged as its aligned hull, 16 bytes longer, and shifted into
+            // place by the consumer warps.  A gathering segment of the
+            // composed AllReduce keeps the 16-byte cut of the reducing
+            // segment it waits on, so its chunks cover whole reducing chunks.
+            // A reduce's body is cut on the sources' side (aligned stages, no
+            // shift), and its sums are stored at the destination's phase.
+            const Cut cut = cut_transfer(r.src_off, r.dst_off, r.bytes, reduce,
+                                         r.sync == kSyncNone);
             body = cut.body;
             if (body > 0) {
                 s.tma = 1;
@@ -356,7 +359,7 @@ purlin_status compile_plan(const CallDesc &c, int variant, int ar_mode, uint32_t
         if (s.tma) {
             uint64_t nch = (body + s.chunk_bytes - 1) / s.chunk_bytes;
             chunk += nch;
-            unit += (s.head ? 1 : 0) + (s.tail ? 1 : 0);
+            unit += units_in(unit_grid(r.src_off, r.dst_off, reduce), 0, s.head) + (s.tail ? 1 : 0);
             if (reduce) p.has_reduce = true;
             else p.has_copy_chunks = true;
             if (!reduce && s.shift) p.has_shifted_copies = true;
