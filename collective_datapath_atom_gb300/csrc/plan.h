@@ -53,9 +53,8 @@ struct Seg {
     uint32_t chunk_begin;  // global index of the segment's first TMA chunk
     uint32_t chunk_bytes;  // bytes per source per TMA chunk
     uint32_t dep_chunk;    // kSyncWait: global index of the notifying chunk for chunk 0
-    uint8_t head;          // tma: bytes before the aligned body (a copy's body may start on a
-                           // 128-byte line: up to 127 bytes, several vector units)
-    uint8_t tail;          // tma: bytes after the body (under 16: one vector unit)
+    uint8_t head;          // tma: bytes before the 16-byte aligned body
+    uint8_t tail;          // tma: bytes after the body
     int8_t src_rank;       // >= 0 copy from that rank; -1 reduce over all ranks in order
     int8_t dst_rank;       // >= 0 that rank; -1 every rank (except skip_rank)
     int8_t skip_rank;      // with dst_rank -1: rank left out, or -1
@@ -77,51 +76,31 @@ PURLIN_HD inline uint64_t unit_grid(uint64_t src_off, uint64_t dst_off, bool red
     return reduce ? src_off : dst_off;
 }
 
-// Vector units covering the bytes [grid + a, grid + b) of a segment whose
-// units follow the 16-byte grid of offset `grid`: one unit per window.
-PURLIN_HD inline uint64_t units_in(uint64_t grid, uint64_t a, uint64_t b) {
-    if (b <= a) return 0;
-    const uint64_t first = (grid + a) / 16;
-    const uint64_t last = (grid + b + 15) / 16;
-    return last - first;
-}
-
-constexpr uint64_t kLineBytes = 128;   // an L2 line
-
-// The ring's cut of one transfer, on the grid its vector units follow
-// (unit_grid): the bytes before the body (head) and after it (tail) go
-// through the vector path, one unit per 16-byte window; the aligned body goes
-// through the ring in chunks.  shift is the source's 16-byte phase relative
-// to the destination.  A copy's body is aligned on the destination: a
-// shifted source is staged as its 16-byte aligned hull and shifted into
-// place as it is read.  With `line`, a copy's body starts on a 128-byte line
-// of the destination, so every 16 KiB chunk, and every warp's 512 contiguous
-// bytes of stores in it, covers whole L2 lines (a warp whose run starts
-// mid-line touches five lines instead of four: 19% more L2 write requests
-// and partial-line writes, measured at 0.78 against 0.90 of the copy peak
-// on an AllGatherV of unequal shares).  A reduce's body is aligned on the
-// sources (16 bytes): they are staged as they are, and the sum is stored at
-// the destination's phase.  Used by the host plan compiler, the device-count
-// kernel and the device-side Atom, so all cut a transfer the same way.
+// The ring's cut of one transfer, on the 16-byte grid its vector units follow
+// (unit_grid): the bytes before the grid's first boundary (head) and after
+// its last (tail) go through the vector path; the aligned body goes through
+// the ring in chunks.  shift is the source's 16-byte phase relative to the
+// destination.  A copy's body is aligned on the destination: a shifted source
+// is staged as its 16-byte aligned hull and shifted into place as it is read.
+// A reduce's body is aligned on the sources: they are staged as they are,
+// and the sum is stored at the destination's phase.  Used by the host plan
+// compiler, the device-count kernel and the device-side Atom, so all cut a
+// transfer the same way.
 struct Cut {
     uint64_t body;
     uint32_t head, tail, shift;
-    uint32_t units;   // vector units when the body is not empty: the head's windows and the tail
 };
 
-PURLIN_HD inline Cut cut_transfer(uint64_t src_off, uint64_t dst_off, uint64_t bytes, bool reduce,
-                                  bool line = false) {
+PURLIN_HD inline Cut cut_transfer(uint64_t src_off, uint64_t dst_off, uint64_t bytes, bool reduce) {
     Cut c;
     const uint64_t grid = unit_grid(src_off, dst_off, reduce);
-    const uint64_t align = line && !reduce ? kLineBytes : 16u;
-    const uint64_t lead = (align - grid % align) % align;
+    const uint64_t lead = (16u - (grid & 15u)) & 15u;
     const uint64_t head = lead < bytes ? lead : bytes;
     const uint64_t rest = bytes - head;
     c.head = (uint32_t)head;
     c.tail = (uint32_t)(rest & 15u);
     c.body = rest - c.tail;
     c.shift = (uint32_t)((src_off - dst_off) & 15u);
-    c.units = (uint32_t)units_in(grid, 0, head) + (c.tail ? 1u : 0u);
     return c;
 }
 
@@ -206,6 +185,15 @@ PURLIN_HD inline FlagAt flag_at(const ChunkOrder &o, uint64_t F, uint64_t d) {
     f.slot = i % F;
     f.gen = i / F;
     return f;
+}
+
+// Vector units covering the bytes [grid + a, grid + b) of a segment whose
+// units follow the 16-byte grid of offset `grid`: one unit per window.
+PURLIN_HD inline uint64_t units_in(uint64_t grid, uint64_t a, uint64_t b) {
+    if (b <= a) return 0;
+    const uint64_t first = (grid + a) / 16;
+    const uint64_t last = (grid + b + 15) / 16;
+    return last - first;
 }
 
 struct Plan {

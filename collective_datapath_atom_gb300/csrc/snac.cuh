@@ -187,14 +187,19 @@ __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
     constexpr int ES = DT == PURLIN_F32 ? 4 : 2;
     const bool reduce = sg.src_rank < 0;
     uint64_t lo, hi;
-    const uint64_t g = unit_grid(sg.src_off, sg.dst_off, reduce);
-    if (RING && sg.tma && k >= units_in(g, 0, sg.head)) {   // the tail: one window
-        lo = sg.bytes - sg.tail;
-        hi = sg.bytes;
-    } else {   // window k of the segment, or of a ring segment's head
+    if (RING && sg.tma) {
+        if (k == 0 && sg.head) {
+            lo = 0;
+            hi = sg.head;
+        } else {
+            lo = sg.bytes - sg.tail;
+            hi = sg.bytes;
+        }
+    } else {
+        const uint64_t g = unit_grid(sg.src_off, sg.dst_off, reduce);
         const uint64_t a = (g / 16 + k) * 16;
         lo = (a > g ? a : g) - g;
-        const uint64_t b = a + 16, e = g + (RING && sg.tma ? sg.head : sg.bytes);
+        const uint64_t b = a + 16, e = g + sg.bytes;
         hi = (b < e ? b : e) - g;
     }
     const int R = p.R;

@@ -195,14 +195,14 @@ __global__ void __launch_bounds__(kVcThreadsMax, 1)
         sg.chunk_bytes = sg.src_rank < 0 ? p.red_chunk : p.copy_chunk;
         uint64_t chunks = 0, units = units_in(unit_grid(so, dof, sg.src_rank < 0), 0, bytes);
         if (ring) {
-            const Cut cut = cut_transfer(so, dof, bytes, sg.src_rank < 0, true);
+            const Cut cut = cut_transfer(so, dof, bytes, sg.src_rank < 0);
             if (cut.body > 0) {
                 sg.tma = 1;
                 sg.head = (uint8_t)cut.head;
                 sg.tail = (uint8_t)cut.tail;
                 sg.shift = (uint8_t)cut.shift;
                 chunks = (cut.body + sg.chunk_bytes - 1) / sg.chunk_bytes;
-                units = cut.units;
+                units = (cut.head ? 1u : 0u) + (cut.tail ? 1u : 0u);
             }
         }
         segs[i] = sg;

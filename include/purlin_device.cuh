@@ -290,14 +290,14 @@ struct Atom {
         s.dst_rank = 0;
         s.skip_rank = -1;
         s.chunk_bytes = chunk;
-        const Cut cut = cut_transfer(src_off, dst_off, bytes, src_rank < 0, true);
+        const Cut cut = cut_transfer(src_off, dst_off, bytes, src_rank < 0);
         if (cut.body > 0) {
             s.tma = 1;
             s.head = (uint8_t)cut.head;
             s.tail = (uint8_t)cut.tail;
             s.shift = (uint8_t)cut.shift;
             *nchunks = (cut.body + chunk - 1) / chunk;
-            *nunits = cut.units;
+            *nunits = (cut.head ? 1u : 0u) + (cut.tail ? 1u : 0u);
         } else {
             *nchunks = 0;
             *nunits = units_in(unit_grid(src_off, dst_off, src_rank < 0), 0, bytes);

@@ -100,3 +100,36 @@ def test_examples_library_exports_its_header():
     exported = set(line.split()[-1] for line in nm.splitlines() if line.strip())
     assert set(names) <= exported
     assert set(examples._SIGNATURES) == set(names)
+
+
+def test_new_entry_points_refuse_bad_arguments_before_any_launch(P):
+    """Argument checks that return before the GPU is touched (they run here
+    without a GPU): the touch floor needs two 16-byte aligned pointers, and a
+    packet channel needs a context, a capacity and a CTA count in range."""
+    vp = ctypes.c_void_p
+    assert P.lib.purlin_touch_launch(None, vp(0x1000), None) == P.PURLIN_ERR_INVALID_ARG
+    assert P.lib.purlin_touch_launch(vp(0x1000), None, None) == P.PURLIN_ERR_INVALID_ARG
+    assert P.lib.purlin_touch_launch(vp(0x1008), vp(0x2000), None) == P.PURLIN_ERR_ALIGNMENT
+    assert P.lib.purlin_touch_launch(vp(0x1000), vp(0x2004), None) == P.PURLIN_ERR_ALIGNMENT
+    ch = P.purlin_packet_channel()
+    assert P.lib.purlin_packet_channel_create(None, 4096, 2, ctypes.byref(ch)) == \
+        P.PURLIN_ERR_INVALID_ARG
+    assert P.lib.purlin_packet_channel_check(None, None) == P.PURLIN_ERR_INVALID_ARG
+    assert P.lib.purlin_packet_channel_check(ctypes.byref(ch), None) == P.PURLIN_ERR_INVALID_ARG
+    assert P.lib.purlin_packet_channel_release(None, ctypes.byref(ch)) == P.PURLIN_ERR_INVALID_ARG
+
+
+def test_packet_channel_layout_matches_the_header():
+    """The binding's struct mirrors include/purlin.h field for field."""
+    import collective_datapath_atom_gb300 as P
+
+    names = [f for f, _ in P.purlin_packet_channel._fields_]
+    assert names == ["staging", "state", "capacity", "timeout_ns", "drop_unit", "ctas", "pad",
+                     "owner"]
+    assert ctypes.sizeof(P.purlin_packet_channel) == 56
+    with open(os.path.join(ROOT, "include", "purlin.h")) as f:
+        text = f.read()
+    body = text[text.index("typedef struct purlin_packet_channel"):]
+    body = body[:body.index("} purlin_packet_channel;")]
+    declared = re.findall(r"\b(\w+);", body)
+    assert declared == names

@@ -167,32 +167,32 @@ def test_cut_invariants(coll, R, dtype):
             for sg in segs:
                 assert sg["bytes"] > 0 and sg["bytes"] % es == 0
                 assert sg["src_off"] % es == 0 and sg["dst_off"] % es == 0
-                # a copy that waits on nothing starts its body on a 128-byte line
-                # of the destination; reduces and the composed gather on 16 bytes
-                line = 128 if sg["src_rank"] >= 0 and sg["sync"] == 0 else 16
                 g = sg["src_off"] if sg["src_rank"] < 0 else sg["dst_off"]
                 assert sg["chunk_begin"] == chunk_total and sg["unit_begin"] == unit_total
                 if sg["tma"]:
                     assert variant == 2
                     body = sg["bytes"] - sg["head_bytes"] - sg["tail_bytes"]
                     assert body > 0 and body % 16 == 0
-                    assert sg["head_bytes"] < line and sg["tail_bytes"] < 16
+                    assert sg["head_bytes"] < 16 and sg["tail_bytes"] < 16
                     # the body is aligned on the grid the segment's units follow:
                     # a reduce's sources, a copy's destination
-                    assert (g + sg["head_bytes"]) % line == 0
+                    assert (g + sg["head_bytes"]) % 16 == 0
+                    if sg["src_rank"] >= 0 and sg["sync"] == 0 and sg["bytes"] >= 144:
+                        # a copy that waits on nothing starts its body on a
+                        # 128-byte line (the bytes before it are a segment of
+                        # their own on the vector path)
+                        assert (g + sg["head_bytes"]) % 128 == 0
                     assert (sg["src_off"] - sg["dst_off"]) % 16 == sg["shift"]
                     assert sg["chunk_bytes"] % 16 == 0
                     chunk_total += -(-body // sg["chunk_bytes"])
-                    # the head's 16-byte windows, and the tail
-                    h0, h1 = g, g + sg["head_bytes"]
-                    unit_total += (-(-h1 // 16) - h0 // 16 if h1 > h0 else 0) + (sg["tail_bytes"] > 0)
+                    unit_total += (sg["head_bytes"] > 0) + (sg["tail_bytes"] > 0)
                 else:
                     # one unit per 16-byte window: a reduce's windows follow
                     # the sources' grid, a copy's the destination's
                     a, b = g, g + sg["bytes"]
                     unit_total += -(-b // 16) - a // 16
-                    if variant == 2:   # only transfers without a whole aligned window skip the ring
-                        assert sg["bytes"] < line + 16
+                    if variant == 2:   # the bytes before a line, or no whole aligned window
+                        assert sg["bytes"] < 128 + 16
             assert chunk_total == nch and unit_total == nun
             # every access stays inside its buffer
             ib, ob = sizes_of(coll, R, n, counts, es)
