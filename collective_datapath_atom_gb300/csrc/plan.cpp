@@ -376,19 +376,23 @@ purlin_status compile_plan(const CallDesc &c, int variant, int ar_mode, uint32_t
     };
     for (const RawSeg &r : raw) {
         const bool ring = variant == kVariantThroughput;
-        // In the ring, a copy that waits on nothing starts its body on a
-        // 128-byte line of the destination, so every chunk, and every warp's
-        // 512 contiguous bytes of stores in it, covers whole L2 lines: the
-        // bytes before the line become a segment of their own on the vector
-        // path.  (A warp whose run starts mid-line touches five lines instead
-        // of four: 19% more L2 write requests and partial-line writes,
-        // measured at 0.78 against 0.90 of the copy peak on an AllGatherV of
-        // unequal shares.)  A gathering segment of the composed AllReduce
-        // keeps the cut of the reducing segment it waits on, so its chunks
-        // cover whole reducing chunks; reduces are cut on their sources.
+        // In the ring, a copy to every rank that waits on nothing (AllGather,
+        // AllGatherV) starts its body on a 128-byte line of the destination,
+        // so every chunk, and every warp's 512 contiguous bytes of stores in
+        // it, covers whole L2 lines: the bytes before the line become a
+        // segment of their own on the vector path.  (A warp whose run starts
+        // mid-line touches five lines instead of four: 19% more L2 write
+        // requests and partial-line writes, measured at 0.78 against 0.90 of
+        // the copy peak on an AllGatherV of unequal shares.)  Point-to-point
+        // copies (AllToAll(V): R*R segments, mostly stored in bulk) keep one
+        // segment each: splitting them measured up to 34% slower, the
+        // segment table outgrowing the ring's staged copy.  A gathering
+        // segment of the composed AllReduce keeps the cut of the reducing
+        // segment it waits on, so its chunks cover whole reducing chunks;
+        // reduces are cut on their sources.
         const uint64_t lead = (kLineBytes - r.dst_off % kLineBytes) % kLineBytes;
-        if (ring && r.src_rank != kRankAll && r.sync == kSyncNone && lead >= 16 &&
-            r.bytes >= lead + 16) {
+        if (ring && r.src_rank != kRankAll && r.dst_rank == kRankAll && r.sync == kSyncNone &&
+            lead >= 16 && r.bytes >= lead + 16) {
             emit(r, 0, lead, false);
             emit(r, lead, r.bytes - lead, true);
         } else {

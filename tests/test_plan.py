@@ -177,10 +177,11 @@ def test_cut_invariants(coll, R, dtype):
                     # the body is aligned on the grid the segment's units follow:
                     # a reduce's sources, a copy's destination
                     assert (g + sg["head_bytes"]) % 16 == 0
-                    if sg["src_rank"] >= 0 and sg["sync"] == 0 and sg["bytes"] >= 144:
-                        # a copy that waits on nothing starts its body on a
-                        # 128-byte line (the bytes before it are a segment of
-                        # their own on the vector path)
+                    if (sg["src_rank"] >= 0 and sg["dst_rank"] < 0 and sg["sync"] == 0
+                            and sg["bytes"] >= 144):
+                        # a copy to every rank that waits on nothing starts its
+                        # body on a 128-byte line (the bytes before it are a
+                        # segment of their own on the vector path)
                         assert (g + sg["head_bytes"]) % 128 == 0
                     assert (sg["src_off"] - sg["dst_off"]) % 16 == sg["shift"]
                     assert sg["chunk_bytes"] % 16 == 0
