@@ -456,6 +456,9 @@ def config_rows(P, ctx, torch, device, stream, flush, peak):
                "algorithmic_bytes": algo, "us_single_flushed": single,
                "gbs_single_flushed": algo / (single * 1e-6) / 1e9}
         row["frac_single_flushed"] = row["gbs_single_flushed"] / peak
+        traffic = recorded_traffic(name)   # DRAM bytes per launch, ncu, this kernel source
+        if traffic is not None:
+            row.update({"traffic": traffic, "traffic_over_algorithmic": traffic / algo})
         if in_bytes > l2:
             b2b = _back_to_back_us(torch, stream, fn, max(3, reps // 2))
             row.update({"us_back_to_back": b2b, "gbs_back_to_back": algo / (b2b * 1e-6) / 1e9,
