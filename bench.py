@@ -712,12 +712,23 @@ def run_gpu(args, rank, world, local_rank):
 
     configs = small = None
     if rank == 0 and not args.no_configs:
-        configs = config_rows(P, ctx, torch, device, stream, flush_buf, peak)
-        small = small_message_rows()
+        # Extra rows: a failure here is recorded in the line, never loses it.
+        try:
+            configs = config_rows(P, ctx, torch, device, stream, flush_buf, peak)
+        except Exception as e:   # noqa: BLE001
+            configs = {"error": f"{type(e).__name__}: {e}"}
+            torch.cuda.synchronize()
+        try:
+            small = small_message_rows()
+        except Exception as e:   # noqa: BLE001
+            small = {"error": f"{type(e).__name__}: {e}"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = cpu_baseline_legs(w, args.cpu_seconds)
+        try:
+            cpu = cpu_baseline_legs(w, args.cpu_seconds)
+        except Exception as e:   # noqa: BLE001
+            cpu = {"error": f"{type(e).__name__}: {e}"}
 
     line = {
         "metric": "effective HBM GB/s (algorithmic read+write bytes / device time)",
