@@ -717,7 +717,6 @@ def run_gpu(args, rank, world, local_rank):
             configs = config_rows(P, ctx, torch, device, stream, flush_buf, peak)
         except Exception as e:   # noqa: BLE001
             configs = {"error": f"{type(e).__name__}: {e}"}
-            torch.cuda.synchronize()
         try:
             small = small_message_rows()
         except Exception as e:   # noqa: BLE001
