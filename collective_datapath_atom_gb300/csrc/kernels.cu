@@ -28,8 +28,10 @@ using ringk::fill_params;
 // ---------------------------------------------------------- latency kernel --
 
 // Four CTAs of 256 threads per SM (the host's grid cap) leave 64 registers
-// a thread; the instantiations for more than 8 ranks take two.
-template <int DT, int MAXR, int MAXSEG>
+// a thread; the instantiations for more than 8 ranks take two.  WHOLE: a
+// build for plans whose segments are all copies of whole aligned 16-byte
+// windows (Plan::all_whole), with only the short unit path (whole_unit).
+template <int DT, int MAXR, int MAXSEG, bool WHOLE = false>
 __global__ void __launch_bounds__(256, MAXR > 8 ? 2 : 4) purlin_latency_kernel(
     const __grid_constant__ KParams<MAXR, MAXSEG> p) {
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
@@ -42,7 +44,7 @@ __global__ void __launch_bounds__(256, MAXR > 8 ? 2 : 4) purlin_latency_kernel(
     // for a 2 KiB AllGather).  Short segments would make a warp read many
     // addresses, so those tables are staged in shared memory.
     if (MAXSEG > 1 && (p.nseg == 1 || p.nunits >= 16ull * (uint64_t)p.nseg)) {
-        units_loop<DT, MAXR, false>(p, p.segs, u0, stride);
+        units_loop<DT, MAXR, false, WHOLE>(p, p.segs, u0, stride);
         return;
     }
     // an inline table of MAXSEG segments, or up to kSmemSegs of a device table
@@ -50,10 +52,10 @@ __global__ void __launch_bounds__(256, MAXR > 8 ? 2 : 4) purlin_latency_kernel(
     __shared__ Seg s_segs[kStage];
     const Seg *segs = stage_segs(p, s_segs, kStage);
     __syncthreads();
-    units_loop<DT, MAXR, false>(p, segs, u0, stride);
+    units_loop<DT, MAXR, false, WHOLE>(p, segs, u0, stride);
 }
 
-template <int DT, int MAXR, int MAXSEG>
+template <int DT, int MAXR, int MAXSEG, bool WHOLE = false>
 cudaError_t launch_lat_t(const LaunchArgs &a) {
     KParams<MAXR, MAXSEG> p;
     fill_params(p, a);
@@ -62,7 +64,7 @@ cudaError_t launch_lat_t(const LaunchArgs &a) {
     cfg.blockDim = dim3((unsigned)a.block);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = a.stream;
-    return cudaLaunchKernelEx(&cfg, purlin_latency_kernel<DT, MAXR, MAXSEG>, p);
+    return cudaLaunchKernelEx(&cfg, purlin_latency_kernel<DT, MAXR, MAXSEG, WHOLE>, p);
 }
 
 __global__ void purlin_empty_kernel() {}
@@ -107,7 +109,18 @@ uint32_t throughput_smem(uint32_t stages, uint32_t slot_stride) {
     return ring_workspace_bytes(stages, slot_stride);
 }
 
-cudaError_t launch_latency(const LaunchArgs &a) { return by_class(class_of(a), a.dtype, LatLaunch{a}); }
+cudaError_t launch_latency(const LaunchArgs &a) {
+    const int pc = class_of(a);
+    if (a.plan->all_whole && (pc == kClassSmall || pc == kClassDev8)) {
+        const bool f32 = a.dtype == PURLIN_F32;
+        if (pc == kClassSmall)
+            return f32 ? launch_lat_t<PURLIN_F32, kSmallMaxR, kSmallMaxSeg, true>(a)
+                       : launch_lat_t<PURLIN_BF16, kSmallMaxR, kSmallMaxSeg, true>(a);
+        return f32 ? launch_lat_t<PURLIN_F32, kSmallMaxR, 1, true>(a)
+                   : launch_lat_t<PURLIN_BF16, kSmallMaxR, 1, true>(a);
+    }
+    return by_class(pc, a.dtype, LatLaunch{a});
+}
 
 cudaError_t launch_throughput(const LaunchArgs &a) {
     if (ragged_ring(*a.plan)) return launch_throughput_ragged(a);

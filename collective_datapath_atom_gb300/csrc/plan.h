@@ -63,7 +63,9 @@ struct Seg {
     uint8_t tma;           // the body goes through the TMA ring
     uint8_t shift;         // tma: 16-byte phase of the source relative to the destination
     uint8_t dep_ratio;     // kSyncWait: notifying chunks covered by one chunk of this segment
-    uint8_t pad[2];
+    uint8_t whole;         // vector path only: source and destination offsets and length are
+                           // multiples of 16 (every unit a whole aligned window)
+    uint8_t pad[1];
 };
 static_assert(sizeof(Seg) == 56, "Seg layout is part of the kernel parameter block");
 
@@ -211,6 +213,7 @@ struct Plan {
     bool has_shifted_copies = false;  // copies the consumer warps shift into place
     bool has_phase_reduce = false;    // reduce chunks stored at another 16-byte phase
     bool composed = false;
+    bool all_whole = false;   // vector path, every segment a copy of whole aligned 16-byte windows
     int variant = kVariantNone;
 };
 

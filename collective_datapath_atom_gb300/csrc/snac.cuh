@@ -181,6 +181,49 @@ __device__ __forceinline__ void put_span(char *d, uint4 v, uint32_t b0, uint32_t
 // are the bytes outside its aligned body (head and tail, on the same grid)
 // (RING: the caller is the ring, whose segments may have a body; the
 // one-shot kernels' never do).
+// A unit of a segment made of whole aligned windows (Seg::whole, up to 8
+// ranks): no window bounds, no shift, plain 128-bit stores.  Same loads, same
+// rank-order sum and rounding as do_unit.  The vector kernel's build for plans
+// made only of such copies (AllGather, AllToAll at sizes that are multiples of
+// 16 bytes) calls it (kernels.cu).  Inlined into do_unit instead, it made the
+// 8-rank builds spill.
+template <int DT, int MAXR, class P>
+__device__ __forceinline__ void whole_unit(const P &p, const Seg &sg, uint64_t k) {
+    using V = atom::Vec<DT>;
+    const int R = p.R;
+    const uint64_t so = sg.src_off + 16 * k, doff = sg.dst_off + 16 * k;
+    uint4 out;
+    const char *self = nullptr;
+    if (sg.src_rank < 0) {   // reduce (SCORE): rank order, binary32, one rounding
+        uint4 v[MAXR];
+#pragma unroll
+        for (int j = 0; j < MAXR; ++j)
+            if (j < R) v[j] = atom::ld_v4(static_cast<const char *>(p.src[j]) + so);
+        float acc[V::VE];
+        V::init(acc, v[0]);
+#pragma unroll
+        for (int j = 1; j < MAXR; ++j)
+            if (j < R) V::add(acc, v[j]);
+        out = V::pack(acc);
+    } else {                 // copy, bitwise
+        const char *sbase = static_cast<const char *>(sg.src_is_dst ? p.dst[sg.src_rank]
+                                                                    : p.src[sg.src_rank]);
+        self = sbase + so;   // in-place AllGather: the block is already there
+        out = atom::ld_v4(self);
+    }
+    if (sg.dst_rank >= 0) {
+        char *d = static_cast<char *>(p.dst[sg.dst_rank]) + doff;
+        if (d != self) atom::st_v4(d, out);
+        return;
+    }
+#pragma unroll
+    for (int r = 0; r < MAXR; ++r) {
+        if (r >= R || r == sg.skip_rank) continue;
+        char *d = static_cast<char *>(p.dst[r]) + doff;
+        if (d != self) atom::st_v4(d, out);
+    }
+}
+
 template <int DT, int MAXR, bool RING, class P>
 __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
     using V = atom::Vec<DT>;
@@ -299,14 +342,16 @@ __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
 // Units u0, u0 + stride, ... of the plan: the first one's segment is found by
 // binary search, later ones by walking forward (units only increase), so
 // the search cost fades for threads that own many units.
-template <int DT, int MAXR, bool RING, class P>
+// WHOLE: every segment is made of whole aligned windows (whole_unit).
+template <int DT, int MAXR, bool RING, bool WHOLE = false, class P>
 __device__ __forceinline__ void units_loop(const P &p, const Seg *segs, uint64_t u0,
                                            uint64_t stride) {
     if (u0 >= p.nunits) return;
     int si = seg_of_unit(segs, p.nseg, u0);
     for (uint64_t u = u0; u < p.nunits; u += stride) {
         while (si + 1 < p.nseg && segs[si + 1].unit_begin <= u) ++si;
-        do_unit<DT, MAXR, RING>(p, segs[si], u - segs[si].unit_begin);
+        if constexpr (WHOLE) whole_unit<DT, MAXR>(p, segs[si], u - segs[si].unit_begin);
+        else do_unit<DT, MAXR, RING>(p, segs[si], u - segs[si].unit_begin);
     }
 }
 
