@@ -29,9 +29,10 @@ using ringk::fill_params;
 
 // Four CTAs of 256 threads per SM (the host's grid cap) leave 64 registers
 // a thread; the instantiations for more than 8 ranks take two.  WHOLE: a
-// build for plans whose segments are all copies of whole aligned 16-byte
-// windows (Plan::all_whole), with only the short unit path (whole_unit).
-template <int DT, int MAXR, int MAXSEG, bool WHOLE = false>
+// build for plans whose segments are all made of whole aligned 16-byte
+// windows and all copies (1) or all reductions (2) (Plan::whole_op), with
+// only the short unit path for that operation (whole_unit).
+template <int DT, int MAXR, int MAXSEG, int WHOLE = 0>
 __global__ void __launch_bounds__(256, MAXR > 8 ? 2 : 4) purlin_latency_kernel(
     const __grid_constant__ KParams<MAXR, MAXSEG> p) {
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
@@ -55,7 +56,7 @@ __global__ void __launch_bounds__(256, MAXR > 8 ? 2 : 4) purlin_latency_kernel(
     units_loop<DT, MAXR, false, WHOLE>(p, segs, u0, stride);
 }
 
-template <int DT, int MAXR, int MAXSEG, bool WHOLE = false>
+template <int DT, int MAXR, int MAXSEG, int WHOLE = 0>
 cudaError_t launch_lat_t(const LaunchArgs &a) {
     KParams<MAXR, MAXSEG> p;
     fill_params(p, a);
@@ -111,13 +112,19 @@ uint32_t throughput_smem(uint32_t stages, uint32_t slot_stride) {
 
 cudaError_t launch_latency(const LaunchArgs &a) {
     const int pc = class_of(a);
-    if (a.plan->all_whole && (pc == kClassSmall || pc == kClassDev8)) {
+    if (a.plan->whole_op != 0 && (pc == kClassSmall || pc == kClassDev8)) {
         const bool f32 = a.dtype == PURLIN_F32;
-        if (pc == kClassSmall)
-            return f32 ? launch_lat_t<PURLIN_F32, kSmallMaxR, kSmallMaxSeg, true>(a)
-                       : launch_lat_t<PURLIN_BF16, kSmallMaxR, kSmallMaxSeg, true>(a);
-        return f32 ? launch_lat_t<PURLIN_F32, kSmallMaxR, 1, true>(a)
-                   : launch_lat_t<PURLIN_BF16, kSmallMaxR, 1, true>(a);
+        const bool red = a.plan->whole_op == 2;
+        if (pc == kClassSmall) {
+            if (red) return f32 ? launch_lat_t<PURLIN_F32, kSmallMaxR, kSmallMaxSeg, 2>(a)
+                                : launch_lat_t<PURLIN_BF16, kSmallMaxR, kSmallMaxSeg, 2>(a);
+            return f32 ? launch_lat_t<PURLIN_F32, kSmallMaxR, kSmallMaxSeg, 1>(a)
+                       : launch_lat_t<PURLIN_BF16, kSmallMaxR, kSmallMaxSeg, 1>(a);
+        }
+        if (red) return f32 ? launch_lat_t<PURLIN_F32, kSmallMaxR, 1, 2>(a)
+                            : launch_lat_t<PURLIN_BF16, kSmallMaxR, 1, 2>(a);
+        return f32 ? launch_lat_t<PURLIN_F32, kSmallMaxR, 1, 1>(a)
+                   : launch_lat_t<PURLIN_BF16, kSmallMaxR, 1, 1>(a);
     }
     return by_class(pc, a.dtype, LatLaunch{a});
 }

@@ -406,12 +406,15 @@ purlin_status compile_plan(const CallDesc &c, int variant, int ar_mode, uint32_t
     size_t k = 0;
     for (Seg &s : p.segs)
         if (s.sync == kSyncWait) s.dep_chunk = k < notify_begin.size() ? notify_begin[k++] : 0;
-    // Copies only: the whole-window build measured faster for AllGather
-    // (256 B per rank 1.99 -> 1.72 us, 2 KiB 2.08 -> 1.96 us per call in a
-    // graph) and AllToAll (1-4%), and slower for the reductions (AllReduce
-    // +2% at 2 KiB, +6% at 8 MiB; ReduceScatter +10% at 8 MiB).
-    p.all_whole = variant == kVariantLatency && !p.segs.empty();
-    for (const Seg &s : p.segs) p.all_whole = p.all_whole && !s.tma && s.whole && s.src_rank >= 0;
+    // A vector-path plan of whole-window copies only, or reductions only,
+    // runs the vector kernel's build for that case (whole_unit).
+    bool whole = variant == kVariantLatency && !p.segs.empty(), copies = true, reduces = true;
+    for (const Seg &s : p.segs) {
+        whole = whole && !s.tma && s.whole;
+        copies = copies && s.src_rank >= 0;
+        reduces = reduces && s.src_rank < 0;
+    }
+    p.whole_op = !whole ? 0 : copies ? 1 : reduces ? 2 : 0;
     if (chunk > 0xFFFFFFF0ull) return PURLIN_ERR_INVALID_ARG;
     p.nchunks = chunk;
     p.nunits = unit;

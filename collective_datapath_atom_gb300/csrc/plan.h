@@ -213,7 +213,8 @@ struct Plan {
     bool has_shifted_copies = false;  // copies the consumer warps shift into place
     bool has_phase_reduce = false;    // reduce chunks stored at another 16-byte phase
     bool composed = false;
-    bool all_whole = false;   // vector path, every segment a copy of whole aligned 16-byte windows
+    int whole_op = 0;   // vector path, every segment of whole aligned 16-byte windows and
+                        // all copies (1) or all reductions (2); else 0
     int variant = kVariantNone;
 };
 

@@ -183,18 +183,20 @@ __device__ __forceinline__ void put_span(char *d, uint4 v, uint32_t b0, uint32_t
 // one-shot kernels' never do).
 // A unit of a segment made of whole aligned windows (Seg::whole, up to 8
 // ranks): no window bounds, no shift, plain 128-bit stores.  Same loads, same
-// rank-order sum and rounding as do_unit.  The vector kernel's build for plans
-// made only of such copies (AllGather, AllToAll at sizes that are multiples of
-// 16 bytes) calls it (kernels.cu).  Inlined into do_unit instead, it made the
-// 8-rank builds spill.
-template <int DT, int MAXR, class P>
+// rank-order sum and rounding as do_unit.  OP 1: a copy; OP 2: a reduction.
+// The vector kernel has a build for plans made only of such copies or only of
+// such reductions (kernels.cu): per call in a graph, AllReduce 2 KiB per rank
+// 1.88 -> 1.63 us and 256 B 1.85 -> 1.45 us, AllGather 256 B 1.99 -> 1.72 us.
+// One build with both operations made the reductions slower, and inlining
+// the short path into do_unit made the 8-rank builds spill.
+template <int DT, int MAXR, int OP, class P>
 __device__ __forceinline__ void whole_unit(const P &p, const Seg &sg, uint64_t k) {
     using V = atom::Vec<DT>;
     const int R = p.R;
     const uint64_t so = sg.src_off + 16 * k, doff = sg.dst_off + 16 * k;
     uint4 out;
     const char *self = nullptr;
-    if (sg.src_rank < 0) {   // reduce (SCORE): rank order, binary32, one rounding
+    if (OP == 2) {   // reduce (SCORE): rank order, binary32, one rounding
         uint4 v[MAXR];
 #pragma unroll
         for (int j = 0; j < MAXR; ++j)
@@ -213,14 +215,14 @@ __device__ __forceinline__ void whole_unit(const P &p, const Seg &sg, uint64_t k
     }
     if (sg.dst_rank >= 0) {
         char *d = static_cast<char *>(p.dst[sg.dst_rank]) + doff;
-        if (d != self) atom::st_v4(d, out);
+        if (OP == 2 || d != self) atom::st_v4(d, out);
         return;
     }
 #pragma unroll
     for (int r = 0; r < MAXR; ++r) {
         if (r >= R || r == sg.skip_rank) continue;
         char *d = static_cast<char *>(p.dst[r]) + doff;
-        if (d != self) atom::st_v4(d, out);
+        if (OP == 2 || d != self) atom::st_v4(d, out);
     }
 }
 
@@ -343,14 +345,14 @@ __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
 // binary search, later ones by walking forward (units only increase), so
 // the search cost fades for threads that own many units.
 // WHOLE: every segment is made of whole aligned windows (whole_unit).
-template <int DT, int MAXR, bool RING, bool WHOLE = false, class P>
+template <int DT, int MAXR, bool RING, int WHOLE = 0, class P>
 __device__ __forceinline__ void units_loop(const P &p, const Seg *segs, uint64_t u0,
                                            uint64_t stride) {
     if (u0 >= p.nunits) return;
     int si = seg_of_unit(segs, p.nseg, u0);
     for (uint64_t u = u0; u < p.nunits; u += stride) {
         while (si + 1 < p.nseg && segs[si + 1].unit_begin <= u) ++si;
-        if constexpr (WHOLE) whole_unit<DT, MAXR>(p, segs[si], u - segs[si].unit_begin);
+        if constexpr (WHOLE != 0) whole_unit<DT, MAXR, WHOLE>(p, segs[si], u - segs[si].unit_begin);
         else do_unit<DT, MAXR, RING>(p, segs[si], u - segs[si].unit_begin);
     }
 }
