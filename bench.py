@@ -435,7 +435,8 @@ def config_rows(P, ctx, torch, device, stream, flush, peak):
     exceed the L2, and for messages of up to 32 MiB per rank the device time
     per call in a CUDA graph, L2 flushed and warm.  Effective GB/s =
     algorithmic read+write bytes / time; frac = that / the measured copy
-    peak.  Inputs: the small exact-integer AllReduce from the host
+    peak; algbw = the pages' totalBytes (one rank's input) / the
+    single-launch time.  Inputs: the small exact-integer AllReduce from the host
     generator; the large ones N(0,1) drawn on the device from a seeded
     generator (the values do not change the work; the parity tests use the
     host-generated workloads)."""
@@ -448,6 +449,9 @@ def config_rows(P, ctx, torch, device, stream, flush, peak):
         return torch.randn(n, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
 
     def measure(name, fn, algo, in_bytes, reps, graph=False):
+        # none of these rows is an AllGather: the pages' totalBytes is the
+        # input size of one rank (every rank's input has the same size here)
+        total = in_bytes // 8
         fn()
         P.purlin_check(ctx)
         info = P.purlin_last_launch(ctx)
@@ -456,6 +460,7 @@ def config_rows(P, ctx, torch, device, stream, flush, peak):
                "algorithmic_bytes": algo, "us_single_flushed": single,
                "gbs_single_flushed": algo / (single * 1e-6) / 1e9}
         row["frac_single_flushed"] = row["gbs_single_flushed"] / peak
+        row.update({"total_bytes": total, "algbw_gbs_single_flushed": total / (single * 1e-6) / 1e9})
         traffic = recorded_traffic(name)   # DRAM bytes per launch, ncu, this kernel source
         if traffic is not None:
             row.update({"traffic": traffic, "traffic_over_algorithmic": traffic / algo})
@@ -650,6 +655,12 @@ def run_gpu(args, rank, world, local_rank):
     ms_per_step = total_ms / args.steps
     value = whole_job_gbs(algo_bytes, args.steps, world, total_ms)
 
+    # the pages' "algorithm bandwidth": totalBytes / time, with totalBytes the
+    # output size of one rank for AllGather and the input size of one rank
+    # otherwise (the largest rank's, where V counts make them differ)
+    total_bytes = (max(d.numel() * d.element_size() for d in dst) if call[0] == "all_gather"
+                   else max(x.nbytes for x in ins))
+
     # roofline of the dominant (only) kernel: one launch per step
     peak, peak_kind = measured_peaks()
     achieved = algo_bytes / (float(np.mean(ms)) / 1e3) / 1e9
@@ -745,6 +756,9 @@ def run_gpu(args, rank, world, local_rank):
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
                      "kernel": KERNEL_OF_VARIANT.get(info["variant"], "none")},
+        "algbw": {"total_bytes": total_bytes, "gbs": total_bytes / (ms_per_step / 1e3) / 1e9,
+                  "note": "pages-style algorithm bandwidth (totalBytes / device time per step), "
+                          "not the headline metric"},
         "back_to_back": b2b,
         "configs": configs,
         "small_messages": small,
