@@ -329,12 +329,18 @@ __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
     if (sg.dst_rank >= 0) {
         put_span<ES>(static_cast<char *>(p.dst[sg.dst_rank]) + doff, out, sh, nb);
     } else if (MAXR <= 8) {
-        // static indices: the destination pointers are read from the
+        // static indices: each destination pointer is read from the
         // parameters directly, not one indexed load per store
+        if (sh == 0 && nb == 16u && (doff & 15u) == 0) {   // whole window (bases 16-B aligned)
 #pragma unroll
-        for (int r = 0; r < MAXR; ++r)
-            if (r < R && r != sg.skip_rank)
-                put_span<ES>(static_cast<char *>(p.dst[r]) + doff, out, sh, nb);
+            for (int r = 0; r < MAXR; ++r)
+                if (r < R && r != sg.skip_rank) atom::st_v4(static_cast<char *>(p.dst[r]) + doff, out);
+        } else {
+#pragma unroll
+            for (int r = 0; r < MAXR; ++r)
+                if (r < R && r != sg.skip_rank)
+                    put_span_words<ES>(static_cast<char *>(p.dst[r]) + doff, out, sh, nb);
+        }
     } else {
         for (int r = 0; r < R; ++r)
             if (r != sg.skip_rank) put_span<ES>(static_cast<char *>(p.dst[r]) + doff, out, sh, nb);
