@@ -374,8 +374,10 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
         if (throughput_occupancy(c.dtype, pclass, ragged, block, smem, &per_sm) != cudaSuccess ||
             per_sm < 1)
             return PURLIN_ERR_UNSUPPORTED;
-        int64_t grid = (int64_t)ctx->sms * std::min(per_sm, std::max(1, shape.ctas_per_sm));
-        if (ctx->opt[PURLIN_OPT_CTAS] > 0) grid = std::min<int64_t>(grid, ctx->opt[PURLIN_OPT_CTAS]);
+        // the policy's CTAs per SM, or the option's grid; never more than fit at once
+        int64_t grid = ctx->opt[PURLIN_OPT_CTAS] > 0
+                           ? std::min<int64_t>(ctx->opt[PURLIN_OPT_CTAS], (int64_t)ctx->sms * per_sm)
+                           : (int64_t)ctx->sms * std::min(per_sm, std::max(1, shape.ctas_per_sm));
         int64_t work = (int64_t)std::max<uint64_t>(pl.nchunks, (pl.nunits + 255) / 256);
         grid = std::max<int64_t>(1, std::min<int64_t>(grid, work));
         a.grid = (int)grid;

@@ -92,8 +92,10 @@ purlin_status run_vcounts(purlin_ctx *ctx, purlin_collective coll, const void *c
     a.dtype = dtype;
     a.vector_copies = ctx->opt[PURLIN_OPT_COPY_STORES] == 0 ? shape.vector_copies
                                                             : ctx->opt[PURLIN_OPT_COPY_STORES] == 2;
-    int64_t grid = (int64_t)ctx->sms * std::min(per_sm, std::max(1, shape.ctas_per_sm));
-    if (ctx->opt[PURLIN_OPT_CTAS] > 0) grid = std::min<int64_t>(grid, ctx->opt[PURLIN_OPT_CTAS]);
+    // the policy's CTAs per SM, or the option's grid; never more than fit at once
+    int64_t grid = ctx->opt[PURLIN_OPT_CTAS] > 0
+                       ? std::min<int64_t>(ctx->opt[PURLIN_OPT_CTAS], (int64_t)ctx->sms * per_sm)
+                       : (int64_t)ctx->sms * std::min(per_sm, std::max(1, shape.ctas_per_sm));
     a.grid = (int)grid;
     a.block = block;
     a.smem = smem;

@@ -287,7 +287,7 @@ typedef enum {
                                         (messages up to 1 MiB per rank; larger ones run mode 2) */
     PURLIN_OPT_CHUNK_BYTES = 3,      /* bytes per source per chunk in the TMA ring */
     PURLIN_OPT_STAGES = 4,           /* TMA ring depth */
-    PURLIN_OPT_CTAS = 5,             /* CTAs of a throughput launch */
+    PURLIN_OPT_CTAS = 5,             /* CTAs of a throughput launch (0: the policy's; at most what fits at once) */
     PURLIN_OPT_SPIN_TIMEOUT_NS = 6,  /* bound on a cross-CTA flag wait (default 100 ms) */
     PURLIN_OPT_DROP_NOTIFY = 7,      /* host-side fault injection: chunk whose notify is skipped; -1 off */
     PURLIN_OPT_LAT_CTAS = 8,         /* max CTAs of a latency launch */

@@ -217,6 +217,37 @@ def test_allreduce_composed_mode(P, dtype, R):
         ctx.close()
 
 
+@pytest.mark.parametrize("coll", ["all_gather", "reduce_scatter", "all_reduce", "all_to_all"])
+def test_ring_grid_option_above_policy(P, ctx8, coll):
+    """PURLIN_OPT_CTAS may ask for more throughput CTAs than the policy's CTAs
+    per SM, up to what fits on the GPU at once: a small ring shape runs two
+    CTAs per SM, an oversized request is capped, and the results stay exact."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    dtype = 1
+    n = (1 << 20) + 40            # several chunks per CTA and a ragged tail
+    n -= n % 8 if coll in ("reduce_scatter", "all_to_all") else 0
+    P.purlin_set_option(ctx8, P.PURLIN_OPT_VARIANT, 2)
+    P.purlin_set_option(ctx8, P.PURLIN_OPT_CONSUMER_WARPS, 4)
+    P.purlin_set_option(ctx8, P.PURLIN_OPT_STAGES, 2)
+    P.purlin_set_option(ctx8, P.PURLIN_OPT_CHUNK_BYTES, 2048)   # 32 KiB stages at most
+    try:
+        for k, want in enumerate((2 * sms, 1 << 20)):
+            P.purlin_set_option(ctx8, P.PURLIN_OPT_CTAS, want)
+            ins = gen_inputs([n] * 8, dtype, seed=301 + k)
+            got, _ = run(P, ctx8, coll, ins, out_sizes(coll, 8, n, None, 2), dtype, n)
+            assert_same(got, oracle_of(coll, ins, dtype), f"{coll} CTAs={want}")
+            info = P.purlin_last_launch(ctx8)
+            assert info["variant"] in (2, 3)
+            if want == 2 * sms:
+                assert info["grid"] == 2 * sms
+            else:
+                assert 2 * sms <= info["grid"] <= 32 * sms   # the occupancy limit
+    finally:
+        for opt in (P.PURLIN_OPT_CTAS, P.PURLIN_OPT_CONSUMER_WARPS, P.PURLIN_OPT_STAGES,
+                    P.PURLIN_OPT_CHUNK_BYTES, P.PURLIN_OPT_VARIANT):
+            P.purlin_set_option(ctx8, opt, 0)
+
+
 def test_allreduce_composed_flag_generations(P, ctx8):
     """Composed AllReduce with more reducing chunks than flag slots per
     parity (256 MiB per rank, 65536 chunks of 4 KiB): chunk c publishes
