@@ -40,14 +40,14 @@ Policy policy_for(purlin_collective coll, int R) {
     // measured with each variant forced (single launches, 4 KiB..32 MiB).
     switch (coll) {
         case PURLIN_COLL_REDUCE_SCATTER:
-            return {clamp16(98304 / (uint64_t)R, 1024, 16384), 2, 32ull << 20, false, 0, 1};
+            return {clamp16(98304 / (uint64_t)R, 1024, 16384), 2, 48ull << 20, false, 0, 1};
         case PURLIN_COLL_REDUCE_SCATTER_V:   // both paths read ragged blocks aligned
-            return {clamp16(98304 / (uint64_t)R, 1024, 16384), 2, 32ull << 20, false, 0, 1};
+            return {clamp16(98304 / (uint64_t)R, 1024, 16384), 2, 24ull << 20, false, 0, 1};
         case PURLIN_COLL_ALL_REDUCE:
             // (composed mode: the gather chunks are stored by the consumer warps)
             return {clamp16(32768 / (uint64_t)R, 512, 8192), 3, 16ull << 20, true, 0, 1};
         case PURLIN_COLL_ALL_GATHER:
-            return {16384, 4, 1ull << 20, true, 8, 1};
+            return {16384, 4, 2ull << 20, true, 8, 1};
         case PURLIN_COLL_ALL_GATHER_V:   // a Zipf split's largest input is 1.18x the mean
             return {16384, 4, 3ull << 20, true, 8, 1};
         default:   // AllToAll(V): two CTAs per SM

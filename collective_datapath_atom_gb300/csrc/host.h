@@ -26,13 +26,15 @@ constexpr int kShiftedCopyConsumerWarps = 6;
 // from the Datapath of Collectives" §4.2), measured on GB300 over 256 B..64
 // MiB per rank and at the workloads' sizes.
 // Crossover: per-rank message bytes up to which the one-shot vector kernel
-// beats the staged ring.  At 64 registers it runs four CTAs of 256 threads
-// per SM, which keeps enough loads in flight that for reductions it wins up
-// to tens of MiB: ReduceScatter and ReduceScatterV 32 MiB (ragged blocks
-// read aligned on both paths; at 64 MiB the ring leads, 0.97 of the copy
-// peak against 0.92), AllReduce 16 MiB (at 32 MiB the two variants trade
-// places from box to box), AllGather 1 MiB, AllGatherV 3 MiB, AllToAll(V)
-// 256 KiB.
+// beats the staged ring (both forced, single launches and graph replays
+// with the L2 flushed, 256 KiB..64 MiB per rank at R = 8).  At 64 registers
+// it runs four CTAs of 256 threads per SM, which keeps enough loads in
+// flight that for reductions it wins up to tens of MiB: ReduceScatter 48 MiB
+// (its whole-window build leads the ring by 2.6% there and ties it at 64
+// MiB), ReduceScatterV 24 MiB (ragged blocks take the general build; at 32
+// MiB the ring leads by 3.5%), AllReduce 16 MiB (the two tie at 24 MiB, the
+// ring leads from 32 MiB), AllGather 2 MiB (they tie at 3 MiB), AllGatherV
+// 3 MiB (its largest input), AllToAll(V) 256 KiB.
 // Ring shape:
 //   ReduceScatter(V)  one destination per reduced chunk: large per-source
 //                     chunks (96 KiB per stage), 2 stages;
