@@ -45,11 +45,11 @@ Policy policy_for(purlin_collective coll, int R) {
             return {clamp16(98304 / (uint64_t)R, 1024, 16384), 2, 24ull << 20, false, 0, 1};
         case PURLIN_COLL_ALL_REDUCE:
             // (composed mode: the gather chunks are stored by the consumer warps)
-            return {clamp16(32768 / (uint64_t)R, 512, 8192), 3, 16ull << 20, true, 0, 1};
+            return {clamp16(32768 / (uint64_t)R, 512, 8192), 4, 16ull << 20, true, 0, 1};
         case PURLIN_COLL_ALL_GATHER:
-            return {16384, 4, 2ull << 20, true, 8, 1};
+            return {16384, 2, 2ull << 20, true, 8, 1};
         case PURLIN_COLL_ALL_GATHER_V:   // a Zipf split's largest input is 1.18x the mean
-            return {16384, 4, 3ull << 20, true, 8, 1};
+            return {16384, 2, 3ull << 20, true, 8, 1};
         default:   // AllToAll(V): two CTAs per SM
             return {16384, 3, 256ull << 10, false, 0, 2};
     }
@@ -96,13 +96,14 @@ purlin_status ring_shape(const purlin_ctx *ctx, const CallDesc &c, const Policy 
     RingShape r;
     r.slot_stride = (pl.slot_bytes + 127u) & ~127u;
     // Point-to-point copies at other 16-byte phases (ragged AllToAllV) go
-    // through the consumer warps: 6 warps and a deeper ring keep two CTAs
-    // per SM (measured +35% over 8 warps).
+    // through the consumer warps: 6 warps keep two CTAs per SM (measured +35%
+    // over 8 warps).  They keep the policy's 3 stages: 4 measured 5-6% slower
+    // from 16 to 256 MiB per rank, 2 slower still.
     const bool shifted_p2p = pl.has_shifted_copies && !shape.vector_copies &&
                              (c.coll == PURLIN_COLL_ALL_TO_ALL ||
                               c.coll == PURLIN_COLL_ALL_TO_ALL_V);
     uint32_t stages = (uint32_t)(ctx->opt[PURLIN_OPT_STAGES] > 0 ? ctx->opt[PURLIN_OPT_STAGES]
-                                 : shifted_p2p ? 4u : shape.stages);
+                                                                 : shape.stages);
     stages = std::min<uint32_t>(32, std::max<uint32_t>(2, stages));
     while (stages > 2 && throughput_smem(stages, r.slot_stride) > limit) --stages;
     r.stages = stages;

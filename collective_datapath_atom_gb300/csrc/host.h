@@ -38,11 +38,15 @@ constexpr int kShiftedCopyConsumerWarps = 6;
 // Ring shape:
 //   ReduceScatter(V)  one destination per reduced chunk: large per-source
 //                     chunks (96 KiB per stage), 2 stages;
-//   AllReduce         R stores per reduced vector: 32 KiB per stage, 3 stages;
+//   AllReduce         R stores per reduced vector: 32 KiB per stage, 4 stages
+//                     (0.8-0.9% faster than 3 at 64 and 256 MiB per rank);
 //   AllGather(V)      one staged tile written to R destinations: 16 KiB
-//                     chunks, 4 stages, and the 8 consumer warps store the
+//                     chunks, 2 stages, and the 8 consumer warps store the
 //                     tile with 128-bit stores (0.956 of the copy peak versus
-//                     0.92 with bulk stores from one warp);
+//                     0.92 with bulk stores from one warp).  2 stages against
+//                     4: AllGather 2.6% faster at 16 MiB per rank and 5.8-6.7%
+//                     at 64-128 MiB, level at 4-8 MiB; AllGatherV level to
+//                     0.6% faster;
 //   AllToAll(V)       one load, one store per chunk: 16 KiB chunks, 3 stages,
 //                     bulk stores (0.98).
 struct Policy {
