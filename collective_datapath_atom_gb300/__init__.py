@@ -147,6 +147,7 @@ _SIGNATURES = {
     "purlin_all_reduce_noalloc": (ctypes.c_int, [ctypes.c_int, _VPP, _VPP, ctypes.c_size_t,
                                                  ctypes.c_int, ctypes.c_int, purlin_layout,
                                                  ctypes.c_void_p]),
+    "purlin_noalloc_check": (ctypes.c_int, [ctypes.c_void_p]),
     "purlin_empty_launch": (ctypes.c_int, [ctypes.c_void_p]),
     "purlin_touch_launch": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "purlin_check": (ctypes.c_int, [_CTX]),
@@ -362,6 +363,12 @@ def purlin_all_reduce_noalloc(R, src, dst, n, dtype, op=None, layout=None, strea
     _ok(lib.purlin_all_reduce_noalloc(int(R), ps, pd, int(n), int(dtype), int(op),
                                       _layout(layout), ctypes.c_void_p(_stream_handle(stream))),
         "purlin_all_reduce_noalloc")
+
+
+def purlin_noalloc_check(stream=None):
+    """Synchronize `stream` and raise if a device-side wait of an
+    allocation-free AllReduce expired since the last check."""
+    _ok(lib.purlin_noalloc_check(ctypes.c_void_p(_stream_handle(stream))), "purlin_noalloc_check")
 
 
 def purlin_empty_launch(stream=None):

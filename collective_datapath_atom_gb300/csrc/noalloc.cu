@@ -37,8 +37,10 @@
 // Calls whose kernels overlap on the GPU (e.g. issued on two streams
 // without ordering) race on the flags and give wrong results: order them.
 // A device-side wait that expires (100 ms bound) is recorded in the error
-// word, which no call reads back and the next call clears: a caller cannot
-// learn that it happened, and that call's outputs are then unspecified.
+// word, and that call's outputs are then unspecified.  The next call clears
+// the word, so a caller that wants to know reads it first with
+// purlin_noalloc_check (a stream synchronize and one 8-byte copy to the
+// host; not during stream capture).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -179,4 +181,25 @@ extern "C" purlin_status purlin_all_reduce_noalloc(int R, const void *const src[
     a.stream = s;
     if (launch_throughput(a) != cudaSuccess) return PURLIN_ERR_CUDA;
     return PURLIN_OK;
+}
+
+extern "C" purlin_status purlin_noalloc_check(purlin_stream stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return PURLIN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    const DeviceState &ds = g_dev[dev];
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PURLIN_ERR_CUDA;
+    if (!ds.ready) return PURLIN_OK;   // no call on this device yet
+    unsigned long long word = 0;
+    unsigned long long *err = ds.scratch + kErrWord;
+    if (cudaMemcpyAsync(&word, err, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return PURLIN_ERR_CUDA;
+    if (word == 0) return PURLIN_OK;
+    if (cudaMemsetAsync(err, 0, sizeof word, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return PURLIN_ERR_CUDA;
+    return PURLIN_ERR_TIMEOUT;
 }

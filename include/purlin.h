@@ -234,16 +234,25 @@ purlin_status purlin_all_to_all_v_device_counts(purlin_ctx *ctx, const void *con
  * sets kernel attributes and zeroes the array with a blocking cudaMemset:
  * make it before any stream capture.  Every call shares the array (it keeps
  * the previous call's contents; the error word is cleared per call), so
- * calls that overlap on the GPU race: order them on one stream.  A caller
- * cannot learn that a device-side wait expired: the kernel records it in the
- * array's error word (100 ms bound per wait, then the launch ends early and
- * that call's outputs are unspecified), but nothing reads that word back and
- * the next call clears it.  Needs about 193 KiB of dynamic shared memory per
+ * calls that overlap on the GPU race: order them on one stream.  A device-
+ * side wait that expires (100 ms bound per wait; the launch then ends early
+ * and that call's outputs are unspecified) is recorded in the array's error
+ * word, which the next call clears: read it before then with
+ * purlin_noalloc_check.  Needs about 193 KiB of dynamic shared memory per
  * CTA (two 96 KiB stages); a device with less returns UNSUPPORTED.  Errors
  * as for purlin_all_reduce, plus CUDA if the set-up or the launch fails. */
 purlin_status purlin_all_reduce_noalloc(int R, const void *const src[], void *const dst[],
                                         size_t n, purlin_dtype dtype, purlin_op op,
                                         purlin_layout layout, purlin_stream stream);
+
+/* Status of the allocation-free AllReduce calls on the current device that
+ * `stream` has run: synchronizes `stream`, reads the scratch array's error
+ * word and clears it.  OK if no device-side wait expired since the word was
+ * last cleared (or no call ran on this device yet); TIMEOUT if one did, and
+ * the outputs of the calls since then are unspecified; CUDA if the
+ * synchronize or the 8-byte copy fails (a device fault).  Not during stream
+ * capture.  Allocates nothing. */
+purlin_status purlin_noalloc_check(purlin_stream stream);
 
 /* ------------------------------------------------------------ measurement */
 

@@ -86,6 +86,7 @@ def test_noalloc_allreduce_in_a_graph(P):
     replay_and_check(P, stream,
                      lambda: P.purlin_all_reduce_noalloc(R, src, dst, n, 1, stream=stream),
                      src, dst, n, calls_per_graph=3)
+    P.purlin_noalloc_check(stream)   # raises if a replayed call's device wait expired
 
 
 def test_device_collective_in_a_graph(P):

@@ -84,6 +84,8 @@ def test_noalloc_matches_context_allreduce_twice(P, dtype, R, n):
             P.purlin_check(ctx)
             st = _call_noalloc(P, R, src, got, n, dtype, stream)
             assert st == P.PURLIN_OK, P.status_string(st)
+            st = P.lib.purlin_noalloc_check(ctypes.c_void_p(stream.cuda_stream))
+            assert st == P.PURLIN_OK, P.status_string(st)   # no device-side wait expired
             torch.cuda.synchronize()
             for d in range(R):
                 assert torch.equal(got[d], exact), f"call {call} rank {d}: differs from the oracle"
@@ -102,6 +104,7 @@ def test_noalloc_allocates_no_device_memory(P):
     free0, _ = torch.cuda.mem_get_info()
     for _ in range(3):
         assert _call_noalloc(P, R, src, dst, n, 1, stream) == P.PURLIN_OK
+        assert P.lib.purlin_noalloc_check(ctypes.c_void_p(stream.cuda_stream)) == P.PURLIN_OK
     torch.cuda.synchronize()
     free1, _ = torch.cuda.mem_get_info()
     assert free1 == free0
