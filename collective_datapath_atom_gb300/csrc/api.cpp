@@ -37,7 +37,7 @@ Policy policy_for(purlin_collective coll, int R) {
         return (uint32_t)(std::min(hi, std::max(lo, v)) & ~uint64_t(15));
     };
     // Crossovers: the largest per-rank input the vector kernel wins at,
-    // measured with each variant forced (single launches, 4 KiB..32 MiB).
+    // measured with each variant forced (host.h).
     switch (coll) {
         case PURLIN_COLL_REDUCE_SCATTER:
             return {clamp16(98304 / (uint64_t)R, 1024, 16384), 2, 48ull << 20, false, 0, 1};
@@ -158,6 +158,10 @@ constexpr size_t kPlanCacheCap = 64;
 // Built-in policy.
 constexpr int64_t kInspectChunkBytes = 32 * 1024;        // plan_inspect default chunk
 constexpr int kLatBlock = 256;
+// Small plans whose every unit stores to all R ranks: see the latency launch.
+constexpr uint64_t kSpreadUnits = 16384;
+constexpr uint64_t kSpreadCtas = 16;
+constexpr uint64_t kSpreadVectors = 2048;
 
 int64_t env_or(const char *name, int64_t dflt) {
     const char *v = std::getenv(name);
@@ -357,6 +361,26 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
         const int max_block = ctx->opt[PURLIN_OPT_LAT_BLOCK] > 0
                                   ? (int)ctx->opt[PURLIN_OPT_LAT_BLOCK] : kLatBlock;
         int block = (int)std::min<uint64_t>(max_block, (pl.nunits + 31) / 32 * 32);
+        // A small plan whose every unit stores to all R ranks (AllReduce,
+        // AllGather(V)) writes R times what it reads: spread it over about
+        // 16 CTAs of 32-128 threads so more SMs drain the stores.  Per call
+        // in a CUDA graph (R = 8, bf16, alternating builds on one box):
+        // AllReduce 2-256 KiB per rank 1.58-2.08 -> 1.39-1.76 us, AllGather
+        // 512 B-16 KiB 1.84-1.96 -> 1.71-1.75 us.  Plans that move fewer
+        // than kSpreadVectors 16-byte vectors (loads + stores) or hold more
+        // than kSpreadUnits units were slower spread, and so were
+        // ReduceScatter and AllToAll (one store per unit): they keep blocks
+        // of up to 256.
+        if (ctx->opt[PURLIN_OPT_LAT_BLOCK] <= 0 && pl.nunits <= kSpreadUnits && !pl.segs.empty() &&
+            std::all_of(pl.segs.begin(), pl.segs.end(),
+                        [](const Seg &sg) { return sg.dst_rank == kRankAll; })) {
+            const bool red = pl.segs.front().src_rank == kRankAll;
+            const uint64_t vectors = pl.nunits * (uint64_t)(red ? 2 * c.R : 1 + c.R);
+            if (vectors >= kSpreadVectors) {
+                const uint64_t per = (pl.nunits + kSpreadCtas - 1) / kSpreadCtas;
+                block = (int)std::min<uint64_t>(128, std::max<uint64_t>(32, (per + 31) / 32 * 32));
+            }
+        }
         uint64_t want = (pl.nunits + block - 1) / block;
         a.block = block;
         a.grid = (int)std::max<uint64_t>(1, std::min<uint64_t>(want, (uint64_t)cap));
