@@ -217,6 +217,34 @@ def test_allreduce_composed_mode(P, dtype, R):
         ctx.close()
 
 
+@pytest.mark.parametrize("coll,n,spread", [
+    ("all_reduce", 1024, True),     # 2 KiB per rank: 128 units of 16 vectors
+    ("all_reduce", 1 << 17, True),  # 256 KiB per rank: 16384 units, the largest spread plan
+    ("all_reduce", 1 << 18, False),  # 32768 units: more than a spread plan holds
+    ("all_reduce", 512, False),     # 64 units: too light to spread
+    ("all_gather", 512, True),      # 1 KiB per rank: 512 units of 9 vectors
+    ("all_gather", 128, False),     # 256 B per rank: too light
+    ("reduce_scatter", 1024, False),  # one store per unit: never spread
+])
+def test_small_all_rank_plans_spread(P, ctx8, coll, n, spread):
+    """A small vector-kernel plan whose every unit stores to all R ranks runs
+    about 16 CTAs of 32-128 threads; other plans keep blocks of up to 256.
+    The results match the oracle either way."""
+    dtype = 1
+    ins = gen_inputs([n] * 8, dtype, seed=411)
+    got, _ = run(P, ctx8, coll, ins, out_sizes(coll, 8, n, None, 2), dtype, n)
+    assert_same(got, oracle_of(coll, ins, dtype), f"{coll} n={n}")
+    info = P.purlin_last_launch(ctx8)
+    assert info["variant"] == 1
+    units = {"all_reduce": n // 8, "all_gather": n, "reduce_scatter": n // 8}[coll]
+    assert info["units"] == units
+    if spread:
+        assert 32 <= info["block"] <= 128 and info["grid"] == -(-units // info["block"])
+        assert info["grid"] >= min(16, units // 32)
+    else:
+        assert info["block"] == min(256, -(-units // 32) * 32)
+
+
 @pytest.mark.parametrize("coll", ["all_gather", "reduce_scatter", "all_reduce", "all_to_all"])
 def test_ring_grid_option_above_policy(P, ctx8, coll):
     """PURLIN_OPT_CTAS may ask for more throughput CTAs than the policy's CTAs
