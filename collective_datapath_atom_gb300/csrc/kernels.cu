@@ -31,12 +31,18 @@ using ringk::fill_params;
 // a thread; the instantiations for more than 8 ranks take two.  WHOLE: a
 // build for plans whose segments are all made of whole aligned 16-byte
 // windows and all copies (1) or all reductions (2) (Plan::whole_op), with
-// only the short unit path for that operation (whole_unit).
+// only the short unit path for that operation (whole_unit); 3, a uniform
+// AllToAll, reads no segment table at all (transposed_unit).
 template <int DT, int MAXR, int MAXSEG, int WHOLE = 0>
 __global__ void __launch_bounds__(256, MAXR > 8 ? 2 : 4) purlin_latency_kernel(
     const __grid_constant__ KParams<MAXR, MAXSEG> p) {
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
     const uint64_t u0 = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if constexpr (WHOLE == 3) {   // uniform AllToAll: addresses from the unit index alone
+        const uint32_t W = (uint32_t)(p.nunits / (uint64_t)(p.R * p.R));
+        for (uint64_t u = u0; u < p.nunits; u += stride) transposed_unit<MAXR>(p, (uint32_t)u, W);
+        return;
+    }
     // An inline table whose segments are long (16 or more units each on
     // average, or a single segment) is read straight from the parameter bank:
     // the threads of a warp then look at one or two segments, nearly a
@@ -111,6 +117,8 @@ uint32_t throughput_smem(uint32_t stages, uint32_t slot_stride) {
 }
 
 cudaError_t launch_latency(const LaunchArgs &a) {
+    if (a.plan->whole_op == 3 && a.R <= kSmallMaxR)   // bytes only: one build serves both dtypes
+        return launch_lat_t<PURLIN_BF16, kSmallMaxR, 1, 3>(a);
     const int pc = class_of(a);
     if (a.plan->whole_op != 0 && (pc == kClassSmall || pc == kClassDev8)) {
         const bool f32 = a.dtype == PURLIN_F32;

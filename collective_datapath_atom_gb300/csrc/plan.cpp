@@ -296,6 +296,7 @@ void raw_segments(const CallDesc &c, bool composed, uint32_t red_chunk, std::vec
 }  // namespace
 
 constexpr uint64_t kLineBytes = 128;   // an L2 line
+constexpr int kTransposeMaxR = 8;       // the vector kernel's build for whole_op 3
 
 purlin_status compile_plan(const CallDesc &c, int variant, int ar_mode, uint32_t red_slot_bytes,
                            uint32_t copy_chunk, Plan *out) {
@@ -415,6 +416,24 @@ purlin_status compile_plan(const CallDesc &c, int variant, int ar_mode, uint32_t
         reduces = reduces && s.src_rank < 0;
     }
     p.whole_op = !whole ? 0 : copies ? 1 : reduces ? 2 : 0;
+    // A uniform AllToAll of whole windows: block (s, d) is segment s*R + d,
+    // W windows from offset d*W*16 of source s to offset s*W*16 of
+    // destination d.  The vector kernel then computes each unit's addresses
+    // from its index, with no table to fetch or search.
+    const size_t R2 = (size_t)c.R * (size_t)c.R;
+    if (p.whole_op == 1 && c.coll == PURLIN_COLL_ALL_TO_ALL && c.R <= kTransposeMaxR &&
+        p.segs.size() == R2 && unit < (1ull << 32)) {
+        const uint64_t B = p.segs[0].bytes, W = B / 16;
+        bool uniform = B > 0 && B % 16 == 0 && unit == (uint64_t)R2 * W;
+        for (size_t i = 0; uniform && i < R2; ++i) {
+            const Seg &g = p.segs[i];
+            const int sr = (int)(i / (size_t)c.R), dr = (int)(i % (size_t)c.R);
+            uniform = g.src_rank == sr && g.dst_rank == dr && g.bytes == B &&
+                      g.src_off == (uint64_t)dr * B && g.dst_off == (uint64_t)sr * B &&
+                      g.unit_begin == (uint64_t)i * W;
+        }
+        if (uniform) p.whole_op = 3;
+    }
     if (chunk > 0xFFFFFFF0ull) return PURLIN_ERR_INVALID_ARG;
     p.nchunks = chunk;
     p.nunits = unit;

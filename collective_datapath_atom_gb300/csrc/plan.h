@@ -214,7 +214,10 @@ struct Plan {
     bool has_phase_reduce = false;    // reduce chunks stored at another 16-byte phase
     bool composed = false;
     int whole_op = 0;   // vector path, every segment of whole aligned 16-byte windows and
-                        // all copies (1) or all reductions (2); else 0
+                        // all copies (1) or all reductions (2); 3: an AllToAll of R*R
+                        // equal blocks of W windows in (source, destination) order and
+                        // fewer than 2^32 units, whose unit u is window u % W of block
+                        // u / W (no segment table needed); else 0
     int variant = kVariantNone;
 };
 

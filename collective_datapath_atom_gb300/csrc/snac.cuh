@@ -226,6 +226,26 @@ __device__ __forceinline__ void whole_unit(const P &p, const Seg &sg, uint64_t k
     }
 }
 
+// Unit u of a uniform AllToAll of whole windows (Plan::whole_op 3): window
+// k = u % W of block (s, d) = (u / W / R, u / W % R), copied from offset
+// (d*W + k)*16 of source s to offset (s*W + k)*16 of destination d.  The
+// rank pointers are picked with static indices (parameter reads at fixed
+// offsets), as in the reduce path's stores.
+template <int MAXR, class P>
+__device__ __forceinline__ void transposed_unit(const P &p, uint32_t u, uint32_t W) {
+    const uint32_t R = (uint32_t)p.R;
+    const uint32_t blk = u / W, k = u - blk * W;
+    const uint32_t s = blk / R, d = blk - s * R;
+    const char *sb = nullptr;
+    char *db = nullptr;
+#pragma unroll
+    for (int j = 0; j < MAXR; ++j) {
+        if ((uint32_t)j == s) sb = static_cast<const char *>(p.src[j]);
+        if ((uint32_t)j == d) db = static_cast<char *>(p.dst[j]);
+    }
+    atom::st_v4(db + ((uint64_t)s * W + k) * 16u, atom::ld_v4(sb + ((uint64_t)d * W + k) * 16u));
+}
+
 template <int DT, int MAXR, bool RING, class P>
 __device__ void do_unit(const P &p, const Seg &sg, uint64_t k) {
     using V = atom::Vec<DT>;

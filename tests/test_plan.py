@@ -328,3 +328,34 @@ def test_aliasing_rules():
     same = [outs[0]] * 4
     assert _call("all_reduce", 4, n, None, src=same,
                  dst=fake_ptrs([n * es] * 4, base=0x7d0000000000)) == P.PURLIN_OK
+
+
+@pytest.mark.parametrize("R", [2, 3, 8])
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_alltoall_units_follow_the_transposition(R, dtype):
+    """The vector kernel's build for a uniform AllToAll of whole windows reads
+    no segment table: it sends unit u, window k = u % W of block u // W =
+    s*R + d, from offset (d*W + k)*16 of source s to offset (s*W + k)*16 of
+    destination d ("Purlin: Separating Orchestration from the Datapath of
+    Collectives" §3.1: AllToAll is the scattered -> transposed layout).  The
+    compiled plan numbers its units exactly that way, so both agree on every
+    unit; a block that is not a whole number of windows has no such plan."""
+    es = ES[dtype]
+    for M in (16 // es, 64 // es * 3, 512):   # elements per block: whole windows
+        n = R * M
+        st, segs, _, nunits = inspect("all_to_all", R, n, None, dtype, 1)
+        assert st == P.PURLIN_OK
+        W = M * es // 16
+        assert nunits == R * R * W and len(segs) == R * R
+        for u in range(nunits):
+            blk, k = divmod(u, W)
+            s, d = divmod(blk, R)
+            g = segs[blk]
+            assert (g["src_rank"], g["dst_rank"]) == (s, d)
+            assert g["unit_begin"] + k == u
+            assert g["src_off"] + 16 * k == (d * W + k) * 16
+            assert g["dst_off"] + 16 * k == (s * W + k) * 16
+    # a ragged block (not a multiple of 16 bytes) is cut differently
+    M = 16 // es + 1
+    st, segs, _, nunits = inspect("all_to_all", R, R * M, None, dtype, 1)
+    assert st == P.PURLIN_OK and nunits != R * R * (M * es // 16)
