@@ -879,8 +879,6 @@ def sweep(args):
         algo = 2 * 8 * n * 2
         reps = 200 if n <= (1 << 20) else 30
         for variant, mode in ((1, 0), (2, 1), (2, 2), (0, 3), (0, 0)):
-            if variant == 1 and n > (16 << 20):
-                continue
             if mode == 3 and 2 * n > (1 << 20):   # packets: up to 1 MiB per rank
                 continue
             setopt(variant, mode)

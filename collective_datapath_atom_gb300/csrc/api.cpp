@@ -37,21 +37,24 @@ Policy policy_for(purlin_collective coll, int R) {
         return (uint32_t)(std::min(hi, std::max(lo, v)) & ~uint64_t(15));
     };
     // Crossovers: the largest per-rank input the vector kernel wins at,
-    // measured with each variant forced (host.h).
+    // measured with each variant forced (host.h).  kVectorAlways: it won at
+    // every size measured, up to 256 MiB per rank.
     switch (coll) {
         case PURLIN_COLL_REDUCE_SCATTER:
-            return {clamp16(98304 / (uint64_t)R, 1024, 16384), 2, 48ull << 20, false, 0, 1};
+            return {clamp16(98304 / (uint64_t)R, 1024, 16384), 2, kVectorAlways, false, 0, 1};
         case PURLIN_COLL_REDUCE_SCATTER_V:   // both paths read ragged blocks aligned
-            return {clamp16(98304 / (uint64_t)R, 1024, 16384), 2, 24ull << 20, false, 0, 1};
+            return {clamp16(98304 / (uint64_t)R, 1024, 16384), 2, kVectorAlways, false, 0, 1};
         case PURLIN_COLL_ALL_REDUCE:
             // (composed mode: the gather chunks are stored by the consumer warps)
-            return {clamp16(32768 / (uint64_t)R, 512, 8192), 4, 16ull << 20, true, 0, 1};
+            return {clamp16(32768 / (uint64_t)R, 512, 8192), 4, kVectorAlways, true, 0, 1};
         case PURLIN_COLL_ALL_GATHER:
-            return {16384, 2, 2ull << 20, true, 8, 1};
-        case PURLIN_COLL_ALL_GATHER_V:   // a Zipf split's largest input is 1.18x the mean
-            return {16384, 2, 3ull << 20, true, 8, 1};
-        default:   // AllToAll(V): two CTAs per SM
-            return {16384, 3, 256ull << 10, false, 0, 2};
+            return {16384, 2, kVectorAlways, true, 8, 1};
+        case PURLIN_COLL_ALL_GATHER_V:
+            return {16384, 2, kVectorAlways, true, 8, 1};
+        case PURLIN_COLL_ALL_TO_ALL:   // two CTAs per SM
+            return {16384, 3, 2ull << 20, false, 0, 2};
+        default:   // AllToAllV: two CTAs per SM
+            return {16384, 3, 512ull << 10, false, 0, 2};
     }
 }
 
@@ -158,6 +161,7 @@ constexpr size_t kPlanCacheCap = 64;
 // Built-in policy.
 constexpr int64_t kInspectChunkBytes = 32 * 1024;        // plan_inspect default chunk
 constexpr int kLatBlock = 256;
+constexpr int64_t kMaxLatGrid = 1 << 24;   // CTAs of a vector-kernel launch
 // Small plans whose every unit stores to all R ranks: see the latency launch.
 constexpr uint64_t kSpreadUnits = 16384;
 constexpr uint64_t kSpreadCtas = 16;
@@ -356,8 +360,13 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
     uint64_t epoch_inc = 1;
     cudaError_t ce;
     if (variant == kVariantLatency) {
+        // One unit a thread: the block scheduler hands out the CTAs as SMs
+        // free up, which balances the tail better than a persistent grid of 4
+        // CTAs per SM looping over the units (6-11% faster for AllGather at 1-8
+        // MiB per rank, 5% for AllReduce at 16-32 MiB); the loop only covers
+        // plans past kMaxLatGrid CTAs.
         const int64_t cap = ctx->opt[PURLIN_OPT_LAT_CTAS] > 0 ? ctx->opt[PURLIN_OPT_LAT_CTAS]
-                                                              : 4 * (int64_t)ctx->sms;
+                                                              : kMaxLatGrid;
         const int max_block = ctx->opt[PURLIN_OPT_LAT_BLOCK] > 0
                                   ? (int)ctx->opt[PURLIN_OPT_LAT_BLOCK] : kLatBlock;
         int block = (int)std::min<uint64_t>(max_block, (pl.nunits + 31) / 32 * 32);

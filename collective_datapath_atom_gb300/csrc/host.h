@@ -27,14 +27,16 @@ constexpr int kShiftedCopyConsumerWarps = 6;
 // MiB per rank and at the workloads' sizes.
 // Crossover: per-rank message bytes up to which the one-shot vector kernel
 // beats the staged ring (both forced, single launches and graph replays
-// with the L2 flushed, 256 KiB..64 MiB per rank at R = 8).  At 64 registers
-// it runs four CTAs of 256 threads per SM, which keeps enough loads in
-// flight that for reductions it wins up to tens of MiB: ReduceScatter 48 MiB
-// (its whole-window build leads the ring by 2.6% there and ties it at 64
-// MiB), ReduceScatterV 24 MiB (ragged blocks take the general build; at 32
-// MiB the ring leads by 3.5%), AllReduce 16 MiB (the two tie at 24 MiB, the
-// ring leads from 32 MiB), AllGather 2 MiB (they tie at 3 MiB), AllGatherV
-// 3 MiB (its largest input), AllToAll(V) 256 KiB.
+// with the L2 flushed, 256 KiB..256 MiB per rank at R = 8, confirmed on a
+// second box).  With one 16-byte window a thread and as many CTAs as that
+// takes, the vector kernel won at every size for AllGather(V), AllReduce
+// and ReduceScatter(V): at 256 MiB per rank AllReduce 628.7 against 657.4
+// us, ReduceScatter 350.2 against 367.6 us; AllGather at 128 MiB 1433.6
+// against 1540.8 us (kVectorAlways).  AllToAll 2 MiB (13.9 against 14.8 us
+// there; the ring leads at 4 MiB in a graph), AllToAllV 512 KiB (the ring
+// leads from 1 MiB).  The composed AllReduce has its own (api.cpp), and so
+// do the device-count calls, whose vector path runs inside the ring's grid
+// (vcounts_api.cpp).
 // Ring shape:
 //   ReduceScatter(V)  one destination per reduced chunk: large per-source
 //                     chunks (96 KiB per stage), 2 stages;
@@ -49,6 +51,8 @@ constexpr int kShiftedCopyConsumerWarps = 6;
 //                     0.6% faster;
 //   AllToAll(V)       one load, one store per chunk: 16 KiB chunks, 3 stages,
 //                     bulk stores (0.98).
+constexpr uint64_t kVectorAlways = ~0ull;   // crossover: the vector kernel at every size
+
 struct Policy {
     uint32_t chunk;         // bytes per source per chunk
     uint32_t stages;

@@ -15,6 +15,20 @@ using namespace purlin::host;
 
 namespace {
 
+// Per-rank input bytes up to which the device-count kernel takes its vector
+// path.  That path runs inside the ring's grid (one or two CTAs per SM,
+// looping over the units), not as the host calls' vector kernel with a CTA
+// for every 256 units, so it keeps the crossovers measured for a vector
+// kernel of that size: AllGatherV 3 MiB, ReduceScatterV 24 MiB, AllToAllV
+// 256 KiB.
+uint64_t device_count_crossover(purlin_collective coll) {
+    switch (coll) {
+        case PURLIN_COLL_ALL_GATHER_V: return 3ull << 20;
+        case PURLIN_COLL_REDUCE_SCATTER_V: return 24ull << 20;
+        default: return 256ull << 10;
+    }
+}
+
 // A V collective whose counts are in device memory (vcounts.cu): the host
 // checks what it can (shape, pointers, the declared capacities' overlaps)
 // and sizes the ring for the worst case of any counts; the kernel derives
@@ -80,7 +94,7 @@ purlin_status run_vcounts(purlin_ctx *ctx, purlin_collective coll, const void *c
                   : variant == kVariantThroughput ? 0ull
                   : ctx->opt[PURLIN_OPT_CROSSOVER_BYTES] > 0
                       ? (uint64_t)ctx->opt[PURLIN_OPT_CROSSOVER_BYTES]
-                      : shape.crossover;
+                      : device_count_crossover(coll);
     a.timeout_ns = ctx->opt[PURLIN_OPT_SPIN_TIMEOUT_NS] > 0 ? ctx->opt[PURLIN_OPT_SPIN_TIMEOUT_NS]
                                                             : kDefaultTimeoutNs;
     a.red_chunk = chunk;

@@ -510,32 +510,46 @@ def test_cfg_allreduce_f32_exact(P, ctx8):
 
 
 def test_cfg_allgather_bf16_full(P, ctx8):
+    """The default variant (the vector kernel) and the ring, each in full."""
     w = workloads.AG_BF16_R8_8MI
     ins = workloads.inputs_for(w)
     src = _device(ins)
-    dst = [torch.empty(8 * w.n, dtype=torch.int16, device="cuda") for _ in range(8)]
-    P.purlin_all_gather(ctx8, src, dst, w.n, 1)
-    P.purlin_check(ctx8)
-    assert P.purlin_last_launch(ctx8)["variant"] == 2
     want = torch.from_numpy(np.concatenate(ins).view(np.int16)).cuda()   # concatenation invariant
-    for d in range(8):
-        assert torch.equal(dst[d], want)
-    del want
-    for d, o in enumerate(oracle.all_gather(ins, 1)):   # and the oracle, in full
-        assert torch.equal(dst[d], torch.from_numpy(o.view(np.int16)).cuda()), f"rank {d}"
+    oracle_out = [torch.from_numpy(o.view(np.int16)).cuda() for o in oracle.all_gather(ins, 1)]
+    try:
+        for variant, ran in ((0, 1), (2, 2)):
+            P.purlin_set_option(ctx8, P.PURLIN_OPT_VARIANT, variant)
+            dst = [torch.full((8 * w.n,), -1, dtype=torch.int16, device="cuda") for _ in range(8)]
+            P.purlin_all_gather(ctx8, src, dst, w.n, 1)
+            P.purlin_check(ctx8)
+            assert P.purlin_last_launch(ctx8)["variant"] == ran
+            for d in range(8):
+                assert torch.equal(dst[d], want)
+                assert torch.equal(dst[d], oracle_out[d]), f"variant {ran} rank {d}"   # the oracle, in full
+            del dst
+    finally:
+        P.purlin_set_option(ctx8, P.PURLIN_OPT_VARIANT, 0)
 
 
 def test_cfg_reducescatter_bf16_full(P, ctx8):
+    """The default variant (the vector kernel) and the ring, each in full."""
     w = workloads.RS_BF16_R8_128MI
     ins = workloads.inputs_for(w)
     src = _device(ins)
     M = w.n // 8
-    dst = [torch.empty(M, dtype=torch.int16, device="cuda") for _ in range(8)]
-    P.purlin_reduce_scatter(ctx8, src, dst, w.n, 1)
-    P.purlin_check(ctx8)
     want = oracle.reduce_scatter(ins, 1)
-    for r in range(8):
-        assert np.array_equal(dst[r].cpu().numpy().view(np.uint16), want[r])
+    try:
+        for variant, ran in ((0, 1), (2, 2)):
+            P.purlin_set_option(ctx8, P.PURLIN_OPT_VARIANT, variant)
+            dst = [torch.full((M,), -1, dtype=torch.int16, device="cuda") for _ in range(8)]
+            P.purlin_reduce_scatter(ctx8, src, dst, w.n, 1)
+            P.purlin_check(ctx8)
+            assert P.purlin_last_launch(ctx8)["variant"] == ran
+            for r in range(8):
+                assert np.array_equal(dst[r].cpu().numpy().view(np.uint16), want[r]), \
+                    f"variant {ran} rank {r}"
+    finally:
+        P.purlin_set_option(ctx8, P.PURLIN_OPT_VARIANT, 0)
 
 
 def test_cfg_alltoallv_moe_full(P, ctx8):
@@ -553,18 +567,28 @@ def test_cfg_alltoallv_moe_full(P, ctx8):
 
 @pytest.mark.parametrize("batch", workloads.AR_BF16_SWEEP_BATCHES)
 def test_cfg_allreduce_sweep(P, ctx8, batch):
+    """Every size with the default variant (the vector kernel); from 4 MiB
+    per rank also with the fused ring."""
     w = workloads.ar_sweep_workload(batch)
     ins = workloads.inputs_for(w)
     src = _device(ins)
-    dst = [torch.empty(w.n, dtype=torch.int16, device="cuda") for _ in range(8)]
-    P.purlin_all_reduce(ctx8, src, dst, w.n, 1)
-    P.purlin_check(ctx8)
     # every output against the oracle's, element by element
     want = torch.from_numpy(oracle.all_reduce_one(ins, 1).view(np.int16)).cuda()
-    for d in range(8):
-        if not torch.equal(dst[d], want):
-            bad = torch.nonzero(dst[d] != want)[0].item()
-            raise AssertionError(f"batch {batch}: rank {d} differs first at element {bad}")
+    try:
+        for variant in ((0, 2) if batch >= 512 else (0,)):
+            P.purlin_set_option(ctx8, P.PURLIN_OPT_VARIANT, variant)
+            dst = [torch.full((w.n,), -1, dtype=torch.int16, device="cuda") for _ in range(8)]
+            P.purlin_all_reduce(ctx8, src, dst, w.n, 1)
+            P.purlin_check(ctx8)
+            assert P.purlin_last_launch(ctx8)["variant"] == (1 if variant == 0 else 2)
+            for d in range(8):
+                if not torch.equal(dst[d], want):
+                    bad = torch.nonzero(dst[d] != want)[0].item()
+                    raise AssertionError(f"batch {batch} variant {variant}: rank {d} differs "
+                                         f"first at element {bad}")
+            del dst
+    finally:
+        P.purlin_set_option(ctx8, P.PURLIN_OPT_VARIANT, 0)
 
 
 # --------------------------------------------------------------- wide R ----
