@@ -5,10 +5,12 @@
 // §2.1: prefill payloads are throughput-bound and decode messages
 // latency-bound, and a high-bandwidth path's setup dominates small messages.
 // §3.2: push for latency, pull for bandwidth.  On one GPU these become the
-// vector kernel and the staged ring.
+// vector kernel and the staged ring; measured on GB300 the vector kernel,
+// one window a thread and a CTA per 256 windows, also wins at every size for
+// AllGather(V), AllReduce and ReduceScatter(V) (the host's policy).
 //
-// Latency kernel: one thread per 16-byte window ("unit"); no flags, since
-//   every output has one owner.
+// Latency (vector) kernel: one thread per 16-byte window ("unit"); no flags,
+//   since every output has one owner.
 // Throughput kernel: persistent CTAs running the ring (snac::run_ring) over
 //   the launch's whole grid (ring_kernel.cuh); this unit builds it for
 //   plans whose ring chunks share their destination's 16-byte phase, and
@@ -27,8 +29,10 @@ using ringk::fill_params;
 
 // ---------------------------------------------------------- latency kernel --
 
-// Four CTAs of 256 threads per SM (the host's grid cap) leave 64 registers
-// a thread; the instantiations for more than 8 ranks take two.  WHOLE: a
+// Launch bounds of four CTAs of 256 threads per SM leave 64 registers a
+// thread; the instantiations for more than 8 ranks take two (the whole-window
+// copy builds use 30 and fit eight).  The host launches a CTA per 256 units,
+// so the loop below normally runs once a thread.  WHOLE: a
 // build for plans whose segments are all made of whole aligned 16-byte
 // windows and all copies (1) or all reductions (2) (Plan::whole_op), with
 // only the short unit path for that operation (whole_unit); 3, a uniform

@@ -38,7 +38,7 @@ enum SyncKind : uint8_t {
 
 enum Variant : int {
     kVariantNone = 0,
-    kVariantLatency = 1,     // one-shot 128-bit vector loads/stores, few CTAs
+    kVariantLatency = 1,     // one-shot 128-bit vector loads/stores, a CTA per 256 windows
     kVariantThroughput = 2,  // persistent CTAs, cp.async.bulk shared-memory ring
 };
 

@@ -11,8 +11,12 @@
  * published (an mbarrier inside a CTA, or a release-store to a per-chunk
  * flag in global memory between CTAs) and consumers copy or reduce them
  * (§3.2, Stage / Notify / And Consume); the datapath ("Atom", §3.3) is a
- * 128-bit vector load/store path for small messages and a cp.async.bulk
- * (TMA) multi-stage shared-memory ring for large ones.
+ * 128-bit vector load/store kernel (one 16-byte window a thread) and a
+ * cp.async.bulk (TMA) multi-stage shared-memory ring.  Which one runs is
+ * chosen per collective and message size from GB300 measurements: the vector
+ * kernel for AllGather(V), AllReduce and ReduceScatter(V) at every size and
+ * for small AllToAll(V), the ring for larger AllToAll(V) and the composed
+ * AllReduce (PURLIN_OPT_VARIANT overrides the choice).
  *
  * Reductions (SCORE, §3.3): every output element is owned by one thread,
  * which adds the R sources in rank order 0..R-1 in binary32, starting from
