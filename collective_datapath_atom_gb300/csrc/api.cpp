@@ -365,8 +365,9 @@ purlin_status run(purlin_ctx *ctx, const CallDesc &c, const void *const src[], v
         // CTAs per SM looping over the units (6-11% faster for AllGather at 1-8
         // MiB per rank, 5% for AllReduce at 16-32 MiB); the loop only covers
         // plans past kMaxLatGrid CTAs.
-        const int64_t cap = ctx->opt[PURLIN_OPT_LAT_CTAS] > 0 ? ctx->opt[PURLIN_OPT_LAT_CTAS]
-                                                              : kMaxLatGrid;
+        const int64_t cap = ctx->opt[PURLIN_OPT_LAT_CTAS] > 0
+                                ? std::min<int64_t>(ctx->opt[PURLIN_OPT_LAT_CTAS], kMaxLatGrid)
+                                : kMaxLatGrid;
         const int max_block = ctx->opt[PURLIN_OPT_LAT_BLOCK] > 0
                                   ? (int)ctx->opt[PURLIN_OPT_LAT_BLOCK] : kLatBlock;
         int block = (int)std::min<uint64_t>(max_block, (pl.nunits + 31) / 32 * 32);

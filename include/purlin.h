@@ -303,7 +303,7 @@ typedef enum {
     PURLIN_OPT_CTAS = 5,             /* CTAs of a throughput launch (0: the policy's; at most what fits at once) */
     PURLIN_OPT_SPIN_TIMEOUT_NS = 6,  /* bound on a cross-CTA flag wait (default 100 ms) */
     PURLIN_OPT_DROP_NOTIFY = 7,      /* host-side fault injection: chunk whose notify is skipped; -1 off */
-    PURLIN_OPT_LAT_CTAS = 8,         /* max CTAs of a latency launch */
+    PURLIN_OPT_LAT_CTAS = 8,         /* max CTAs of a latency launch (0: a CTA per block of units, up to 2^24) */
     PURLIN_OPT_LAT_BLOCK = 9,        /* threads per CTA of a latency launch (32..256, multiple of 32) */
     PURLIN_OPT_CONSUMER_WARPS = 10,  /* consumer warps of a throughput CTA (1..14) */
     PURLIN_OPT_COPY_STORES = 11      /* aligned copies in the ring: 0 auto, 1 bulk stores (TMA), 2 vector stores */
